@@ -1,0 +1,67 @@
+/*
+ * CPU oracle for GDN / KDA ReplaySSM decode.  TEST INFRASTRUCTURE ONLY: the
+ * product library never includes this header or links this code.
+ *
+ * Every array is double and row-major.  Shapes (N slots, HV value heads, HK key
+ * heads, K key dim, V value dim, L ring length, B batch rows):
+ *   state      [N][HV][V][K]     checkpoint S0 (values held at the state type)
+ *   ring_d     [N][HV][L][V]     cached corrections d
+ *   ring_k     [N][HK][L][K]     cached keys, shared by the value heads of a group
+ *   ring_g     [N][HV][L]        GDN log-gates   ([N][HV][L][K] for KDA)
+ *   write_pos  [N]               valid ring entries = next write index
+ *   mixed_qkv  [B][2*HK*K+HV*V]  q | k | v
+ *   g          [B][HV]           GDN log-gate    ([B][HV][K] for KDA)
+ *   beta       [B][HV]
+ *   o          [B][HV][V]
+ */
+#ifndef GDN_ORACLE_H
+#define GDN_ORACLE_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_F64 = 0, ORACLE_F32 = 1, ORACLE_F16 = 2, ORACLE_BF16 = 3 };
+enum { ORACLE_GATE_SCALAR = 0, ORACLE_GATE_PER_K = 1 };
+enum { ORACLE_BAD_SLOT = 1u, ORACLE_BAD_WRITE_POS = 2u };
+
+typedef struct {
+    int N, HV, HK, K, V, L;
+    int gate;         /* ORACLE_GATE_SCALAR (GDN) or ORACLE_GATE_PER_K (KDA) */
+    int state_dtype;  /* storage rounding of the checkpoint                  */
+    int ring_dtype;   /* storage rounding of ring d and k (g is never rounded) */
+} oracle_geom;
+
+double oracle_round(double x, int dtype);
+void oracle_round_array(double *x, long n, int dtype);
+
+void oracle_gdn_step(int K, int V, double *S, const double *q, const double *k,
+                     const double *v, double g, double beta, double *y, double *u);
+void oracle_kda_step(int K, int V, double *S, const double *q, const double *k,
+                     const double *v, const double *g, double beta, double *y, double *u);
+
+int oracle_packed_decode(const oracle_geom *G, double *state, int B, const int *indices,
+                         const double *mixed_qkv, const double *g, const double *beta,
+                         double q_scale, int qk_l2norm, double *o, unsigned *status);
+
+void oracle_replay_state(const oracle_geom *G, const double *state, const double *ring_d,
+                         const double *ring_k, const double *ring_g, int slot, int hv, int p,
+                         double *S);
+
+int oracle_replay_decode(const oracle_geom *G, double *state, double *ring_d, double *ring_k,
+                         double *ring_g, const int *write_pos, int B, const int *indices,
+                         const unsigned char *force_flush, const double *mixed_qkv,
+                         const double *g, const double *beta, double q_scale, int qk_l2norm,
+                         double *o, unsigned char *flushed, unsigned *status);
+
+int oracle_replay_advance(int N, int B, const int *indices, const unsigned char *force_flush,
+                          int L, int *write_pos, unsigned *status);
+
+int oracle_replay_fold(const oracle_geom *G, double *state, const double *ring_d,
+                       const double *ring_k, const double *ring_g, const int *write_pos,
+                       int n, const int *slots, unsigned *status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,446 @@
+"""Pins of the CPU oracle.
+
+Each pin checks the oracle against something other than itself: a value the
+pages print (the L = 4 cursor table), a closed form, an invariant of the
+recurrence, a reduction to a simpler case, or a library routine (numpy / torch
+float conversion).  A pin is a plain function that raises AssertionError on a
+mismatch.  test_oracle_pins runs them all; test_oracle_mutations plants
+mistakes in copies of the oracle source and checks that each is caught.
+
+Page references (title, section):
+  sglang #28451 "ReplaySSM decode": Modifications; Design 1, 3, 5, 7.
+  "ReplaySSM" explainer (llm.rainlin.net): 1, 2.1, 2.2, 3.1, 3.3.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed: int) -> np.random.Generator:
+    return np.random.default_rng(seed)
+
+
+def _unit(x: np.ndarray) -> np.ndarray:
+    return x / np.linalg.norm(x)
+
+
+def _close(a, b, tol, what):
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    scale = max(1.0, float(np.max(np.abs(b))) if b.size else 0.0)
+    assert a.shape == b.shape and err <= tol * scale, f"{what}: max err {err:.3e} (tol {tol:.1e})"
+
+
+# ---------------------------------------------------------------------------
+# Storage rounding against library conversions.
+# ---------------------------------------------------------------------------
+
+def pin_round_f16_f32_match_numpy():
+    r = _rng(0)
+    x = r.standard_normal(4000) * 10.0 ** r.integers(-9, 6, 4000)
+    special = [2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -25, 2.0 ** -14, 65504.0, 65519.99, 65520.0,
+               1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 1 + 2.0 ** -24, 1 + 3 * 2.0 ** -24, -0.0, 1e-30,
+               -5.96e-8, 1e39]
+    x = np.concatenate([x, special, -np.asarray(special)])
+    with np.errstate(over="ignore"):
+        for dt, npdt in ((O.F16, np.float16), (O.F32, np.float32)):
+            want = x.astype(npdt).astype(np.float64)
+            got = O.round_to(x, dt)
+            assert np.array_equal(got, want), f"rounding to {npdt.__name__} differs from numpy"
+
+
+def pin_round_bf16_matches_torch():
+    r = _rng(1)
+    x32 = (r.standard_normal(4000) * 10.0 ** r.integers(-40, 38, 4000)).astype(np.float32)
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 2.0 ** -133, 3 * 2.0 ** -134], dtype=np.float32)
+    x32 = np.concatenate([x32, ties, -ties])
+    want = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_to(x32.astype(np.float64), O.BF16)
+    assert np.array_equal(got, want), "rounding to bf16 differs from torch"
+
+
+# ---------------------------------------------------------------------------
+# The sequential recurrence (explainer section 1; #28451 Design 7).
+# K != V everywhere so a transposed operand cannot pass.
+# ---------------------------------------------------------------------------
+
+K5, V3 = 5, 3
+
+
+def pin_gdn_retrieval():
+    """beta = 1, |k| = 1: the new state maps k to v exactly, and y = S_t k = v."""
+    r = _rng(2)
+    S = r.standard_normal((V3, K5))
+    k = _unit(r.standard_normal(K5))
+    v = r.standard_normal(V3)
+    y, _ = O.gdn_step(S, k, k, v, -0.7, 1.0)
+    _close(S @ k, v, 1e-13, "S_t k")
+    _close(y, v, 1e-13, "y with q = k")
+
+
+def pin_gdn_decay_only():
+    """beta = 0: S_t = exp(g) S, y = exp(g) S q, no correction."""
+    r = _rng(3)
+    S0 = r.standard_normal((V3, K5))
+    S = S0.copy()
+    q, k, v = r.standard_normal(K5), r.standard_normal(K5), r.standard_normal(V3)
+    y, u = O.gdn_step(S, q, k, v, -0.3, 0.0)
+    _close(S, np.exp(-0.3) * S0, 1e-15, "decayed state")
+    _close(y, np.exp(-0.3) * (S0 @ q), 1e-14, "decayed output")
+    assert np.all(u == 0.0)
+
+
+def pin_gdn_identity_step():
+    """beta = 0 and g = 0 leave the state bit-identical; y = S q."""
+    r = _rng(4)
+    S0 = r.standard_normal((V3, K5))
+    S = S0.copy()
+    q = r.standard_normal(K5)
+    y, _ = O.gdn_step(S, q, r.standard_normal(K5), r.standard_normal(V3), 0.0, 0.0)
+    assert np.array_equal(S, S0)
+    _close(y, S0 @ q, 1e-14, "y")
+
+
+def pin_gdn_other_directions_only_decay():
+    """beta = 1, |k| = 1: a direction x orthogonal to k sees only the decay."""
+    r = _rng(5)
+    S0 = r.standard_normal((V3, K5))
+    S = S0.copy()
+    k = _unit(r.standard_normal(K5))
+    x = r.standard_normal(K5)
+    x -= (x @ k) * k
+    O.gdn_step(S, r.standard_normal(K5), k, r.standard_normal(V3), -0.4, 1.0)
+    _close(S @ x, np.exp(-0.4) * (S0 @ x), 1e-13, "S_t x")
+
+
+def pin_gdn_erase_history():
+    """g = -1e4 underflows alpha to 0: S_t = beta v k^T, y = beta v (k^T q)."""
+    r = _rng(6)
+    S = r.standard_normal((V3, K5))
+    q, k, v = r.standard_normal(K5), r.standard_normal(K5), r.standard_normal(V3)
+    y, u = O.gdn_step(S, q, k, v, -1e4, 0.6)
+    _close(S, 0.6 * np.outer(v, k), 1e-15, "state")
+    _close(y, 0.6 * v * (k @ q), 1e-14, "y")
+    _close(u, 0.6 * v, 1e-15, "u")
+
+
+def pin_gdn_correction_vanishes_when_retrieved():
+    """If v already equals the decayed retrieval exp(g) S k, the correction u is 0."""
+    r = _rng(7)
+    S0 = r.standard_normal((V3, K5))
+    k, q = r.standard_normal(K5), r.standard_normal(K5)
+    v = np.exp(-0.2) * (S0 @ k)
+    S = S0.copy()
+    y, u = O.gdn_step(S, q, k, v, -0.2, 0.9)
+    _close(u, np.zeros(V3), 1e-14, "u")
+    _close(S, np.exp(-0.2) * S0, 1e-14, "state")
+
+
+def pin_kda_equal_channels_is_gdn():
+    """A per-channel gate with every channel equal reduces KDA to GDN."""
+    r = _rng(8)
+    S0 = r.standard_normal((V3, K5))
+    q, k, v = r.standard_normal(K5), r.standard_normal(K5), r.standard_normal(V3)
+    Sa, Sb = S0.copy(), S0.copy()
+    ya, ua = O.gdn_step(Sa, q, k, v, -0.45, 0.7)
+    yb, ub = O.kda_step(Sb, q, k, v, np.full(K5, -0.45), 0.7)
+    _close(Sb, Sa, 1e-14, "state")
+    _close(yb, ya, 1e-14, "y")
+
+
+def pin_kda_decay_is_per_key_column():
+    """KDA with beta = 0: column c of the state (key channel c) decays by exp(g[c])."""
+    r = _rng(9)
+    S0 = r.standard_normal((V3, K5))
+    g = -r.random(K5)
+    q = r.standard_normal(K5)
+    S = S0.copy()
+    y, _ = O.kda_step(S, q, r.standard_normal(K5), r.standard_normal(V3), g, 0.0)
+    _close(S, S0 * np.exp(g)[None, :], 1e-15, "state")
+    _close(y, S0 @ (np.exp(g) * q), 1e-14, "y")
+
+
+def pin_kda_retrieval():
+    r = _rng(10)
+    S = r.standard_normal((V3, K5))
+    k = _unit(r.standard_normal(K5))
+    v = r.standard_normal(V3)
+    y, _ = O.kda_step(S, k, k, v, -r.random(K5), 1.0)
+    _close(S @ k, v, 1e-13, "S_t k")
+    _close(y, v, 1e-13, "y")
+
+
+# ---------------------------------------------------------------------------
+# The replay state machine (explainer 2.1, 3.1-3.3; #28451 Design 1/3/5/7).
+# ---------------------------------------------------------------------------
+
+def _packed_row(q_heads, k_heads, v_heads):
+    return np.concatenate([np.ravel(q_heads), np.ravel(k_heads), np.ravel(v_heads)])
+
+
+class _Seq:
+    """Random per-step inputs for one slot; HV value heads sharing HK key heads."""
+
+    def __init__(self, seed, steps, HV, HK, K, V, gate):
+        r = _rng(seed)
+        self.q = np.stack([[_unit(r.standard_normal(K)) / np.sqrt(K) for _ in range(HK)] for _ in range(steps)])
+        self.k = np.stack([[_unit(r.standard_normal(K)) for _ in range(HK)] for _ in range(steps)])
+        self.v = r.standard_normal((steps, HV, V))
+        self.g = -np.log1p(np.exp(r.standard_normal((steps, HV, K) if gate else (steps, HV))))
+        self.beta = 1 / (1 + np.exp(-r.standard_normal((steps, HV))))
+        self.HV, self.HK = HV, HK
+
+    def row(self, t):
+        return _packed_row(self.q[t], self.k[t], self.v[t])[None, :]
+
+
+def _run_replay(G, S0, seq, steps, force=None, slot=0, fold_at=None):
+    """Drives the oracle's replay decode over `steps` tokens for one slot.
+    Returns per-step outputs, flushed flags, write_pos before each step, caches."""
+    N, HV, HK, K, V, L = G.N, G.HV, G.HK, G.K, G.V, G.L
+    gk = (K,) if G.gate == O.GATE_PER_K else ()
+    cache = O.Cache(np.zeros((N, HV, V, K)), np.full((N, HV, L, V), np.nan),
+                    np.full((N, HK, L, K), np.nan), np.full((N, HV, L) + gk, np.nan))
+    cache.state[slot] = S0
+    wp = np.zeros(N, dtype=np.int32)
+    outs, flags, cursors = [], [], []
+    for t in range(steps):
+        if fold_at is not None and t == fold_at:
+            assert O.replay_fold(G, cache, wp, [slot]) == 0
+            wp[slot] = 0
+        ff = None if force is None else np.array([force[t]], dtype=np.uint8)
+        cursors.append(int(wp[slot]))
+        o, fl, st = O.replay_decode(G, cache, wp, [slot], ff, seq.row(t), seq.g[t][None], seq.beta[t][None])
+        assert st == 0
+        assert O.replay_advance(N, [slot], ff, L, wp) == 0
+        outs.append(o[0])
+        flags.append(int(fl[0]))
+    return np.array(outs), flags, cursors, cache, wp
+
+
+def _run_sequential(S0, seq, steps, gate):
+    """O1 per value head from the same checkpoint."""
+    HV, HK = seq.HV, seq.HK
+    S = [S0[h].copy() for h in range(HV)]
+    ys, us = [], []
+    for t in range(steps):
+        yt, ut = [], []
+        for h in range(HV):
+            hk = h // (HV // HK)
+            fn = O.kda_step if gate else O.gdn_step
+            y, u = fn(S[h], seq.q[t][hk], seq.k[t][hk], seq.v[t][h], seq.g[t][h], seq.beta[t][h])
+            yt.append(y)
+            ut.append(u)
+        ys.append(yt)
+        us.append(ut)
+    return np.array(ys), np.array(us), np.array(S)
+
+
+def _replay_matches_sequential(gate):
+    HV, HK, K, V, L, steps = 4, 2, K5, V3, 8, 19
+    G = O.geom(2, HV, HK, K, V, L, gate=gate, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(20 + gate)
+    S0 = r.standard_normal((HV, V, K)) * 0.3
+    seq = _Seq(30 + gate, steps, HV, HK, K, V, gate)
+    outs, flags, cursors, cache, wp = _run_replay(G, S0, seq, steps, slot=1)
+    ys, us, S_seq = _run_sequential(S0, seq, steps, gate)
+    _close(outs, ys, 1e-12, "replay outputs vs the sequential recurrence")
+    # natural flush every L steps: cursor 0..L-1 then back to 0
+    assert cursors == [t % L for t in range(steps)]
+    assert flags == [int(t % L == L - 1) for t in range(steps)]
+    # the state rebuilt from checkpoint + ring after the last step equals S_t
+    for h in range(HV):
+        _close(O.replay_state(G, cache, 1, h, int(wp[1])), S_seq[h], 1e-12, "replayed state")
+    # the cached corrections are the recurrence's u_t for the steps since the flush
+    last_flush = max(t for t in range(steps) if flags[t])
+    for j, t in enumerate(range(last_flush + 1, steps)):
+        _close(cache.ring_d[1, :, j], us[t], 1e-12, "ring d")
+    # slot 0 was never named by a row: untouched
+    assert np.all(cache.state[0] == 0.0) and np.all(np.isnan(cache.ring_d[0]))
+
+
+def pin_replay_identity_gdn():
+    """S_{c+h} = P_h S_c + sum_j w_{j,h} u_j k_j^T matches the step-by-step recurrence."""
+    _replay_matches_sequential(O.GATE_SCALAR)
+
+
+def pin_replay_identity_kda():
+    _replay_matches_sequential(O.GATE_PER_K)
+
+
+def pin_l1_is_packed_decode():
+    """L = 1: every step flushes and the replay decode is the packed decode."""
+    HV, HK, K, V, steps = 2, 1, 4, 6, 5
+    G = O.geom(1, HV, HK, K, V, 1, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(40)
+    S0 = r.standard_normal((HV, V, K))
+    seq = _Seq(41, steps, HV, HK, K, V, 0)
+    outs, flags, cursors, cache, _ = _run_replay(G, S0, seq, steps)
+    state = S0[None].copy()
+    for t in range(steps):
+        o, st = O.packed_decode(G, state, [0], seq.row(t), seq.g[t][None], seq.beta[t][None])
+        _close(outs[t], o[0], 1e-13, f"step {t}")
+    assert flags == [1] * steps and cursors == [0] * steps
+    _close(cache.state, state, 1e-13, "checkpoint")
+
+
+def pin_walkthrough_L4():
+    """The explainer's L = 4 table (section 3.3): checkpoint before each step,
+    valid entries before each step, and the action taken."""
+    rows = []
+    with open(os.path.join(GOLDEN, "replay_walkthrough_L4.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                step, ckpt, valid, action = line.split()
+                rows.append((int(step), ckpt, [] if valid == "-" else [int(x) for x in valid.split(",")], action))
+    HV, HK, K, V, L = 1, 1, 4, 4, 4
+    G = O.geom(1, HV, HK, K, V, L, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(50)
+    S0 = r.standard_normal((HV, V, K))
+    seq = _Seq(51, len(rows), HV, HK, K, V, 0)
+    _, _, S4 = _run_sequential(S0, seq, 4, 0)
+    cache = O.Cache(S0[None].copy(), np.full((1, HV, L, V), np.nan), np.full((1, HK, L, K), np.nan),
+                    np.full((1, HV, L), np.nan))
+    wp = np.zeros(1, dtype=np.int32)
+    for step, ckpt, valid, action in rows:
+        want_ckpt = S0 if ckpt == "S0" else S4
+        _close(cache.state[0], want_ckpt, 1e-13, f"checkpoint before step {step}")
+        # the valid entries are the tokens since the last flush, numbered from 1
+        first = step - int(wp[0])
+        assert list(range(first, step)) == valid, f"valid entries before step {step}"
+        _, fl, st = O.replay_decode(G, cache, wp, [0], None, seq.row(step - 1), seq.g[step - 1][None],
+                                    seq.beta[step - 1][None])
+        assert st == 0
+        assert ("flush" if fl[0] else "append") == action, f"action at step {step}"
+        O.replay_advance(1, [0], None, L, wp)
+
+
+def pin_forced_flush_mid_ring():
+    """force_flush at a cursor below L-1 folds the valid entries and the current
+    token into the checkpoint and restarts the ring (#28451 Design 5)."""
+    HV, HK, K, V, L, steps = 2, 2, K5, V3, 6, 9
+    G = O.geom(1, HV, HK, K, V, L, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(60)
+    S0 = r.standard_normal((HV, V, K))
+    seq = _Seq(61, steps, HV, HK, K, V, 0)
+    force = [0, 0, 1, 0, 0, 0, 0, 0, 0]
+    outs, flags, cursors, cache, wp = _run_replay(G, S0, seq, steps, force=force)
+    ys, _, S_seq = _run_sequential(S0, seq, steps, 0)
+    _close(outs, ys, 1e-12, "outputs")
+    assert cursors == [0, 1, 2, 0, 1, 2, 3, 4, 5]
+    assert flags == [0, 0, 1, 0, 0, 0, 0, 0, 1]
+    _close(cache.state[0], S_seq, 1e-12, "checkpoint after the natural flush")
+
+
+def pin_fold_then_reset():
+    """Folding the ring into the checkpoint and resetting the cursor changes no output."""
+    HV, HK, K, V, L, steps = 2, 1, K5, V3, 8, 7
+    G = O.geom(1, HV, HK, K, V, L, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(70)
+    S0 = r.standard_normal((HV, V, K))
+    seq = _Seq(71, steps, HV, HK, K, V, 0)
+    outs, _, cursors, cache, _ = _run_replay(G, S0, seq, steps, fold_at=4)
+    ys, _, _ = _run_sequential(S0, seq, steps, 0)
+    _close(outs, ys, 1e-12, "outputs across a fold")
+    assert cursors == [0, 1, 2, 3, 0, 1, 2]
+    _, _, S_at4 = _run_sequential(S0, seq, 4, 0)
+    _, _, S_at7 = _run_sequential(S0, seq, 7, 0)
+    # the fold made the checkpoint the state after 4 tokens; 3 more are in the ring
+    _close(np.array([O.replay_state(G, cache, 0, h, 0) for h in range(HV)]), S_at4, 1e-12, "folded checkpoint")
+    _close(np.array([O.replay_state(G, cache, 0, h, 3) for h in range(HV)]), S_at7, 1e-12, "replayed")
+
+
+def pin_packed_layout_and_gqa():
+    """mixed_qkv = q | k | v with key head hv // (HV/HK): from a zero state one
+    step gives o = beta v_hv (k_hk . q_hk) and appends (beta v_hv, k_hk, g)."""
+    HV, HK, K, V, L = 4, 2, K5, V3, 4
+    G = O.geom(3, HV, HK, K, V, L, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(80)
+    q = r.standard_normal((HK, K))
+    k = r.standard_normal((HK, K))
+    v = r.standard_normal((HV, V))
+    g = -r.random(HV)
+    beta = r.random(HV)
+    cache = O.Cache(np.zeros((3, HV, V, K)), np.full((3, HV, L, V), np.nan), np.full((3, HK, L, K), np.nan),
+                    np.full((3, HV, L), np.nan))
+    wp = np.zeros(3, dtype=np.int32)
+    o, fl, st = O.replay_decode(G, cache, wp, [2], None, _packed_row(q, k, v)[None], g[None], beta[None])
+    assert st == 0 and fl[0] == 0
+    for h in range(HV):
+        hk = h // 2
+        _close(o[0, h], beta[h] * v[h] * (k[hk] @ q[hk]), 1e-14, f"o head {h}")
+        _close(cache.ring_d[2, h, 0], beta[h] * v[h], 1e-15, "ring d")
+        assert cache.ring_g[2, h, 0] == g[h]
+    for hk in range(HK):
+        assert np.array_equal(cache.ring_k[2, hk, 0], k[hk])
+    assert np.all(np.isnan(cache.ring_d[2, :, 1:])) and np.all(np.isnan(cache.ring_d[:2]))
+
+
+def pin_padding_and_bad_rows():
+    """Negative slots emit zeros and touch nothing; a slot >= N or a cursor
+    outside [0, L) sets a status bit and is treated as padding."""
+    HV, HK, K, V, L = 2, 1, 4, 4, 4
+    G = O.geom(2, HV, HK, K, V, L, ring_dtype=O.F16)
+    r = _rng(90)
+    cache = O.Cache(r.standard_normal((2, HV, V, K)), np.full((2, HV, L, V), np.nan),
+                    np.full((2, HK, L, K), np.nan), np.full((2, HV, L), np.nan))
+    before = cache.copy()
+    row = r.standard_normal((3, 2 * HK * K + HV * V))
+    wp = np.array([0, 7], dtype=np.int32)
+    o, fl, st = O.replay_decode(G, cache, wp, [-1, 5, 1], None, row, -r.random((3, HV)), r.random((3, HV)))
+    assert np.all(o == 0.0) and list(fl) == [0, 0, 0]
+    assert st == (O.BAD_SLOT | O.BAD_WRITE_POS)
+    for a, b in ((cache.state, before.state), (cache.ring_d, before.ring_d), (cache.ring_k, before.ring_k)):
+        assert np.array_equal(a, b, equal_nan=True)
+    wp2 = wp.copy()
+    assert O.replay_advance(2, [-1, 5, 1], None, L, wp2) == (O.BAD_SLOT | O.BAD_WRITE_POS)
+    assert np.array_equal(wp2, wp)
+
+
+def pin_storage_rounding():
+    """Ring d and k are stored at the ring type (fp16 here), g exactly, and a
+    flushed checkpoint at fp32."""
+    HV, HK, K, V, L = 2, 1, 8, 8, 2
+    G = O.geom(1, HV, HK, K, V, L, state_dtype=O.F32, ring_dtype=O.F16)
+    r = _rng(100)
+    seq = _Seq(101, 2, HV, HK, K, V, 0)
+    cache = O.Cache(O.round_to(r.standard_normal((1, HV, V, K)), O.F32), np.full((1, HV, L, V), np.nan),
+                    np.full((1, HK, L, K), np.nan), np.full((1, HV, L), np.nan))
+    wp = np.zeros(1, dtype=np.int32)
+    O.replay_decode(G, cache, wp, [0], None, seq.row(0), seq.g[0][None], seq.beta[0][None])
+    assert np.array_equal(cache.ring_k[0, 0, 0], seq.k[0][0].astype(np.float16).astype(np.float64))
+    d = cache.ring_d[0, :, 0]
+    assert np.array_equal(d, d.astype(np.float16).astype(np.float64))
+    assert np.array_equal(cache.ring_g[0, :, 0], seq.g[0])
+    O.replay_advance(1, [0], None, L, wp)
+    O.replay_decode(G, cache, wp, [0], None, seq.row(1), seq.g[1][None], seq.beta[1][None])
+    s = cache.state[0]
+    assert np.array_equal(s, s.astype(np.float32).astype(np.float64))
+
+
+def pin_superposition():
+    """With exact storage the outputs are jointly linear in (S0, v) for fixed q, k, g, beta."""
+    HV, HK, K, V, L, steps = 2, 1, K5, V3, 4, 9
+    G = O.geom(1, HV, HK, K, V, L, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(110)
+    Sa, Sb = r.standard_normal((HV, V, K)), r.standard_normal((HV, V, K))
+    sa = _Seq(111, steps, HV, HK, K, V, 0)
+    sb = _Seq(111, steps, HV, HK, K, V, 0)
+    sb.v = r.standard_normal(sb.v.shape)
+    sab = _Seq(111, steps, HV, HK, K, V, 0)
+    sab.v = sa.v + sb.v
+    oa = _run_replay(G, Sa, sa, steps)[0]
+    ob = _run_replay(G, Sb, sb, steps)[0]
+    oab = _run_replay(G, Sa + Sb, sab, steps)[0]
+    _close(oab, oa + ob, 1e-12, "superposition")
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
