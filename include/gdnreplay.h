@@ -1,0 +1,188 @@
+/*
+ * gdnreplay — Gated DeltaNet (GDN) / Kimi Delta Attention (KDA) single-token
+ * decode with the ReplaySSM checkpoint + ring cache, for one GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer in a call below is a DEVICE pointer unless its comment
+ * says otherwise.  Every buffer is owned by the caller; the library allocates
+ * no device memory and never synchronises: each call enqueues kernels on
+ * `stream` and returns.  Host-side argument checks run before any launch and
+ * return GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED with nothing enqueued; a
+ * launch failure returns GDN_ERR_CUDA.  gdn_last_error() gives the calling
+ * thread's message for its last failing call.
+ *
+ * Problems found on the device (a slot index >= num_slots, a write_pos outside
+ * [0, ring_len), a wait that ran out) are OR-ed as GDN_DEV_* bits into the
+ * optional `dev_status` word (a device uint32; NULL disables reporting).  The
+ * row is then treated as a padding row.  No kernel traps.
+ *
+ * Sources, by page title and section:
+ *  [P1] sglang pull request #28451 "ReplaySSM decode": Modifications (the GDN
+ *       decode equations), Design 1 (output-only reconstruction), Design 2
+ *       (tensor-core reconstruction), Design 3 (per-slot write_pos and its
+ *       advance rule), Design 4 (device-side flush branch), Design 5
+ *       (force_flush, write_pos reset on copy-on-write), Design 7 (KDA gate).
+ *  [P2] "ReplaySSM" explainer (llm.rainlin.net): section 1 (recurrence), 2.1
+ *       (replay identity), 2.2 (cache layout table), 3.1 (packed mixed_qkv,
+ *       ssm_state_indices, negative padding rows), 3.2 (non-flush step), 3.3
+ *       (flush step), 5.2 (KDA gate cache [N, HV, L, K]).
+ *
+ * Layouts (row-major, innermost last; N slots, HV value heads, HK key heads
+ * with HV % HK == 0, K key dim, V value dim, L ring length, B batch rows):
+ *   state      [N, HV, V, K]  fp32 checkpoint S0 ("temporal", [P2] 2.2)
+ *   ring_d     [N, HV, L, V]  ring dtype: cached corrections d
+ *   ring_k     [N, HK, L, K]  ring dtype: cached keys, shared by a key head's group
+ *   ring_g     [N, HV, L]     fp32 GDN log-gates; [N, HV, L, K] for KDA
+ *   write_pos  [N]            int32 per-slot valid count = next write index
+ *   mixed_qkv  [B, 2*HK*K + HV*V] (row stride given): q | k | v, q and k in HK
+ *              blocks of K, v in HV blocks of V; value head hv uses key head
+ *              hv / (HV/HK)
+ *   g          [B, HV] fp32 log-gate (<= 0); [B, HV, K] for KDA
+ *   beta       [B, HV] fp32
+ *   out        [B, HV, V] out dtype
+ */
+#ifndef GDNREPLAY_H
+#define GDNREPLAY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer       */
+    GDN_ERR_UNSUPPORTED = 2, /* valid but not built: K/V, dtype combination, L   */
+    GDN_ERR_CUDA = 3         /* a launch or runtime call failed                   */
+} gdn_status_t;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype_t;
+
+/* Gate granularity ([P1] Design 7): one log-gate per value head (GDN), or one
+ * per key channel of each value head (KDA). */
+typedef enum { GDN_GATE_SCALAR = 0, GDN_GATE_PER_K = 1 } gdn_gate_t;
+
+/* How the replayed state S = A S0 + sum_j w_j d_j k_j^T is evaluated.
+ * TENSOR: the L-deep sum is one small GEMM on the tensor cores (tcgen05, fp32
+ *         accumulation) — [P1] Design 2.  Operands: f16, bf16 or tf32 for an
+ *         fp16, bf16 or fp32 ring.
+ * FFMA:   every term in fp32 on the CUDA cores (slower, tighter error bound). */
+typedef enum { GDN_RECON_TENSOR = 0, GDN_RECON_FFMA = 1 } gdn_recon_t;
+
+/* dev_status bits */
+#define GDN_DEV_BAD_SLOT      1u /* ssm_state_indices[b] >= num_slots               */
+#define GDN_DEV_BAD_WRITE_POS 2u /* write_pos[slot] outside [0, ring_len)           */
+#define GDN_DEV_TIMEOUT       4u /* an on-chip wait gave up (row output is garbage) */
+#define GDN_DEV_INTERNAL      8u /* shared memory not aligned as the kernel assumes  */
+
+/* One layer's geometry.  Built: k_dim == v_dim in {64, 128}; 1 <= ring_len <= 64;
+ * state_dtype GDN_F32; ring_dtype GDN_F32, GDN_F16 or GDN_BF16. */
+typedef struct {
+    int32_t num_slots;   /* N  */
+    int32_t num_v_heads; /* HV */
+    int32_t num_k_heads; /* HK, HV % HK == 0 */
+    int32_t k_dim;       /* K  */
+    int32_t v_dim;       /* V  */
+    int32_t ring_len;    /* L >= 1 (L == 1: every step flushes, the ring is never used) */
+    int32_t gate;        /* gdn_gate_t  */
+    int32_t state_dtype; /* gdn_dtype_t */
+    int32_t ring_dtype;  /* gdn_dtype_t; the g ring is always fp32 */
+} gdn_layer_desc_t;
+
+/* One layer's cache, device pointers, layouts above.  state, ring_d and ring_k
+ * must be 16-byte aligned.  The rings may be NULL when ring_len == 1. */
+typedef struct {
+    float *state;
+    void *ring_d;
+    void *ring_k;
+    float *ring_g;
+} gdn_layer_cache_t;
+
+/* One decode step's inputs and output, device pointers. */
+typedef struct {
+    const void *mixed_qkv;            /* [B, row] in qkv_dtype                         */
+    int32_t qkv_dtype;                /* gdn_dtype_t                                   */
+    int64_t qkv_row_stride;           /* elements between rows (>= 2*HK*K + HV*V)      */
+    const float *g;                   /* [B, HV] (GDN) or [B, HV, K] (KDA)             */
+    const float *beta;                /* [B, HV]                                       */
+    const int32_t *ssm_state_indices; /* [B] row -> slot; negative = padding row       */
+    int32_t batch;                    /* B >= 0 (0: nothing is launched)               */
+    float q_scale;                    /* q <- q * q_scale (1 when pre-scaled)          */
+    int32_t qk_l2norm;                /* 1: q, k <- x / sqrt(sum x^2 + 1e-6) first     */
+    void *out;                        /* [B, HV, V] in out_dtype                       */
+    int32_t out_dtype;                /* gdn_dtype_t                                   */
+} gdn_step_t;
+
+/* Packed decode, the read + write baseline ([P1] Motivation; [P2] section 1):
+ * per row b with slot s = ssm_state_indices[b] >= 0 and every value head,
+ *   S~ = alpha S (KDA: S Diag(exp g)),  d = beta (v - S~ k),  S <- S~ + d k^T,
+ *   out = S q,
+ * with S = state[s, hv] read and written back in place.  Padding rows (s < 0)
+ * get out = 0 and touch nothing.  Rows must map to distinct slots. */
+GDN_API gdn_status_t gdn_packed_decode(const gdn_layer_desc_t *desc, float *state,
+                               const gdn_step_t *step, uint32_t *dev_status,
+                               gdn_stream_t stream);
+
+/* ReplaySSM decode of one layer ([P1] Modifications, Design 1/2/4/5/7; [P2]
+ * 3.2, 3.3).  Per row b, slot s, p = write_pos[s], value head hv:
+ *   is_flush = (p == L-1) or force_flush[b];
+ *   S = A S0 + sum_{j<p} w_j d_j k_j^T (KDA: S0 Diag(A) + sum d_j (w_j o k_j)^T),
+ *       A and w_j from the cached log-gates (empty sums give 1);
+ *   GDN: Sq = alpha S q, Sk = alpha S k;   KDA: Sq = S (a o q), Sk = S (a o k);
+ *   d = beta (v - Sk);   out = Sq + d (k^T q);
+ *   flush:     state[s, hv] <- alpha S + d k^T (KDA: S Diag(a) + d k^T);
+ *   otherwise: ring_d[s, hv, p] <- d, ring_g[s, hv, p] <- g and, from the first
+ *              value head of each group, ring_k[s, hk, p] <- k (ring dtype, RNE).
+ * Only ring entries j < p are read, so stale entries need no clearing.
+ * write_pos is read only: call gdn_replayssm_advance once after the last layer
+ * of the forward.  force_flush ([B] uint8, nonzero = flush) may be NULL.
+ * flushed_out ([B] uint8, may be NULL) receives 1 for rows that flushed.
+ * Padding rows (s < 0) get out = 0, flushed_out = 0 and touch nothing.
+ * Rows must map to distinct slots.  recon is a gdn_recon_t. */
+GDN_API gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
+                                  const int32_t *write_pos, const uint8_t *force_flush,
+                                  const gdn_step_t *step, int32_t recon, uint8_t *flushed_out,
+                                  uint32_t *dev_status, gdn_stream_t stream);
+
+/* Cursor advance, once per forward after all layers ([P1] Design 3):
+ * write_pos[s] <- (write_pos[s] == L-1 or force_flush[b]) ? 0 : write_pos[s] + 1
+ * for each row b with s = ssm_state_indices[b] >= 0.  force_flush may be NULL. */
+GDN_API gdn_status_t gdn_replayssm_advance(const int32_t *ssm_state_indices, int32_t batch,
+                                   const uint8_t *force_flush, int32_t num_slots,
+                                   int32_t ring_len, int32_t *write_pos,
+                                   uint32_t *dev_status, gdn_stream_t stream);
+
+/* Fold the ring into the checkpoint for each listed slot (every value head):
+ * state[s] <- A S0 + sum_{j<write_pos[s]} w_j d_j k_j^T, in fp32 on the CUDA
+ * cores.  This is the state a snapshot or a copy-on-write must see ([P1]
+ * Design 5; [P2] 4.1).  write_pos is not changed: follow with
+ * gdn_replayssm_reset_slots.  Negative entries of slots[n] are skipped. */
+GDN_API gdn_status_t gdn_replayssm_flush(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
+                                 const int32_t *write_pos, const int32_t *slots, int32_t n,
+                                 uint32_t *dev_status, gdn_stream_t stream);
+
+/* write_pos[slots[i]] <- 0 for each listed slot (slot allocation and
+ * copy-on-write, [P1] Design 3 and 5).  Negative entries are skipped. */
+GDN_API gdn_status_t gdn_replayssm_reset_slots(int32_t *write_pos, int32_t num_slots,
+                                       const int32_t *slots, int32_t n,
+                                       uint32_t *dev_status, gdn_stream_t stream);
+
+/* Static text for a status code (host). */
+GDN_API const char *gdn_status_str(gdn_status_t status);
+
+/* Message for the calling host thread's last failing call ("" if none). */
+GDN_API const char *gdn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDNREPLAY_H */

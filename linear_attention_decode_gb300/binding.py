@@ -1,0 +1,236 @@
+"""ctypes binding of libgdnreplay.so — argument marshalling only.
+
+Each function has the name of the C entry point it calls (declared in
+``include/gdnreplay.h``).  It checks that the torch tensors it is given have the
+shapes, dtypes and device the C call expects (the C layer cannot see tensor
+sizes), packs their device pointers into the C structs, calls the library on
+the current CUDA stream (or the one given) and raises ``GdnError`` on a
+non-OK status.  There is no fallback: if the library is missing, loading it
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdnreplay.so")
+
+from .constants import (BF16, DEV_BAD_SLOT, DEV_BAD_WRITE_POS, DEV_INTERNAL, DEV_TIMEOUT,  # noqa: F401
+                        F16, F32, GATE_PER_K, GATE_SCALAR, GDN_DTYPE, RECON_FFMA, RECON_TENSOR,
+                        TORCH_DTYPE)
+
+
+class GdnError(RuntimeError):
+    pass
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("num_slots", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
+                ("num_k_heads", ctypes.c_int32), ("k_dim", ctypes.c_int32),
+                ("v_dim", ctypes.c_int32), ("ring_len", ctypes.c_int32),
+                ("gate", ctypes.c_int32), ("state_dtype", ctypes.c_int32),
+                ("ring_dtype", ctypes.c_int32)]
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("state", ctypes.c_void_p), ("ring_d", ctypes.c_void_p),
+                ("ring_k", ctypes.c_void_p), ("ring_g", ctypes.c_void_p)]
+
+
+class _Step(ctypes.Structure):
+    _fields_ = [("mixed_qkv", ctypes.c_void_p), ("qkv_dtype", ctypes.c_int32),
+                ("qkv_row_stride", ctypes.c_int64), ("g", ctypes.c_void_p),
+                ("beta", ctypes.c_void_p), ("ssm_state_indices", ctypes.c_void_p),
+                ("batch", ctypes.c_int32), ("q_scale", ctypes.c_float),
+                ("qk_l2norm", ctypes.c_int32), ("out", ctypes.c_void_p),
+                ("out_dtype", ctypes.c_int32)]
+
+
+def layer_desc(num_slots, num_v_heads, num_k_heads, k_dim, v_dim, ring_len,
+               gate=GATE_SCALAR, ring_dtype=F16, state_dtype=F32) -> LayerDesc:
+    return LayerDesc(num_slots, num_v_heads, num_k_heads, k_dim, v_dim, ring_len,
+                     gate, state_dtype, ring_dtype)
+
+
+@dataclass
+class Cache:
+    """One layer's cache tensors (device)."""
+    state: torch.Tensor                     # [N, HV, V, K] fp32
+    ring_d: Optional[torch.Tensor] = None   # [N, HV, L, V] ring dtype
+    ring_k: Optional[torch.Tensor] = None   # [N, HK, L, K] ring dtype
+    ring_g: Optional[torch.Tensor] = None   # [N, HV, L] or [N, HV, L, K] fp32
+
+
+@dataclass
+class Step:
+    """One decode step's inputs and output (device)."""
+    mixed_qkv: torch.Tensor          # [B, >= 2*HK*K + HV*V], unit inner stride
+    g: torch.Tensor                  # [B, HV] or [B, HV, K] fp32
+    beta: torch.Tensor               # [B, HV] fp32
+    ssm_state_indices: torch.Tensor  # [B] int32
+    out: torch.Tensor                # [B, HV, V]
+    q_scale: float = 1.0
+    qk_l2norm: bool = False
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libgdnreplay.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise GdnError(f"{path} is missing: build it with linear_attention_decode_gb300.build")
+        lib = ctypes.CDLL(path)
+        vp, i32, u32p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p
+        dp = ctypes.POINTER(LayerDesc)
+        cp, sp = ctypes.POINTER(_Cache), ctypes.POINTER(_Step)
+        lib.gdn_packed_decode.argtypes = [dp, vp, sp, u32p, vp]
+        lib.gdn_replayssm_decode.argtypes = [dp, cp, vp, vp, sp, i32, vp, u32p, vp]
+        lib.gdn_replayssm_advance.argtypes = [vp, i32, vp, i32, i32, vp, u32p, vp]
+        lib.gdn_replayssm_flush.argtypes = [dp, cp, vp, vp, i32, u32p, vp]
+        lib.gdn_replayssm_reset_slots.argtypes = [vp, i32, vp, i32, u32p, vp]
+        for f in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_advance",
+                  "gdn_replayssm_flush", "gdn_replayssm_reset_slots"):
+            getattr(lib, f).restype = ctypes.c_int
+        lib.gdn_status_str.argtypes = [ctypes.c_int]
+        lib.gdn_status_str.restype = ctypes.c_char_p
+        lib.gdn_last_error.argtypes = []
+        lib.gdn_last_error.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, fn: str) -> None:
+    if status != 0:
+        lib = load_library()
+        raise GdnError(f"{fn}: {lib.gdn_status_str(status).decode()}: {lib.gdn_last_error().decode()}")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: Optional[torch.Tensor], name: str, shape=None, dtype=None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise GdnError(f"{name} is required")
+    if not t.is_cuda:
+        raise GdnError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise GdnError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise GdnError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise GdnError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _status_ptr(dev_status):
+    return _dev(dev_status, "dev_status", (1,), torch.int32, optional=True)
+
+
+def _pack_step(d: LayerDesc, s: Step) -> _Step:
+    B = s.ssm_state_indices.shape[0]
+    HV, HK, K, V = d.num_v_heads, d.num_k_heads, d.k_dim, d.v_dim
+    q = s.mixed_qkv
+    if not q.is_cuda or q.dim() != 2 or q.shape[0] != B or q.stride(1) != 1:
+        raise GdnError("mixed_qkv must be a CUDA [B, row] tensor with unit inner stride")
+    if q.shape[1] < 2 * HK * K + HV * V:
+        raise GdnError("mixed_qkv rows are shorter than 2*HK*K + HV*V")
+    if q.dtype not in GDN_DTYPE:
+        raise GdnError("mixed_qkv must be fp32, bf16 or fp16")
+    gshape = (B, HV, K) if d.gate == GATE_PER_K else (B, HV)
+    if s.out.dtype not in GDN_DTYPE:
+        raise GdnError("out must be fp32, bf16 or fp16")
+    return _Step(q.data_ptr() if B else None, GDN_DTYPE[q.dtype], q.stride(0) if B > 1 else q.shape[1],
+                 _dev(s.g, "g", gshape, torch.float32),
+                 _dev(s.beta, "beta", (B, HV), torch.float32),
+                 _dev(s.ssm_state_indices, "ssm_state_indices", (B,), torch.int32),
+                 B, float(s.q_scale), int(bool(s.qk_l2norm)),
+                 _dev(s.out, "out", (B, HV, V)), GDN_DTYPE[s.out.dtype])
+
+
+def _pack_cache(d: LayerDesc, c: Cache) -> _Cache:
+    N, HV, HK, K, V, L = d.num_slots, d.num_v_heads, d.num_k_heads, d.k_dim, d.v_dim, d.ring_len
+    rdt = TORCH_DTYPE[d.ring_dtype]
+    st = _dev(c.state, "state", (N, HV, V, K), torch.float32)
+    opt = L == 1
+    gshape = (N, HV, L, K) if d.gate == GATE_PER_K else (N, HV, L)
+    return _Cache(st, _dev(c.ring_d, "ring_d", (N, HV, L, V), rdt, opt),
+                  _dev(c.ring_k, "ring_k", (N, HK, L, K), rdt, opt),
+                  _dev(c.ring_g, "ring_g", gshape, torch.float32, opt))
+
+
+def gdn_packed_decode(desc: LayerDesc, state: torch.Tensor, step: Step,
+                      dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    st = _dev(state, "state", (desc.num_slots, desc.num_v_heads, desc.v_dim, desc.k_dim), torch.float32)
+    s = _pack_step(desc, step)
+    _check(load_library().gdn_packed_decode(ctypes.byref(desc), st, ctypes.byref(s),
+                                            _status_ptr(dev_status), _stream(stream)),
+           "gdn_packed_decode")
+
+
+def gdn_replayssm_decode(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor,
+                         force_flush: Optional[torch.Tensor], step: Step,
+                         recon: int = RECON_TENSOR, flushed_out: Optional[torch.Tensor] = None,
+                         dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    B = step.ssm_state_indices.shape[0]
+    c = _pack_cache(desc, cache)
+    s = _pack_step(desc, step)
+    _check(load_library().gdn_replayssm_decode(
+        ctypes.byref(desc), ctypes.byref(c),
+        _dev(write_pos, "write_pos", (desc.num_slots,), torch.int32),
+        _dev(force_flush, "force_flush", (B,), torch.uint8, optional=True),
+        ctypes.byref(s), int(recon),
+        _dev(flushed_out, "flushed_out", (B,), torch.uint8, optional=True),
+        _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_decode")
+
+
+def gdn_replayssm_advance(ssm_state_indices: torch.Tensor, force_flush: Optional[torch.Tensor],
+                          num_slots: int, ring_len: int, write_pos: torch.Tensor,
+                          dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    B = ssm_state_indices.shape[0]
+    _check(load_library().gdn_replayssm_advance(
+        _dev(ssm_state_indices, "ssm_state_indices", (B,), torch.int32), B,
+        _dev(force_flush, "force_flush", (B,), torch.uint8, optional=True),
+        int(num_slots), int(ring_len), _dev(write_pos, "write_pos", (num_slots,), torch.int32),
+        _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_advance")
+
+
+def gdn_replayssm_flush(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor,
+                        slots: torch.Tensor, dev_status: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    n = slots.shape[0]
+    c = _pack_cache(desc, cache)
+    _check(load_library().gdn_replayssm_flush(
+        ctypes.byref(desc), ctypes.byref(c),
+        _dev(write_pos, "write_pos", (desc.num_slots,), torch.int32),
+        _dev(slots, "slots", (n,), torch.int32), n, _status_ptr(dev_status), _stream(stream)),
+        "gdn_replayssm_flush")
+
+
+def gdn_replayssm_reset_slots(write_pos: torch.Tensor, slots: torch.Tensor,
+                              dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    n = slots.shape[0]
+    N = write_pos.shape[0]
+    _check(load_library().gdn_replayssm_reset_slots(
+        _dev(write_pos, "write_pos", (N,), torch.int32), N,
+        _dev(slots, "slots", (n,), torch.int32), n, _status_ptr(dev_status), _stream(stream)),
+        "gdn_replayssm_reset_slots")
+
+
+def gdn_status_str(status: int) -> str:
+    return load_library().gdn_status_str(int(status)).decode()
+
+
+def gdn_last_error() -> str:
+    return load_library().gdn_last_error().decode()

@@ -1,0 +1,346 @@
+// CUDA-core kernels: the packed read+write decode (the baseline), the ReplaySSM
+// decode with the replay sum evaluated term by term in fp32 FFMA, the standalone
+// ring fold, and the cursor advance / reset kernels.
+//
+// Thread mapping of the row loops: one CTA per (row, value head), 4 warps.  A
+// warp works on 4 state rows at a time; lane = 8 * row_in_group + column_group,
+// and a lane owns columns 32*m + 4*column_group + {0..3} (m < K/32), so each
+// 16-byte load of a warp covers four 128-byte runs of four rows and a row's
+// contraction over K needs only a 3-step shuffle among its 8 lanes.
+#include "gdn_common.cuh"
+#include "gdn_kernels.h"
+
+namespace gdn {
+
+constexpr int kThreads = 128;
+
+// Stages the replay operands of (slot, hv) in shared memory ([P1] Design 1, 7):
+//   GDN: Dw[j][r] = w_j d_j[r], Kr[j][c] = k_j[c], returns A;
+//   KDA: Dw[j][r] = d_j[r],     Kr[j][c] = w_j[c] k_j[c], Acol[c] = A[c].
+// Only entries j < p are read.  Ends with a CTA barrier.
+template <int D, int GATE>
+__device__ float stage_replay(const DecodeParams &P, int slot, int hv, int p, float *wv,
+                              float *Acol, float *Dw, float *Kr) {
+  const int t = threadIdx.x;
+  const int hk = hv / P.G;
+  const int64_t dbase = ((int64_t)slot * P.HV + hv) * P.L * D;
+  const int64_t kbase = ((int64_t)slot * P.HK + hk) * P.L * D;
+  float A = 1.f;
+  if (GATE == GDN_GATE_SCALAR) {
+    if (t == 0) wv[63] = replay_decays(P.ring_g + ((int64_t)slot * P.HV + hv) * P.L, 1, p, wv, 1);
+    __syncthreads();
+    A = wv[63];
+    if (t < D)
+      for (int j = 0; j < p; ++j) {
+        Dw[j * D + t] = wv[j] * load_as_f32(P.ring_d, dbase + (int64_t)j * D + t, P.ring_dtype);
+        Kr[j * D + t] = load_as_f32(P.ring_k, kbase + (int64_t)j * D + t, P.ring_dtype);
+      }
+  } else {
+    if (t < D) {
+      const float *g = P.ring_g + ((int64_t)slot * P.HV + hv) * P.L * D + t;
+      Acol[t] = replay_decays(g, D, p, Kr + t, D);  // w_j[c] parked in Kr
+      for (int j = 0; j < p; ++j) {
+        Dw[j * D + t] = load_as_f32(P.ring_d, dbase + (int64_t)j * D + t, P.ring_dtype);
+        Kr[j * D + t] *= load_as_f32(P.ring_k, kbase + (int64_t)j * D + t, P.ring_dtype);
+      }
+    }
+  }
+  __syncthreads();
+  return A;
+}
+
+// REPLAY = false: packed decode (read S, write S every step).
+// REPLAY = true:  ReplaySSM decode with the replay sum on the CUDA cores.
+template <int D, int GATE, bool REPLAY>
+__global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParams P) {
+  constexpr int M = D / 32;             // float4 chunks per lane per row
+  constexpr int ROWS_PER_WARP = D / 4;  // 4 warps
+  constexpr int NIT = ROWS_PER_WARP / 4;
+  const int b = blockIdx.x / P.HV, hv = blockIdx.x % P.HV;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int rg = lane >> 3, cg = lane & 7;
+  extern __shared__ float4 smem_f4[];
+  float *q = reinterpret_cast<float *>(smem_f4);
+  float *k = q + D, *v = k + D, *a = v + D, *Acol = a + D, *red = Acol + D, *wv = red + 8;
+  float *Dw = wv + 64, *Kr = Dw + (P.L - 1) * D;
+
+  RowInfo ri;
+  if (REPLAY) {
+    ri = resolve_row(P, b, hv == 0 && t == 0);
+  } else {
+    int slot = P.idx[b];
+    ri = RowInfo{slot, 0, 1, slot >= 0 && slot < P.N};
+    if (slot >= P.N && hv == 0 && t == 0) set_status(P.status, GDN_DEV_BAD_SLOT);
+  }
+  if (REPLAY && hv == 0 && t == 0 && P.flushed) P.flushed[b] = ri.live ? (uint8_t)ri.flush : 0;
+  if (!ri.live) {  // padding row: zeros, no cache access
+    if (t < D) store_from_f32(P.out, ((int64_t)b * P.HV + hv) * D + t, P.out_dtype, 0.f);
+    return;
+  }
+  const int slot = ri.slot, p = ri.p;
+  const int64_t bh = (int64_t)b * P.HV + hv;
+
+  const float kq = load_qkv<D>(P, b, hv, q, k, v, red);
+  const float beta = P.beta[bh];
+  float alpha = 1.f, A = 1.f;
+  if (GATE == GDN_GATE_SCALAR) {
+    alpha = expf(P.g[bh]);
+  } else if (t < D) {
+    a[t] = expf(P.g[bh * D + t]);
+    Acol[t] = 1.f;
+  }
+  if (REPLAY) {
+    A = stage_replay<D, GATE>(P, slot, hv, p, wv, Acol, Dw, Kr);
+  } else {
+    __syncthreads();
+  }
+
+  // Per-lane column constants.
+  float4 qe[M], ke[M], kraw[M], a4[M], A4[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int c4 = 8 * m + cg;
+    kraw[m] = reinterpret_cast<const float4 *>(k)[c4];
+    qe[m] = reinterpret_cast<const float4 *>(q)[c4];
+    ke[m] = kraw[m];
+    if (GATE == GDN_GATE_PER_K) {
+      a4[m] = reinterpret_cast<const float4 *>(a)[c4];
+      A4[m] = reinterpret_cast<const float4 *>(Acol)[c4];
+      qe[m] = make_float4(a4[m].x * qe[m].x, a4[m].y * qe[m].y, a4[m].z * qe[m].z, a4[m].w * qe[m].w);
+      ke[m] = make_float4(a4[m].x * ke[m].x, a4[m].y * ke[m].y, a4[m].z * ke[m].z, a4[m].w * ke[m].w);
+    }
+  }
+
+  float4 *S = reinterpret_cast<float4 *>(P.state + ((int64_t)slot * P.HV + hv) * D * D);
+  float4 cur[M], nxt[M];
+  {
+    const int r0 = warp * ROWS_PER_WARP + rg;
+#pragma unroll
+    for (int m = 0; m < M; ++m) cur[m] = S[r0 * (D / 4) + 8 * m + cg];
+  }
+#pragma unroll 1
+  for (int it = 0; it < NIT; ++it) {
+    const int r = warp * ROWS_PER_WARP + it * 4 + rg;
+    if (it + 1 < NIT) {
+#pragma unroll
+      for (int m = 0; m < M; ++m) nxt[m] = S[(r + 4) * (D / 4) + 8 * m + cg];
+    }
+    // Replayed row r of the pre-token state.
+    float4 s[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      if (GATE == GDN_GATE_SCALAR) {
+        s[m] = REPLAY ? make_float4(A * cur[m].x, A * cur[m].y, A * cur[m].z, A * cur[m].w) : cur[m];
+      } else {
+        s[m] = REPLAY ? make_float4(A4[m].x * cur[m].x, A4[m].y * cur[m].y, A4[m].z * cur[m].z,
+                                    A4[m].w * cur[m].w)
+                      : cur[m];
+      }
+    }
+    if (REPLAY) {
+      for (int j = 0; j < p; ++j) {
+        const float dw = Dw[j * D + r];
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const float4 kr = reinterpret_cast<const float4 *>(Kr + j * D)[8 * m + cg];
+          s[m].x = fmaf(dw, kr.x, s[m].x);
+          s[m].y = fmaf(dw, kr.y, s[m].y);
+          s[m].z = fmaf(dw, kr.z, s[m].z);
+          s[m].w = fmaf(dw, kr.w, s[m].w);
+        }
+      }
+    }
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      sq = dot4(s[m], qe[m], sq);
+      sk = dot4(s[m], ke[m], sk);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    if (GATE == GDN_GATE_SCALAR) {
+      sq *= alpha;
+      sk *= alpha;
+    }
+    const float d = beta * (v[r] - sk);
+    const float o = fmaf(d, kq, sq);
+    if (cg == 0) store_from_f32(P.out, bh * D + r, P.out_dtype, o);
+    if (ri.flush) {
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        float4 n;
+        if (GATE == GDN_GATE_SCALAR) {
+          n = make_float4(fmaf(d, kraw[m].x, alpha * s[m].x), fmaf(d, kraw[m].y, alpha * s[m].y),
+                          fmaf(d, kraw[m].z, alpha * s[m].z), fmaf(d, kraw[m].w, alpha * s[m].w));
+        } else {
+          n = make_float4(fmaf(d, kraw[m].x, s[m].x * a4[m].x), fmaf(d, kraw[m].y, s[m].y * a4[m].y),
+                          fmaf(d, kraw[m].z, s[m].z * a4[m].z), fmaf(d, kraw[m].w, s[m].w * a4[m].w));
+        }
+        S[r * (D / 4) + 8 * m + cg] = n;
+      }
+    } else if (cg == 0) {
+      store_from_f32(P.ring_d, (((int64_t)slot * P.HV + hv) * P.L + p) * D + r, P.ring_dtype, d);
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) cur[m] = nxt[m];
+  }
+
+  if (REPLAY && !ri.flush) {  // ring append of k (one writer per key head) and g
+    const int hk = hv / P.G;
+    if (GATE == GDN_GATE_SCALAR) {
+      if (t == 0) P.ring_g[((int64_t)slot * P.HV + hv) * P.L + p] = P.g[bh];
+    } else if (t < D) {
+      P.ring_g[(((int64_t)slot * P.HV + hv) * P.L + p) * D + t] = P.g[bh * D + t];
+    }
+    if (hv % P.G == 0 && t < D)
+      store_from_f32(P.ring_k, (((int64_t)slot * P.HK + hk) * P.L + p) * D + t, P.ring_dtype, k[t]);
+  }
+}
+
+// Standalone fold: state[s, hv] <- replayed state with write_pos[s] entries.
+template <int D, int GATE>
+__global__ void __launch_bounds__(kThreads) fold_kernel(const DecodeParams P) {
+  constexpr int M = D / 32;
+  constexpr int ROWS_PER_WARP = D / 4;
+  const int i = blockIdx.x / P.HV, hv = blockIdx.x % P.HV;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int rg = lane >> 3, cg = lane & 7;
+  extern __shared__ float4 smem_f4[];
+  float *Acol = reinterpret_cast<float *>(smem_f4), *wv = Acol + D, *Dw = wv + 64;
+  float *Kr = Dw + (P.L - 1) * D;
+  const int slot = P.slots[i];
+  if (slot < 0) return;
+  if (slot >= P.N) {
+    if (hv == 0 && t == 0) set_status(P.status, GDN_DEV_BAD_SLOT);
+    return;
+  }
+  const int p = P.write_pos[slot];
+  if (p < 0 || p >= P.L) {
+    if (hv == 0 && t == 0) set_status(P.status, GDN_DEV_BAD_WRITE_POS);
+    return;
+  }
+  if (GATE == GDN_GATE_PER_K && t < D) Acol[t] = 1.f;
+  const float A = stage_replay<D, GATE>(P, slot, hv, p, wv, Acol, Dw, Kr);
+  float4 A4[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m)
+    A4[m] = GATE == GDN_GATE_PER_K ? reinterpret_cast<const float4 *>(Acol)[8 * m + cg]
+                                   : make_float4(A, A, A, A);
+  float4 *S = reinterpret_cast<float4 *>(P.state + ((int64_t)slot * P.HV + hv) * D * D);
+  for (int it = 0; it < ROWS_PER_WARP / 4; ++it) {
+    const int r = warp * ROWS_PER_WARP + it * 4 + rg;
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const float4 c = S[r * (D / 4) + 8 * m + cg];
+      float4 s = make_float4(A4[m].x * c.x, A4[m].y * c.y, A4[m].z * c.z, A4[m].w * c.w);
+      for (int j = 0; j < p; ++j) {
+        const float dw = Dw[j * D + r];
+        const float4 kr = reinterpret_cast<const float4 *>(Kr + j * D)[8 * m + cg];
+        s.x = fmaf(dw, kr.x, s.x);
+        s.y = fmaf(dw, kr.y, s.y);
+        s.z = fmaf(dw, kr.z, s.z);
+        s.w = fmaf(dw, kr.w, s.w);
+      }
+      S[r * (D / 4) + 8 * m + cg] = s;
+    }
+  }
+}
+
+__global__ void advance_kernel(const int32_t *idx, int B, const uint8_t *ff, int N, int L,
+                               int32_t *write_pos, uint32_t *status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int slot = idx[b];
+  if (slot < 0) return;
+  if (slot >= N) {
+    set_status(status, GDN_DEV_BAD_SLOT);
+    return;
+  }
+  const int p = write_pos[slot];
+  if (p < 0 || p >= L) {
+    set_status(status, GDN_DEV_BAD_WRITE_POS);
+    return;
+  }
+  const bool flush = (p == L - 1) || (ff != nullptr && ff[b] != 0);
+  write_pos[slot] = flush ? 0 : p + 1;
+}
+
+__global__ void reset_kernel(int32_t *write_pos, int N, const int32_t *slots, int n,
+                             uint32_t *status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int slot = slots[i];
+  if (slot < 0) return;
+  if (slot >= N) {
+    set_status(status, GDN_DEV_BAD_SLOT);
+    return;
+  }
+  write_pos[slot] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers.
+// ---------------------------------------------------------------------------
+
+static size_t ffma_smem_bytes(int D, int L, bool replay) {
+  size_t floats = 5 * (size_t)D + 8 + 64 + (replay ? 2 * (size_t)(L - 1) * D : 0);
+  return floats * sizeof(float);
+}
+
+template <int D, int GATE, bool REPLAY>
+static cudaError_t launch_decode_t(const DecodeParams &P, cudaStream_t s) {
+  const size_t smem = ffma_smem_bytes(D, P.L, REPLAY);
+  auto kern = ffma_decode_kernel<D, GATE, REPLAY>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)P.B * P.HV, kThreads, smem, s>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ffma_decode(const DecodeParams &P, int D, int gate, bool replay, cudaStream_t s) {
+  if (D == 128) {
+    if (gate == GDN_GATE_SCALAR)
+      return replay ? launch_decode_t<128, 0, true>(P, s) : launch_decode_t<128, 0, false>(P, s);
+    return replay ? launch_decode_t<128, 1, true>(P, s) : launch_decode_t<128, 1, false>(P, s);
+  }
+  if (gate == GDN_GATE_SCALAR)
+    return replay ? launch_decode_t<64, 0, true>(P, s) : launch_decode_t<64, 0, false>(P, s);
+  return replay ? launch_decode_t<64, 1, true>(P, s) : launch_decode_t<64, 1, false>(P, s);
+}
+
+template <int D, int GATE>
+static cudaError_t launch_fold_t(const DecodeParams &P, int n, cudaStream_t s) {
+  const size_t smem = (2 * (size_t)D + 64 + 2 * (size_t)(P.L - 1) * D) * sizeof(float);
+  auto kern = fold_kernel<D, GATE>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)n * P.HV, kThreads, smem, s>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fold(const DecodeParams &P, int D, int gate, int n, cudaStream_t s) {
+  if (D == 128)
+    return gate == GDN_GATE_SCALAR ? launch_fold_t<128, 0>(P, n, s) : launch_fold_t<128, 1>(P, n, s);
+  return gate == GDN_GATE_SCALAR ? launch_fold_t<64, 0>(P, n, s) : launch_fold_t<64, 1>(P, n, s);
+}
+
+cudaError_t launch_advance(const int32_t *idx, int B, const uint8_t *ff, int N, int L,
+                           int32_t *write_pos, uint32_t *status, cudaStream_t s) {
+  advance_kernel<<<(B + 255) / 256, 256, 0, s>>>(idx, B, ff, N, L, write_pos, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset(int32_t *write_pos, int N, const int32_t *slots, int n, uint32_t *status,
+                         cudaStream_t s) {
+  reset_kernel<<<(n + 255) / 256, 256, 0, s>>>(write_pos, N, slots, n, status);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

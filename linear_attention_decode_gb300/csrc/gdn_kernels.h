@@ -1,0 +1,29 @@
+// Internal launchers (host side) of the gdnreplay kernels; arguments are
+// already validated by the C ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+// Packed decode (replay = false) or ReplaySSM decode with FFMA replay (replay = true).
+cudaError_t launch_ffma_decode(const DecodeParams &P, int D, int gate, bool replay, cudaStream_t s);
+
+// ReplaySSM decode with the replay sum on the tensor cores (tcgen05) and the
+// checkpoint streamed by TMA.  Writes a reason into *why on a host-side failure.
+cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why);
+
+cudaError_t launch_fold(const DecodeParams &P, int D, int gate, int n, cudaStream_t s);
+
+cudaError_t launch_advance(const int32_t *idx, int B, const uint8_t *ff, int N, int L,
+                           int32_t *write_pos, uint32_t *status, cudaStream_t s);
+
+cudaError_t launch_reset(int32_t *write_pos, int N, const int32_t *slots, int n, uint32_t *status,
+                         cudaStream_t s);
+
+// Dynamic shared memory of one tensor-core decode CTA (bytes).
+size_t tc_smem_bytes(int D, int gate, int ring_dtype, int L);
+
+}  // namespace gdn

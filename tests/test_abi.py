@@ -1,0 +1,106 @@
+"""The C ABI library without a GPU: it loads, exports every entry point that
+include/*.h declares, and its host-side argument checks reject bad calls
+before any CUDA call is made."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from linear_attention_decode_gb300 import binding as Bd
+from linear_attention_decode_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_entry_points():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        names += re.findall(r"GDN_API\s+[\w\s\*]*?\b(gdn_\w+)\s*\(", open(h).read())
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return Bd.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for n in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_advance",
+              "gdn_replayssm_flush", "gdn_replayssm_reset_slots", "gdn_status_str", "gdn_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_entry_points():
+        assert hasattr(lib, n), f"{n} is declared in include/ but not exported"
+
+
+def _step(batch=4, row=2 * 16 * 128 + 32 * 128):
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: every case below fails a host check
+    return Bd._Step(fake, Bd.BF16, row, fake, fake, fake, batch, 1.0, 0, fake, Bd.F32)
+
+
+def _desc(**kw):
+    d = dict(num_slots=8, num_v_heads=32, num_k_heads=16, k_dim=128, v_dim=128, ring_len=16)
+    d.update(kw)
+    return Bd.layer_desc(**d)
+
+
+CASES = [
+    ("hv_not_multiple_of_hk", _desc(num_k_heads=5), 1),
+    ("k_dim_96", _desc(k_dim=96, v_dim=96), 2),
+    ("k_ne_v", _desc(v_dim=64), 2),
+    ("ring_len_65", _desc(ring_len=65), 2),
+    ("ring_len_0", _desc(ring_len=0), 1),
+    ("bf16_state", Bd.layer_desc(8, 32, 16, 128, 128, 16, state_dtype=Bd.BF16), 2),
+    ("bad_gate", Bd.layer_desc(8, 32, 16, 128, 128, 16, gate=7), 1),
+]
+
+
+@pytest.mark.parametrize("name,desc,code", CASES, ids=[c[0] for c in CASES])
+def test_decode_rejects_bad_descriptors(lib, name, desc, code):
+    cache = Bd._Cache(0x1000, 0x1000, 0x1000, 0x1000)
+    st = lib.gdn_replayssm_decode(ctypes.byref(desc), ctypes.byref(cache), 0x1000, None,
+                                  ctypes.byref(_step()), 0, None, None, None)
+    assert st == code, lib.gdn_last_error().decode()
+    st = lib.gdn_packed_decode(ctypes.byref(desc), 0x1000, ctypes.byref(_step()), None, None)
+    assert st == code
+
+
+def test_decode_rejects_bad_pointers_and_sizes(lib):
+    d = _desc()
+    good = Bd._Cache(0x1000, 0x1000, 0x1000, 0x1000)
+    calls = [
+        (Bd._Cache(0x1004, 0x1000, 0x1000, 0x1000), _step(), 0x1000, 0),   # misaligned state
+        (Bd._Cache(0x1000, None, 0x1000, 0x1000), _step(), 0x1000, 0),     # missing ring
+        (good, _step(row=100), 0x1000, 0),                                  # short qkv row
+        (good, _step(batch=-1), 0x1000, 0),                                 # negative batch
+        (good, _step(), None, 0),                                           # no write_pos
+        (good, _step(), 0x1000, 5),                                         # unknown recon
+    ]
+    for cache, step, wp, recon in calls:
+        st = lib.gdn_replayssm_decode(ctypes.byref(d), ctypes.byref(cache), wp, None, ctypes.byref(step),
+                                      recon, None, None, None)
+        assert st == 1, lib.gdn_last_error().decode()
+        assert lib.gdn_last_error().decode() != ""
+
+
+def test_empty_calls_are_no_ops(lib):
+    d = _desc()
+    cache = Bd._Cache(0x1000, 0x1000, 0x1000, 0x1000)
+    assert lib.gdn_replayssm_decode(ctypes.byref(d), ctypes.byref(cache), 0x1000, None,
+                                    ctypes.byref(_step(batch=0)), 0, None, None, None) == 0
+    assert lib.gdn_replayssm_advance(None, 0, None, 8, 16, None, None, None) == 0
+    assert lib.gdn_replayssm_flush(ctypes.byref(d), ctypes.byref(cache), None, None, 0, None, None) == 0
+    assert lib.gdn_replayssm_reset_slots(0x1000, 8, None, 0, None, None) == 0
+    assert lib.gdn_replayssm_advance(None, 4, None, 8, 16, None, None, None) == 1
+    assert lib.gdn_replayssm_reset_slots(None, 8, 0x1000, 3, None, None) == 1
+
+
+def test_status_strings(lib):
+    assert lib.gdn_status_str(0).decode() == "ok"
+    assert "invalid" in lib.gdn_status_str(1).decode()

@@ -1,0 +1,79 @@
+"""Host-side logic of bench.py on the CPU: the algorithmic byte count against
+the bandwidth figures the explainer prints, and the multi-rank aggregation
+(gloo, world size 2)."""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_state_traffic_matches_the_explainer():
+    """"ReplaySSM" explainer, section 1 and 5.1: the packed decode moves 8*dv*dk
+    state bytes per head-step; ReplaySSM with one checkpoint read per step and a
+    flush every L steps moves 4*dv*dk*(1 + 1/L) on average, 53.1% at L = 16."""
+    K = V = 128
+    for L in (1, 4, 8, 16, 32):
+        cycle = [bench.head_step_parts(K, V, 2, p, p == L - 1, 2, 2, 2)["state"] for p in range(L)]
+        assert sum(cycle) / L == pytest.approx(4 * V * K * (1 + 1 / L))
+    packed = 8 * V * K
+    ratio = sum(bench.head_step_parts(K, V, 2, p, p == 15, 2, 2, 2)["state"] for p in range(16)) / 16 / packed
+    assert round(100 * ratio, 1) == 53.1
+    # 64 KiB of fp32 state per 128 x 128 head, 128 KiB read + write (section 1)
+    assert bench.head_step_parts(K, V, 2, 0, True, 2, 2, 0)["state"] == 128 * 1024
+
+
+def test_amortised_bytes_per_head_step():
+    """fp16 ring, bf16 in/out, GQA 2:1, L = 16, cursor uniform over the cycle:
+    65536 (read) + 7.5 * 388 (replay) + 15/16 * 388 (append) + 4096 (flush)
+    + 520 (inputs) + 256 (output) bytes."""
+    L = 16
+    mean = sum(bench.head_step_bytes(128, 128, 2, p, p == L - 1, 2, 2, 2) for p in range(L)) / L
+    assert mean == pytest.approx(65536 + 7.5 * 388 + 15 / 16 * 388 + 4096 + 520 + 256)
+    assert bench.packed_head_step_bytes(128, 128, 2, 2, 2) == 131072 + 520 + 256
+
+
+def test_launch_bytes_counts_padding_rows():
+    from linear_attention_decode_gb300 import inputs as I
+    w = I.QWEN3NEXT_LAYER
+    one = bench.launch_bytes(w, [3], [False], 2, 0)
+    assert bench.launch_bytes(w, [3], [False], 2, 4) == one + 4 * w.HV * w.V * 2
+    assert one == w.HV * bench.head_step_bytes(128, 128, 2, 3, False, 2, 2, 2)
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    elapsed = [0.25, 0.5][rank]
+    m = bench.max_over_ranks(elapsed, torch.device("cpu"))
+    q.put((rank, m, bench.job_throughput(1000.0, world, m)))
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29000 + os.getpid() % 1000
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for _, m, v in res:
+        assert m == 0.5 and v == pytest.approx(2 * 1000.0 / 0.5)
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""

@@ -1,0 +1,329 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+Bounds: max|err| <= tau * max|ref| per launch tensor, tau = 1e-5 for an fp32
+ring with the CUDA-core replay, 2e-3 for tensor-core replay or an fp16/bf16
+ring.  Integer and index results (cursors, flush flags, padding rows, k/g ring
+entries, untouched slots) are compared bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_harness import (TOL_TC, Layer, desc_of, oracle_geom, rel_err, run_parity, run_sampled)
+from linear_attention_decode_gb300 import binding as Bd
+from linear_attention_decode_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TC, FF = Bd.RECON_TENSOR, Bd.RECON_FFMA
+
+# Several CTAs per launch, a ragged batch with padding rows, mixed flush and
+# append rows (staggered cursors) and GQA 2:1, at the pages' head size.
+RAGGED = I.Workload("ragged", N=16, B=5, n_pad=2, HV=8, HK=4, K=128, L=16, ring_dtype=Bd.F16,
+                    qkv_dtype=Bd.BF16, steps=34, staggered=True, seed=11)
+KDA_SMALL = I.Workload("kda small", N=8, B=3, n_pad=1, HV=4, HK=4, K=128, L=16, ring_dtype=Bd.F16,
+                       qkv_dtype=Bd.BF16, gate=Bd.GATE_PER_K, steps=34, staggered=True, seed=12)
+
+
+@pytest.fixture(autouse=True)
+def _lib(gdnlib):
+    yield
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_tiny_fp32(recon):
+    rep = run_parity(I.TINY, recon)
+    assert sum(s.flushes for s in rep.steps) == 8 * I.TINY.B  # 32 steps, L = 4
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("ring", [Bd.F16, Bd.BF16, Bd.F32], ids=["f16", "bf16", "f32"])
+def test_ragged_staggered(recon, ring):
+    rep = run_parity(I.with_(RAGGED, ring_dtype=ring), recon)
+    assert sum(s.flushes for s in rep.steps) > 0 and sum(s.appends for s in rep.steps) > 0
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_kda(recon):
+    run_parity(KDA_SMALL, recon)
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_head_dim_64_gqa(recon):
+    w = I.Workload("k64", N=6, B=4, HV=4, HK=1, K=64, L=8, ring_dtype=Bd.F16, qkv_dtype=Bd.F16,
+                   steps=18, staggered=True, seed=13)
+    run_parity(w, recon)
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_longest_ring(recon):
+    w = I.Workload("L64", N=3, B=2, HV=2, HK=1, K=128, L=64, ring_dtype=Bd.F16, qkv_dtype=Bd.BF16,
+                   steps=70, seed=14)
+    rep = run_parity(w, recon)
+    assert sum(s.flushes for s in rep.steps) == 2
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_forced_flush_mid_ring(recon):
+    sched = lambda t, rows: (np.arange(rows) % 3 == t % 3).astype(np.uint8) if t % 5 == 2 else np.zeros(rows, np.uint8)
+    rep = run_parity(I.with_(RAGGED, steps=20), recon, force=sched)
+    assert sum(s.flushes for s in rep.steps) > 0
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_three_layer_stack_shared_cursor(recon):
+    run_parity(I.with_(RAGGED, steps=18), recon, layers=3)
+
+
+def test_bf16_output():
+    # bf16 rounding of the output alone can be 2^-8 relative: one bf16 ulp on top of the bound
+    run_parity(I.with_(RAGGED, steps=10), TC, out_dtype=torch.bfloat16, tol=TOL_TC + 2.0 ** -8)
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_in_kernel_l2norm_and_scale(recon):
+    run_parity(I.with_(RAGGED, steps=6), recon, q_scale=0.37, qk_l2norm=True)
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_beta0_g0_leaves_checkpoint_bit_identical(recon):
+    """beta = 0 and g = 0 at every step: d = 0 and alpha = 1, so after a full
+    ring cycle the flushed checkpoint equals S0 bit for bit."""
+    w = I.with_(RAGGED, steps=16, staggered=False)
+
+    def zero_gates(t, si):
+        si.g.zero_()
+        si.beta.zero_()
+
+    gen = I.generator(w.seed, "cpu")
+    wp = I.write_pos(gen, w, "cpu")
+    S0 = I.cache(gen, w, wp, "cpu").state
+    rep = run_parity(w, recon, tweak=zero_gates, check_untouched=False)
+    assert rep.steps[-1].flushes == w.B
+    # re-run to get the device state after the last (flush) step
+    gen = I.generator(w.seed, "cpu")
+    wp = I.write_pos(gen, w, "cpu")
+    layer = Layer.make(w, gen, wp)
+    idx = I.indices(gen, w.B, w.N, w.n_pad, "cpu").cuda()
+    wpd = wp.cuda()
+    for t in range(w.steps):
+        si = I.step_inputs(gen, w, "cpu")
+        zero_gates(t, si)
+        out = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
+        Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wpd, None,
+                                Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx, out), recon)
+        Bd.gdn_replayssm_advance(idx, None, w.N, w.L, wpd)
+    assert torch.equal(layer.dev.state.cpu().view(torch.int32), S0.view(torch.int32))
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_erased_history_closed_form(recon):
+    """g = -1e4 makes alpha underflow to 0: out = beta v (k^T q) whatever the history."""
+    w = I.with_(RAGGED, steps=1)
+    gen = I.generator(w.seed, "cpu")
+    wp = I.write_pos(gen, w, "cpu")
+    layer = Layer.make(w, gen, wp)
+    idx = I.indices(gen, w.B, w.N, w.n_pad, "cpu")
+    si = I.step_inputs(gen, w, "cpu")
+    si.g.fill_(-1e4)
+    out = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
+    Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wp.cuda(), None,
+                            Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx.cuda(), out), recon)
+    x = si.mixed_qkv.double()
+    R = x.shape[0]
+    q = x[:, : w.HK * w.K].reshape(R, w.HK, w.K)
+    k = x[:, w.HK * w.K: 2 * w.HK * w.K].reshape(R, w.HK, w.K)
+    v = x[:, 2 * w.HK * w.K:].reshape(R, w.HV, w.V)
+    kq = (q * k).sum(-1).repeat_interleave(w.HV // w.HK, dim=1)  # [R, HV]
+    ref = si.beta.double()[..., None] * v * kq[..., None]
+    live = idx >= 0
+    assert rel_err(out.cpu()[live].numpy(), ref[live].numpy()) <= 1e-5
+    assert torch.all(out.cpu()[~live] == 0)
+
+
+def test_l1_replay_is_packed_decode_bitwise():
+    """L = 1: the CUDA-core replay decode and the packed decode give identical bits."""
+    w = I.Workload("L1", N=6, B=4, n_pad=1, HV=8, HK=4, K=128, L=1, ring_dtype=Bd.F32,
+                   qkv_dtype=Bd.BF16, steps=5, seed=15)
+    gen = I.generator(w.seed, "cpu")
+    S0 = I.state(gen, w.N, w.HV, w.V, w.K, "cpu").cuda()
+    idx = I.indices(gen, w.B, w.N, w.n_pad, "cpu").cuda()
+    sa, sb = S0.clone(), S0.clone()
+    wp = torch.zeros(w.N, dtype=torch.int32, device="cuda")
+    flushed = torch.empty(idx.shape[0], dtype=torch.uint8, device="cuda")
+    d = desc_of(w)
+    for _ in range(w.steps):
+        si = I.step_inputs(gen, w, "cuda")
+        oa = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
+        ob = torch.empty_like(oa)
+        Bd.gdn_replayssm_decode(d, Bd.Cache(sa), wp, None, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, oa), FF, flushed)
+        Bd.gdn_packed_decode(d, sb, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, ob))
+        Bd.gdn_replayssm_advance(idx, None, w.N, 1, wp)
+        assert torch.equal(oa, ob) and torch.equal(sa, sb)
+        assert torch.equal(flushed.cpu(), (idx.cpu() >= 0).to(torch.uint8))
+    assert torch.all(wp == 0)
+
+
+def test_l1_tensor_path_matches_packed():
+    w = I.Workload("L1", N=6, B=4, HV=8, HK=4, K=128, L=1, ring_dtype=Bd.F16, qkv_dtype=Bd.BF16,
+                   steps=4, seed=16)
+    gen = I.generator(w.seed, "cpu")
+    S0 = I.state(gen, w.N, w.HV, w.V, w.K, "cpu").cuda()
+    idx = I.indices(gen, w.B, w.N, 0, "cpu").cuda()
+    sa, sb = S0.clone(), S0.clone()
+    wp = torch.zeros(w.N, dtype=torch.int32, device="cuda")
+    d = desc_of(w)
+    for _ in range(w.steps):
+        si = I.step_inputs(gen, w, "cuda")
+        oa = torch.empty((w.B, w.HV, w.V), device="cuda")
+        ob = torch.empty_like(oa)
+        Bd.gdn_replayssm_decode(d, Bd.Cache(sa), wp, None, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, oa), TC)
+        Bd.gdn_packed_decode(d, sb, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, ob))
+        assert rel_err(oa.cpu().numpy(), ob.cpu().numpy()) <= 1e-5
+        assert rel_err(sa.cpu().numpy(), sb.cpu().numpy()) <= 1e-5
+
+
+@pytest.mark.parametrize("gate", [Bd.GATE_SCALAR, Bd.GATE_PER_K], ids=["gdn", "kda"])
+def test_packed_decode_vs_oracle(gate):
+    w = I.Workload("packed", N=10, B=6, n_pad=2, HV=4, HK=2 if gate == Bd.GATE_SCALAR else 4, K=128, L=1,
+                   ring_dtype=Bd.F32, qkv_dtype=Bd.F32, gate=gate, steps=6, seed=17)
+    gen = I.generator(w.seed, "cpu")
+    S0 = I.state(gen, w.N, w.HV, w.V, w.K, "cpu")
+    idx = I.indices(gen, w.B, w.N, w.n_pad, "cpu")
+    dev = S0.cuda()
+    ora = O.f64(S0).copy()
+    G = O.geom(w.N, w.HV, w.HK, w.K, w.V, 1, gate=gate, state_dtype=O.F32)
+    for _ in range(w.steps):
+        si = I.step_inputs(gen, w, "cpu")
+        out = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
+        Bd.gdn_packed_decode(desc_of(w), dev, Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx.cuda(), out))
+        o_ref, st = O.packed_decode(G, ora, idx.numpy(), si.mixed_qkv, si.g, si.beta)
+        assert st == 0
+        live = idx.numpy() >= 0
+        assert rel_err(out.cpu().numpy()[live], o_ref[live]) <= 1e-5
+        assert np.all(out.cpu().numpy()[~live] == 0)
+        assert rel_err(dev.cpu().numpy(), ora) <= 1e-5
+
+
+@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+def test_bad_rows_set_status_and_touch_nothing(recon):
+    w = I.with_(RAGGED, steps=1)
+    gen = I.generator(w.seed, "cpu")
+    wp = I.write_pos(gen, w, "cpu")
+    layer = Layer.make(w, gen, wp)
+    wp[3] = w.L + 2                                         # cursor out of range
+    idx = torch.tensor([-1, w.N + 5, 3, 1], dtype=torch.int32)  # padding, bad slot, bad cursor, good
+    si = I.step_inputs(gen, w, "cpu", rows=4)
+    out = torch.full((4, w.HV, w.V), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flushed = torch.full((4,), 7, dtype=torch.uint8, device="cuda")
+    before = layer.dev.state.clone()
+    Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wp.cuda(), None,
+                            Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx.cuda(), out),
+                            recon, flushed, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == (Bd.DEV_BAD_SLOT | Bd.DEV_BAD_WRITE_POS)
+    o = out.cpu()
+    assert torch.all(o[:3] == 0) and torch.all(torch.isfinite(o[3]))
+    assert flushed.cpu()[:3].tolist() == [0, 0, 0]
+    assert torch.equal(layer.dev.state[3], before[3])
+    status.zero_()
+    wpd = wp.cuda()
+    Bd.gdn_replayssm_advance(idx.cuda(), None, w.N, w.L, wpd, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == (Bd.DEV_BAD_SLOT | Bd.DEV_BAD_WRITE_POS)
+    assert int(wpd[3].item()) == w.L + 2
+
+
+def test_empty_and_all_padding_batches():
+    w = I.with_(RAGGED, steps=1)
+    gen = I.generator(w.seed, "cpu")
+    wp = I.write_pos(gen, w, "cpu")
+    layer = Layer.make(w, gen, wp)
+    before = [t.clone() for t in (layer.dev.state, layer.dev.ring_d, layer.dev.ring_k, layer.dev.ring_g)]
+    for rows in (0, 3):
+        idx = torch.full((rows,), -1, dtype=torch.int32, device="cuda")
+        si = I.step_inputs(gen, w, "cuda", rows=rows)
+        out = torch.full((rows, w.HV, w.V), float("nan"), device="cuda")
+        for recon in (FF, TC):
+            Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wp.cuda(), None,
+                                    Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out), recon)
+        Bd.gdn_packed_decode(desc_of(w), layer.dev.state, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out))
+        torch.cuda.synchronize()
+        assert torch.all(out == 0)
+    after = (layer.dev.state, layer.dev.ring_d, layer.dev.ring_k, layer.dev.ring_g)
+    for a, b in zip(after, before):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+@pytest.mark.parametrize("gate", [Bd.GATE_SCALAR, Bd.GATE_PER_K], ids=["gdn", "kda"])
+def test_fold_then_reset(gate):
+    """gdn_replayssm_flush folds the ring into the checkpoint (oracle replay_fold);
+    gdn_replayssm_reset_slots zeroes the cursors; decoding then continues."""
+    w = I.with_(KDA_SMALL if gate == Bd.GATE_PER_K else RAGGED, steps=1)
+    w = I.with_(w, ring_dtype=Bd.F32)
+    gen = I.generator(w.seed, "cpu")
+    wp = I.write_pos(gen, w, "cpu")
+    layer = Layer.make(w, gen, wp)
+    slots = torch.tensor([1, -1, 4, 2], dtype=torch.int32)
+    wpd = wp.cuda()
+    Bd.gdn_replayssm_flush(desc_of(w), layer.dev, wpd, slots.cuda())
+    O.replay_fold(oracle_geom(w), layer.ora, wp.numpy(), slots.numpy())
+    assert rel_err(layer.dev.state.cpu().numpy(), layer.ora.state) <= 1e-5
+    Bd.gdn_replayssm_reset_slots(wpd, slots.cuda())
+    expect = wp.clone()
+    expect[[1, 4, 2]] = 0
+    assert torch.equal(wpd.cpu(), expect)
+
+
+def test_host_side_rejects_bad_arguments():
+    w = I.with_(RAGGED, steps=1)
+    gen = I.generator(w.seed, "cpu")
+    wp = I.write_pos(gen, w, "cpu")
+    layer = Layer.make(w, gen, wp)
+    idx = I.indices(gen, w.B, w.N, w.n_pad, "cpu").cuda()
+    si = I.step_inputs(gen, w, "cuda")
+    out = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
+    step = Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out)
+    bad = [desc_of(I.with_(w, K=96)), Bd.layer_desc(w.N, 6, 4, 128, 128, 16),
+           Bd.layer_desc(w.N, w.HV, w.HK, 128, 128, 65)]
+    for d in bad:
+        with pytest.raises(Bd.GdnError):
+            Bd.gdn_replayssm_decode(d, layer.dev, wp.cuda(), None, step, TC)
+    with pytest.raises(Bd.GdnError):
+        Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wp.cuda(), None, step, 7)
+
+
+@pytest.mark.parametrize("w", [I.QWEN3NEXT_LAYER, I.HEADLINE, I.KDA_LAYER],
+                         ids=["qwen3next_layer", "headline_B256_L16", "kda_layer"])
+def test_full_size_sampled(w):
+    """The launch configuration the benchmark times, checked on sampled rows."""
+    run_sampled(w, TC, steps=3)
+
+
+def test_drift_after_four_rings():
+    """4L steps of the tensor-core path with an fp16 ring: error against the
+    oracle with storage rounding stays within the bound; the distance to the
+    unrounded recurrence (double storage) is reported."""
+    w = I.with_(RAGGED, staggered=False, steps=64, n_pad=0)
+    rep = run_parity(w, TC)
+    gen = I.generator(w.seed, "cpu")
+    wp = I.write_pos(gen, w, "cpu")
+    c = I.cache(gen, w, wp, "cpu")
+    idx = I.indices(gen, w.B, w.N, w.n_pad, "cpu").numpy()
+    Gp = O.geom(w.N, w.HV, w.HK, w.K, w.V, w.L, state_dtype=O.F64, ring_dtype=O.F64)
+    pure = O.Cache.from_arrays(c.state, c.ring_d, c.ring_k, c.ring_g)
+    Gq = oracle_geom(w)
+    quant = O.Cache.from_arrays(c.state, c.ring_d, c.ring_k, c.ring_g)
+    wpp, wpq = wp.numpy().copy(), wp.numpy().copy()
+    drift = 0.0
+    for t in range(w.steps):
+        si = I.step_inputs(gen, w, "cpu")
+        op, _, _ = O.replay_decode(Gp, pure, wpp, idx, None, si.mixed_qkv, si.g, si.beta)
+        oq, _, _ = O.replay_decode(Gq, quant, wpq, idx, None, si.mixed_qkv, si.g, si.beta)
+        O.replay_advance(w.N, idx, None, w.L, wpp)
+        O.replay_advance(w.N, idx, None, w.L, wpq)
+        drift = max(drift, rel_err(oq, op))
+    print(f"\n[drift 4L] tensor path vs oracle+storage rounding: out {rep.max_o:.3e}, "
+          f"checkpoint {rep.max_state:.3e}; storage rounding vs unrounded recurrence: {drift:.3e}")
+    assert rep.max_o <= TOL_TC
