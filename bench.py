@@ -8,6 +8,8 @@ uniformly over [0, L) so flush and append rows mix in every launch.  Every step
 reads 512 MiB of checkpoint (4x the 129 MB L2), so no L2 flush is needed.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       [--workload headline|qwen3next_layer|kda_layer|sweep:B:L:f16|f32] [--recon tensor|ffma]
+       [--kernel-only]   (timed decode loop only: for profiling and sweeps)
 Under torchrun each rank runs an independent replica on its own GPU (the
 path has no exchange step); rank 0 prints one JSON line.
 """
@@ -271,6 +273,21 @@ def run_reference(args):
     return 0
 
 
+def pick_workload(name):
+    from linear_attention_decode_gb300 import inputs as I
+    from linear_attention_decode_gb300.constants import BF16, F16, F32
+    if name == "headline":
+        return I.HEADLINE
+    if name == "qwen3next_layer":
+        return I.with_(I.QWEN3NEXT_LAYER, staggered=True)
+    if name == "kda_layer":
+        return I.with_(I.KDA_LAYER, staggered=True)
+    if name.startswith("sweep:"):
+        _, B, L, rd = name.split(":")
+        return I.sweep_point(int(B), int(L), {"f16": F16, "f32": F32, "bf16": BF16}[rd])
+    raise SystemExit(f"unknown workload {name}")
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -287,7 +304,9 @@ def run_ours(args):
     cuda_build.build()
     Bd.load_library()
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = I.HEADLINE
+    w = pick_workload(args.workload)
+    recon = Bd.RECON_FFMA if args.recon == "ffma" else Bd.RECON_TENSOR
+    rb = 4 if w.ring_dtype == Bd.F32 else 2
     gen = I.generator(w.seed + rank, dev)
     wp = I.write_pos(gen, w, dev)
     c = I.cache(gen, w, wp, dev)
@@ -316,7 +335,7 @@ def run_ours(args):
         return launch_bytes(w, p, p == w.L - 1, 2, int((idx_h < 0).sum()))
 
     def step(i):
-        Bd.gdn_replayssm_decode(desc, cache, wp, None, steps_in[i % POOL], Bd.RECON_TENSOR, None, None, stream)
+        Bd.gdn_replayssm_decode(desc, cache, wp, None, steps_in[i % POOL], recon, None, None, stream)
         Bd.gdn_replayssm_advance(idx, None, w.N, w.L, wp, None, stream)
 
     for i in range(args.warmup):
@@ -327,7 +346,12 @@ def run_ours(args):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the cursors follow the advance rule, so every timed launch's bytes are
+    # known up front (no host bookkeeping inside the timed region)
     total_bytes = 0.0
+    for i in range(K):
+        total_bytes += launch_bytes_now()
+        host_advance()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -335,11 +359,9 @@ def run_ours(args):
         start.record(stream)
         for i in range(K):
             ev[i][0].record(stream)
-            Bd.gdn_replayssm_decode(desc, cache, wp, None, steps_in[i % POOL], Bd.RECON_TENSOR, None, None, stream)
+            Bd.gdn_replayssm_decode(desc, cache, wp, None, steps_in[i % POOL], recon, None, None, stream)
             ev[i][1].record(stream)
             Bd.gdn_replayssm_advance(idx, None, w.N, w.L, wp, None, stream)
-            total_bytes += launch_bytes_now()
-            host_advance()
         stop.record(stream)
         torch.cuda.synchronize()
     if ws > 1:
@@ -356,7 +378,16 @@ def run_ours(args):
     bytes_per_launch = total_bytes / K
     peak, peak_src = measured_hbm_peak()
     achieved = bytes_per_launch / mean_kern_s / 1e9
-    traffic = profiled_traffic()
+    traffic = profiled_traffic() if (args.workload == "headline" and recon == Bd.RECON_TENSOR) else None
+    if args.kernel_only:
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "recon": args.recon, "steps": K,
+                              "kernel_ms": mean_kern_s * 1e3, "ms_per_step": elapsed_ms / K,
+                              "head_steps_per_s": value, "algorithmic_bytes_per_launch": bytes_per_launch,
+                              "hbm_gbs_algorithmic": achieved, "frac": achieved / peak}))
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
 
     # in-repo packed decode on the same batches (baseline: reads and writes the state)
     pk = max(64, K // 8)
@@ -370,7 +401,8 @@ def run_ours(args):
     pb.record(stream)
     torch.cuda.synchronize()
     packed_s = pa.elapsed_time(pb) / 1e3 / pk
-    pbytes = w.B * w.HV * packed_head_step_bytes(w.K, w.V, w.HV // w.HK, 2, 2) + (rows - w.B) * w.HV * w.V * 2
+    pbytes = (w.B * w.HV * packed_head_step_bytes(w.K, w.V, w.HV // w.HK, 2, 2, w.gate == Bd.GATE_PER_K)
+              + (rows - w.B) * w.HV * w.V * 2)
 
     # end to end through the public API with host buffers: H2D of each step's
     # inputs from pinned memory, the two calls, D2H of the output, every step
@@ -393,7 +425,7 @@ def run_ours(args):
         dg.copy_(hg[j], non_blocking=True)
         db.copy_(hb[j], non_blocking=True)
         di.copy_(hi, non_blocking=True)
-        Bd.gdn_replayssm_decode(desc, cache, wp, None, e_step, Bd.RECON_TENSOR, None, None, stream)
+        Bd.gdn_replayssm_decode(desc, cache, wp, None, e_step, recon, None, None, stream)
         Bd.gdn_replayssm_advance(di, None, w.N, w.L, wp, None, stream)
         hout.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -445,6 +477,9 @@ def main():
     ap.add_argument("--steps", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=32)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="headline")
+    ap.add_argument("--recon", choices=["tensor", "ffma"], default="tensor")
+    ap.add_argument("--kernel-only", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--ref-budget", type=float, default=60.0,

@@ -15,6 +15,11 @@ cudaError_t launch_ffma_decode(const DecodeParams &P, int D, int gate, bool repl
 // checkpoint streamed by TMA.  Writes a reason into *why on a host-side failure.
 cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why);
 
+// Persistent warp-specialised variant of the above (one CTA per SM).  Returns
+// cudaErrorNotSupported, with nothing launched, when its shared-memory layout
+// does not fit the configuration.
+cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUtensorMap &map, cudaStream_t s);
+
 cudaError_t launch_fold(const DecodeParams &P, int D, int gate, int n, cudaStream_t s);
 
 cudaError_t launch_advance(const int32_t *idx, int B, const uint8_t *ff, int N, int L,

@@ -49,16 +49,23 @@ def test_kda(recon):
 
 
 @pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
-def test_head_dim_64_gqa(recon):
-    w = I.Workload("k64", N=6, B=4, HV=4, HK=1, K=64, L=8, ring_dtype=Bd.F16, qkv_dtype=Bd.F16,
-                   steps=18, staggered=True, seed=13)
+@pytest.mark.parametrize("gate,L", [(Bd.GATE_SCALAR, 8), (Bd.GATE_PER_K, 8), (Bd.GATE_PER_K, 24)],
+                         ids=["gdn_L8", "kda_L8", "kda_L24"])
+def test_head_dim_64(recon, gate, L):
+    w = I.Workload("k64", N=6, B=4, HV=4, HK=1 if gate == Bd.GATE_SCALAR else 4, K=64, L=L,
+                   ring_dtype=Bd.F16, qkv_dtype=Bd.F16, gate=gate, steps=L + 10, staggered=True, seed=13)
     run_parity(w, recon)
 
 
 @pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
-def test_longest_ring(recon):
-    w = I.Workload("L64", N=3, B=2, HV=2, HK=1, K=128, L=64, ring_dtype=Bd.F16, qkv_dtype=Bd.BF16,
-                   steps=70, seed=14)
+@pytest.mark.parametrize("ring", [Bd.F16, Bd.F32], ids=["f16", "f32"])
+@pytest.mark.parametrize("gate", [Bd.GATE_SCALAR, Bd.GATE_PER_K], ids=["gdn", "kda"])
+def test_longest_ring(recon, ring, gate):
+    """L = 64: replay depth beyond what a prep thread keeps in registers; with an
+    fp32 ring the persistent kernel's stages do not fit and the one-CTA-per-head
+    tensor-core kernel runs instead."""
+    w = I.Workload("L64", N=3, B=2, HV=2, HK=1 if gate == Bd.GATE_SCALAR else 2, K=128, L=64,
+                   ring_dtype=ring, qkv_dtype=Bd.BF16, gate=gate, steps=70, seed=14)
     rep = run_parity(w, recon)
     assert sum(s.flushes for s in rep.steps) == 2
 
