@@ -34,7 +34,7 @@ UNIT = "head-steps/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE = os.path.join(ROOT, "profiles", "gdn_replayssm_decode_tc_B256_L16.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "linear_attention_decode_gb300", "csrc", f)
-                  for f in ("gdn_tc.cu", "gdn_common.cuh")]
+                  for f in ("gdn_tcp.cu", "gdn_tc_common.cuh", "gdn_common.cuh")]
 
 
 # ---------------------------------------------------------------------------
@@ -450,7 +450,7 @@ def run_ours(args):
         "hbm_gbs_algorithmic": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "gdn_replayssm_decode (tcgen05 replay, TMA checkpoint stream)",
+                     "kernel": "tcp_decode_kernel (gdn_replayssm_decode: persistent tcgen05 replay, TMA stream)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "frac_of_8tbs": achieved / 8000.0,
                      "algorithmic_bytes_per_launch": bytes_per_launch, "kernel_ms": mean_kern_s * 1e3},

@@ -443,4 +443,37 @@ def pin_superposition():
     _close(oab, oa + ob, 1e-12, "superposition")
 
 
+def pin_q_scale_is_linear_and_l2norm_scale_free():
+    """out = alpha S q + d (k^T q) with d independent of q: the output is exactly
+    linear in q_scale.  With the in-kernel L2 norm on, rescaling the raw q and k
+    of a row by positive factors leaves every output unchanged (up to the norm's
+    epsilon)."""
+    HV, HK, K, V, L = 2, 1, 6, 4, 4
+    G = O.geom(1, HV, HK, K, V, L, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(120)
+    seq = _Seq(121, 3, HV, HK, K, V, 0)
+    S0 = r.standard_normal((HV, V, K))
+
+    def run(scale, l2, qmul=1.0, kmul=1.0):
+        cache = O.Cache(S0[None].copy(), np.full((1, HV, L, V), np.nan), np.full((1, HK, L, K), np.nan),
+                        np.full((1, HV, L), np.nan))
+        wp = np.zeros(1, dtype=np.int32)
+        outs = []
+        for t in range(3):
+            row = seq.row(t).copy()
+            row[0, :HK * K] *= qmul
+            row[0, HK * K:2 * HK * K] *= kmul
+            o, _, _ = O.replay_decode(G, cache, wp, [0], None, row, seq.g[t][None], seq.beta[t][None], scale, l2)
+            O.replay_advance(1, [0], None, L, wp)
+            outs.append(o)
+        return np.array(outs)
+
+    base = run(1.0, 0)
+    _close(run(0.37, 0)[0], 0.37 * base[0], 1e-14, "first step linear in q_scale")
+    a = run(0.5, 1, qmul=10.0, kmul=10.0)
+    b = run(0.5, 1, qmul=70.0, kmul=30.0)
+    _close(b, a, 1e-6, "L2 norm makes the output independent of q, k magnitudes")
+    assert np.max(np.abs(a - base)) > 1e-3  # the norm does change un-normalised inputs
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -59,6 +59,12 @@ MUTATIONS = [
     ("advance_off_by_one",
      "write_pos[slot] = (p == L - 1 || ff) ? 0 : p + 1;",
      "write_pos[slot] = (p == L - 2 || ff) ? 0 : p + 1;"),
+    ("q_scale_ignored",
+     "for (int c = 0; c < K; c++) q[c] *= q_scale;",
+     "for (int c = 0; c < K; c++) q[c] *= 1.0;"),
+    ("l2norm_of_q_only",
+     "for (int c = 0; c < K; c++) { q[c] /= nq; k[c] /= nk; }",
+     "for (int c = 0; c < K; c++) { q[c] /= nq; }"),
     ("f16_mantissa_width",
      "case ORACLE_F16:  return round_binary(x, 10, -14, 15);",
      "case ORACLE_F16:  return round_binary(x, 11, -14, 15);"),
