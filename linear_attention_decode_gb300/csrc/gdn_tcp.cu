@@ -2,31 +2,33 @@
 // cores.  One CTA per SM walks a round-robin share of the (row, value head)
 // items.
 //
-// Roles (448 threads):
-//   warp 0       producer: for each item, once its info stage is free, bulk-copies
-//                the first p ring entries (d, k; KDA also g) and, when aligned,
-//                the q, k, v vectors into the stage's landing zone (land barrier),
-//                then streams the fp32 checkpoint S0 [V, K] by TMA one [V x 32]
-//                box (128-byte swizzled) at a time through a ring of NB box slots
-//                (box_full / box_empty barriers);
-//   warp 1       allocates 2 x K TMEM columns (two accumulators) and issues the
-//                replay contraction tcgen05.mma for each item into one of them;
-//   warps 2-9    two prep warpgroups taking alternate items: from the landing
-//                zone they compute the replay decays and write the two K-major
-//                operand tiles ([P1] Design 1 and 7)
+// Roles (544 threads):
+//   warp 0       producer: streams each item's fp32 checkpoint S0 [V, K] by TMA,
+//                one [V x 32] box (128-byte swizzled) at a time, through a ring
+//                of NB box slots (box_full / box_empty); it also allocates the
+//                2 x K TMEM columns (two accumulators);
+//   warps 1-8    two prep warpgroups taking alternate items.  A group's leader
+//                bulk-copies the first p ring entries (d, k; KDA also g) and,
+//                when aligned, q, k, v of its items two group-items ahead into
+//                the group's landing slots (land_full).  From a landed slot the
+//                group computes the replay decays and the two K-major operand tiles
+//                ([P1] Design 1 and 7)
 //                      GDN  A[v][j] = w_j d_j[v],  B[c][j] = k_j[c]
 //                      KDA  A[v][j] = d_j[v],      B[c][j] = w_j[c] k_j[c]
-//                plus the epilogue's vectors (info_full barrier);
-//   warps 10-13  epilogue: thread r owns state row r (TMEM lane r).  It adds
-//                A S0[r][:] (KDA: S0[r][:] o A) to dS[r][:] from TMEM, contracts
-//                with q and k in registers, writes out[r] = alpha Sq + d (k^T q)
-//                with d = beta (v - alpha Sk); a flush item rewrites its box rows
-//                with alpha S + d k^T and TMA-stores them, otherwise (d, k, g) are
-//                appended to the ring.  It then frees the stage (info_empty).
+//                plus the epilogue's vectors, written into an info stage
+//                (info_full / info_empty); the group leader then issues the
+//                replay contraction tcgen05.mma into the group's accumulator;
+//   warps 9-16   two epilogue warpgroups, group g taking the items of prep group
+//                g and reading accumulator g: thread r owns state row r (TMEM
+//                lane r).  It adds A S0[r][:] (KDA: S0[r][:] o A) to dS[r][:],
+//                contracts with q and k in registers (packed fp32x2 FMAs), writes
+//                out[r] = alpha Sq + d (k^T q) with d = beta (v - alpha Sk); a
+//                flush item rewrites its box rows with alpha S + d k^T and
+//                TMA-stores them, otherwise (d, k, g) are appended to the ring.
 // Every wait is bounded: a wait that runs out raises a CTA-wide abort flag and
 // GDN_DEV_TIMEOUT; all roles then leave their loops, the producer and the MMA
-// thread wait (bounded) for their own copies and contraction still in flight,
-// and the CTA frees its TMEM and returns.
+// issuers wait (bounded) for their own copies and contractions still in
+// flight, and the CTA frees its TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include "gdn_common.cuh"
@@ -35,25 +37,30 @@
 
 namespace gdn {
 
-constexpr int kTcpThreads = 448;
-constexpr int kItemsMax = 256;  // items one CTA may own (sets the table size)
+constexpr int kTcpThreads = 544;  // 17 warps
+constexpr int kItemsMax = 256;    // items one CTA may own (sets the table size)
 #ifndef GDN_TCP_STAGES
-#define GDN_TCP_STAGES 3  // info stages (operand tiles + landing zone) in flight
+#define GDN_TCP_STAGES 3  // info stages (operand tiles + epilogue vectors)
+#endif
+#ifndef GDN_TCP_LANDING
+#define GDN_TCP_LANDING 4  // landing slots (raw ring rows and q/k/v)
 #endif
 
-
 struct TcpLayout {
-  int KD, KC, NI, NB;
+  int KD, KC, NI, NL, NB;
   int qkv_bulk;  // 1: q, k, v arrive by bulk copy (16-byte aligned rows)
-  uint32_t box_bytes, stage_bytes;
-  uint32_t off_stage, off_table, off_bars, total;
-  // offsets inside an info stage
-  uint32_t st_A, st_B, st_f, st_ld, st_lk, st_lg, st_lq;
+  uint32_t box_bytes, stage_bytes, land_bytes;
+  uint32_t off_stage, off_land, off_table, off_bars, total;
+  uint32_t st_A, st_B, st_f;        // inside an info stage
+  uint32_t ld_d, ld_k, ld_g, ld_q;  // inside a landing slot
 };
 
-// Shared memory: NB checkpoint boxes | NI info stages | item table | barriers.
-// An info stage: A tile | B tile | fp32 vectors | landing zone (d rows, k rows,
-// KDA g rows, q k v).
+// Epilogue vectors of an item (floats): q, k, v for GDN; KDA adds a o k, a, the
+// total decay per channel and the current log-gate.  Then 8 scalars.
+__host__ __device__ inline int field_floats(int D, int gate) { return (gate == GDN_GATE_PER_K ? 7 : 3) * D + 8; }
+
+// Shared memory: NB checkpoint boxes | NI info stages | NL landing slots | item
+// table | barriers.
 static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, int qkv_bytes, int qkv_bulk,
                             int smem_budget) {
   TcpLayout t{};
@@ -67,40 +74,59 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
   t.st_A = 0;
   t.st_B = (uint32_t)(128 * t.KD * es);
   t.st_f = t.st_B + (uint32_t)(D * t.KD * es);
-  t.st_ld = t.st_f + (uint32_t)(7 * D + 144) * 4;
-  t.st_lk = t.st_ld + (uint32_t)(depth * D * ring_bytes);
-  t.st_lg = t.st_lk + (uint32_t)(depth * D * ring_bytes);
-  t.st_lq = t.st_lg + (uint32_t)(gate == GDN_GATE_PER_K ? depth * D * 4 : 0);
-  t.stage_bytes = t.st_lq + (uint32_t)(qkv_bulk ? 3 * D * qkv_bytes : 0);
-  t.stage_bytes = (t.stage_bytes + 127) & ~127u;
-  const uint32_t table = (uint32_t)kItemsMax * 8;
-  const uint32_t bars = 512;
+  t.stage_bytes = (t.st_f + (uint32_t)field_floats(D, gate) * 4 + 127) & ~127u;
+  t.ld_d = 0;
+  t.ld_k = t.ld_d + (uint32_t)(depth * D * ring_bytes);
+  t.ld_g = t.ld_k + (uint32_t)(depth * D * ring_bytes);
+  t.ld_q = t.ld_g + (uint32_t)(gate == GDN_GATE_PER_K ? depth * D * 4 : 0);
+  t.land_bytes = (t.ld_q + (uint32_t)(qkv_bulk ? 3 * D * qkv_bytes : 0) + 127) & ~127u;
+  const uint32_t table = (uint32_t)kItemsMax * 8 + (uint32_t)kItemsMax * 4;  // table + live list
+  const uint32_t bars = 640;
   t.NI = GDN_TCP_STAGES;
-  const long rest = (long)smem_budget - (long)t.NI * t.stage_bytes - table - bars;
+  t.NL = GDN_TCP_LANDING;
+  const long rest = (long)smem_budget - (long)t.NI * t.stage_bytes - (long)t.NL * t.land_bytes - table - bars;
   t.NB = rest > 0 ? (int)(rest / t.box_bytes) : 0;
   if (t.NB > 16) t.NB = 16;
   t.off_stage = (uint32_t)t.NB * t.box_bytes;
-  t.off_table = t.off_stage + (uint32_t)t.NI * t.stage_bytes;
+  t.off_land = t.off_stage + (uint32_t)t.NI * t.stage_bytes;
+  t.off_table = t.off_land + (uint32_t)t.NL * t.land_bytes;
   t.off_bars = t.off_table + table;
   t.total = t.off_bars + bars;
   return t;
 }
 
 struct TcpBars {
-  uint32_t box_full, box_empty, land, info_full, info_empty, tmem_full, tmem_empty;
+  uint32_t box_full, box_empty, land_full, info_full, info_empty, tmem_full, tmem_empty, flush;
   __device__ uint32_t bf(int i) const { return box_full + 8 * i; }
   __device__ uint32_t be(int i) const { return box_empty + 8 * i; }
-  __device__ uint32_t ld(int i) const { return land + 8 * i; }
+  __device__ uint32_t lf(int i) const { return land_full + 8 * i; }
   __device__ uint32_t inf(int i) const { return info_full + 8 * i; }
   __device__ uint32_t ine(int i) const { return info_empty + 8 * i; }
   __device__ uint32_t tf(int i) const { return tmem_full + 8 * i; }
   __device__ uint32_t te(int i) const { return tmem_empty + 8 * i; }
+  __device__ uint32_t fl(int i) const { return flush + 8 * i; }
 };
 
 // Bounded wait that also gives up when another thread raised the abort flag.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                         uint32_t *status);
+
+// The same for a whole warp: lane 0 polls, the warp follows with its verdict
+// (fewer threads hammering the barrier unit).
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                              uint32_t *status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+
+// A completed phase is caught by the non-blocking test: a blocking try_wait on
+// a phase that is already complete was measured at ~240 ns on GB300.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                          uint32_t *status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -111,23 +137,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       return false;
     }
   }
-}
-
-// Sum of x and y over one 128-thread warpgroup (named barrier `bar_id`).
-__device__ __forceinline__ float2 group_sum2(float x, float y, float *red, uint32_t bar_id, int pt) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    x += __shfl_xor_sync(0xffffffffu, x, o);
-    y += __shfl_xor_sync(0xffffffffu, y, o);
-  }
-  if ((pt & 31) == 0) {
-    red[pt >> 5] = x;
-    red[4 + (pt >> 5)] = y;
-  }
-  named_bar_sync(bar_id, 128);
-  float2 r = make_float2((red[0] + red[1]) + (red[2] + red[3]), (red[4] + red[5]) + (red[6] + red[7]));
-  named_bar_sync(bar_id, 128);
-  return r;
 }
 
 template <int KIND>
@@ -164,6 +173,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   constexpr int NBOX = D / 32;
   constexpr int BOX_BYTES = D * 128;
   constexpr int RB = RING_DT == GDN_F32 ? 4 : 2;
+  constexpr int NF = GATE == GDN_GATE_PER_K ? 7 : 3;  // epilogue vectors per item
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -173,7 +183,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   const int T = P.B * P.HV;
   const int G = gridDim.x;
   const int n = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / G + 1 : 0;
-  const int NB = lay.NB, NI = lay.NI;
+  const int NB = lay.NB, NI = lay.NI, NL = lay.NL;
   const int qes = P.qkv_dtype == GDN_F32 ? 4 : 2;
 
   if (smem_addr(smem) & 1023u) {  // the 128-byte swizzle assumes a 1024-byte aligned base
@@ -183,19 +193,19 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   int2 *table = reinterpret_cast<int2 *>(smem + lay.off_table);
   uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + lay.off_bars);
   const uint32_t bar0 = smem_addr(bar_mem);
-  const TcpBars bars{bar0,
-                     bar0 + 8u * NB,
-                     bar0 + 16u * NB,
-                     bar0 + 16u * NB + 8u * NI,
-                     bar0 + 16u * NB + 16u * NI,
-                     bar0 + 16u * NB + 24u * NI,
-                     bar0 + 16u * NB + 24u * NI + 16u};
-  // Two flush barriers, used by alternate flush items: an epilogue thread can
-  // run one item ahead of another, and its arrival for the next flush item must
-  // not count toward the current one.
-  const uint32_t flush_bar0 = bar0 + 16u * NB + 24u * NI + 32u;
-  // misc[0] TMEM base, misc[1] abort flag, misc[2..3] prep-group go/stop words
-  uint32_t *misc = reinterpret_cast<uint32_t *>(bar_mem + 2 * NB + 3 * NI + 6);
+  TcpBars bars;
+  bars.box_full = bar0;
+  bars.box_empty = bars.box_full + 8u * NB;
+  bars.land_full = bars.box_empty + 8u * NB;
+  bars.info_full = bars.land_full + 8u * NL;
+  bars.info_empty = bars.info_full + 8u * NI;
+  bars.tmem_full = bars.info_empty + 8u * NI;
+  bars.tmem_empty = bars.tmem_full + 16u;
+  bars.flush = bars.tmem_empty + 16u;  // two per epilogue group (see the epilogue)
+  // misc[0] TMEM base, misc[1] abort flag, misc[2..3] prep-group go/stop words,
+  // misc[4] number of live items
+  uint32_t *misc = reinterpret_cast<uint32_t *>(bar_mem + 2 * NB + NL + 2 * NI + 8);
+  int *live_j = reinterpret_cast<int *>(table + kItemsMax);  // j of the li-th live item
   volatile uint32_t *abort_flag = misc + 1;
 
   // --- item table: slot, cursor, flush decision of every item of this CTA ---
@@ -210,8 +220,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       mbar_init(bars.bf(i), 1);
       mbar_init(bars.be(i), 128);
     }
+    for (int i = 0; i < NL; ++i) mbar_init(bars.lf(i), 1);
     for (int i = 0; i < NI; ++i) {
-      mbar_init(bars.ld(i), 1);
       mbar_init(bars.inf(i), 1);
       mbar_init(bars.ine(i), 128);
     }
@@ -219,58 +229,45 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       mbar_init(bars.tf(i), 1);
       mbar_init(bars.te(i), 128);
     }
-    mbar_init(flush_bar0, 128);
-    mbar_init(flush_bar0 + 8u, 128);
+    for (int i = 0; i < 4; ++i) mbar_init(bars.fl(i), 128);
     misc[1] = 0u;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 0) {
     tmem_alloc(smem_addr(misc), 2 * D);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (warp == 0) {  // live items in order: live_j[li] = table index of the li-th live item
+    int cnt = 0;
+    for (int base = 0; base < n; base += 32) {
+      const bool live = base + lane < n && (table[base + lane].y & 512);
+      const uint32_t m = __ballot_sync(0xffffffffu, live);
+      if (live) live_j[cnt + __popc(m & ((1u << lane) - 1u))] = base + lane;
+      cnt += __popc(m);
+    }
+    if (lane == 0) misc[4] = (uint32_t)cnt;
+  }
+  __syncthreads();
   const uint32_t tmem = misc[0];
   uint8_t *boxes = smem;
   uint8_t *stages = smem + lay.off_stage;
+  uint8_t *lands = smem + lay.off_land;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&tmap);
       uint32_t use = 0;
-      int li = 0, land_issued = 0;
+      int li = 0;
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
         const int2 e = table[j];
         if (!(e.y & 512)) continue;
-        const int item = (int)blockIdx.x + j * G, b = item / P.HV, hv = item % P.HV, hk = hv / P.G;
-        const int p = e.y & 255, slot = e.x, s = li % NI;
-        const uint32_t u = (uint32_t)(li / NI);
-        // landing zone of the item's info stage
-        if (u > 0 && !(ok = wait_bar(bars.ine(s), (u - 1) & 1, abort_flag, P.status))) break;
-        uint8_t *st = stages + s * lay.stage_bytes;
-        const uint32_t ring_bytes = (uint32_t)(p * D * RB);
-        const uint32_t gbytes = GATE == GDN_GATE_PER_K ? (uint32_t)(p * D * 4) : 0u;
-        const uint32_t qbytes = lay.qkv_bulk ? (uint32_t)(3 * D * qes) : 0u;
-        mbar_arrive_expect_tx(bars.ld(s), 2 * ring_bytes + gbytes + qbytes);
-        if (p > 0) {
-          const int64_t drow = ((int64_t)slot * P.HV + hv) * P.L;
-          const int64_t krow = ((int64_t)slot * P.HK + hk) * P.L;
-          bulk_load(smem_addr(st + lay.st_ld), (const uint8_t *)P.ring_d + drow * D * RB, ring_bytes, bars.ld(s));
-          bulk_load(smem_addr(st + lay.st_lk), (const uint8_t *)P.ring_k + krow * D * RB, ring_bytes, bars.ld(s));
-          if (GATE == GDN_GATE_PER_K)
-            bulk_load(smem_addr(st + lay.st_lg), P.ring_g + drow * D, gbytes, bars.ld(s));
-        }
-        if (lay.qkv_bulk) {
-          const uint8_t *row = (const uint8_t *)P.qkv + (int64_t)b * P.qkv_stride * qes;
-          const uint32_t vb = (uint32_t)(D * qes);
-          bulk_load(smem_addr(st + lay.st_lq), row + (int64_t)hk * vb, vb, bars.ld(s));
-          bulk_load(smem_addr(st + lay.st_lq + vb), row + ((int64_t)P.HK + hk) * vb, vb, bars.ld(s));
-          bulk_load(smem_addr(st + lay.st_lq + 2 * vb), row + (2 * (int64_t)P.HK + hv) * vb, vb, bars.ld(s));
-        }
-        ++land_issued;
+        const int hv = ((int)blockIdx.x + j * G) % P.HV;
+        const int slot = e.x;
         // checkpoint boxes
         const int row0 = (slot * P.HV + hv) * D;
         for (int c = 0; c < NBOX; ++c, ++use) {
@@ -282,65 +279,71 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         }
         ++li;
       }
-      if (*abort_flag) {  // let this thread's copies still in flight land first
+      if (*abort_flag)  // let this thread's copies still in flight land first
         for (uint32_t k = use > (uint32_t)NB ? use - NB : 0u; k < use; ++k)
           mbar_wait_bounded(bars.bf((int)(k % NB)), (k / NB) & 1, kWaitLimitNs);
-        for (int k = land_issued > NI ? land_issued - NI : 0; k < land_issued; ++k)
-          mbar_wait_bounded(bars.ld(k % NI), (uint32_t)(k / NI) & 1, kWaitLimitNs);
-      }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = make_idesc(KIND, D);
-      const uint32_t sbo = (uint32_t)lay.KC * 128;
-      int li = 0;
-      for (int j = 0; j < n; ++j) {
-        const int2 e = table[j];
-        if (!(e.y & 512)) continue;
-        const int p = e.y & 255, s = li % NI, tb = li & 1;
-        const uint32_t u = (uint32_t)(li / NI), ut = (uint32_t)(li >> 1);
-        if (!wait_bar(bars.inf(s), u & 1, abort_flag, P.status)) break;
-        if (ut > 0 && !wait_bar(bars.te(tb), (ut - 1) & 1, abort_flag, P.status)) break;
-        tc_fence_after();
-        if (p > 0) {
-          const uint32_t a0 = smem_addr(stages + s * lay.stage_bytes + lay.st_A);
-          const uint32_t b0 = smem_addr(stages + s * lay.stage_bytes + lay.st_B);
-          const int nsteps = (p + KSTEP - 1) / KSTEP;
-          for (int i = 0; i < nsteps; ++i)
-            tc_mma<KIND == 2 ? 1 : 0>(tmem + tb * D, make_sdesc(a0 + 256 * i, 128, sbo),
-                                      make_sdesc(b0 + 256 * i, 128, sbo), idesc, i > 0 ? 1u : 0u);
-          tc_commit(bars.tf(tb));
-        } else {
-          mbar_arrive(bars.tf(tb));
-        }
-        ++li;
+  } else if (warp < 9) {
+    // ------------------------------------------------------------ prep + MMA
+    // Group pg takes the live items with li % 2 == pg; its leader also issues
+    // the item's contraction into TMEM accumulator pg.
+    const int pg = (warp - 1) >> 2;
+    const int pt = tid - 32 - 128 * pg;  // 0..127: operand row / key channel
+    const uint32_t bar_id = 1 + pg;
+    const uint32_t idesc = make_idesc(KIND, D);
+    volatile uint32_t *go = misc + 2 + pg;
+    bool leader_ok = true;  // leader only: false after a wait ran out
+    int li = 0, nmma = 0, land_next = pg;  // leader: next live item to land
+    const int nlive = (int)misc[4];
+    // The group's landing slots (li % NL with NL = 4: two per group) are filled
+    // by its own leader two group-items ahead: right after the group has read a
+    // slot, the copies for the item that uses it next are issued.
+    auto land = [&](int lj) {
+      const int jl = live_j[lj];
+      const int2 el = table[jl];
+      const int itl = (int)blockIdx.x + jl * G, bl = itl / P.HV, hvl = itl % P.HV, hkl = hvl / P.G;
+      const int pl = el.y & 255, sl = el.x, l = lj % NL;
+      uint8_t *ld = lands + l * lay.land_bytes;
+      const uint32_t ring_bytes = (uint32_t)(pl * D * RB);
+      const uint32_t gbytes = GATE == GDN_GATE_PER_K ? (uint32_t)(pl * D * 4) : 0u;
+      const uint32_t qbytes = lay.qkv_bulk ? (uint32_t)(3 * D * qes) : 0u;
+      mbar_arrive_expect_tx(bars.lf(l), 2 * ring_bytes + gbytes + qbytes);
+      if (pl > 0) {
+        const int64_t drow = ((int64_t)sl * P.HV + hvl) * P.L;
+        const int64_t krow = ((int64_t)sl * P.HK + hkl) * P.L;
+        bulk_load(smem_addr(ld + lay.ld_d), (const uint8_t *)P.ring_d + drow * D * RB, ring_bytes, bars.lf(l));
+        bulk_load(smem_addr(ld + lay.ld_k), (const uint8_t *)P.ring_k + krow * D * RB, ring_bytes, bars.lf(l));
+        if (GATE == GDN_GATE_PER_K) bulk_load(smem_addr(ld + lay.ld_g), P.ring_g + drow * D, gbytes, bars.lf(l));
       }
-      if (*abort_flag && li > 0)  // the last contraction must finish before TMEM is freed
-        mbar_wait_bounded(bars.tf((li - 1) & 1), (uint32_t)((li - 1) >> 1) & 1, kWaitLimitNs);
-    }
-  } else if (warp < 10) {
-    // ------------------------------------------------------------ prep (2 groups)
-    const int grp = (warp - 2) >> 2;
-    const int pt = tid - 64 - 128 * grp;
-    const uint32_t bar_id = 1 + grp;
-    int li = 0;
+      if (lay.qkv_bulk) {
+        const uint8_t *row = (const uint8_t *)P.qkv + (int64_t)bl * P.qkv_stride * qes;
+        const uint32_t vb = (uint32_t)(D * qes);
+        bulk_load(smem_addr(ld + lay.ld_q), row + (int64_t)hkl * vb, vb, bars.lf(l));
+        bulk_load(smem_addr(ld + lay.ld_q + vb), row + ((int64_t)P.HK + hkl) * vb, vb, bars.lf(l));
+        bulk_load(smem_addr(ld + lay.ld_q + 2 * vb), row + (2 * (int64_t)P.HK + hvl) * vb, vb, bars.lf(l));
+      }
+    };
+    if (pt == 0)
+      for (; land_next < nlive && land_next < pg + NL; land_next += 2) land(land_next);
     for (int j = 0; j < n; ++j) {
       const int2 e = table[j];
       if (!(e.y & 512)) continue;
-      if ((li & 1) != grp) {
+      if ((li & 1) != pg) {
         ++li;
         continue;
       }
-      const int p = e.y & 255, slot = e.x, s = li % NI;
-      const uint32_t u = (uint32_t)(li / NI);
+      const int p = e.y & 255, slot = e.x, s = li % NI, l = li % NL;
+      const uint32_t u = (uint32_t)(li / NI), ul = (uint32_t)(li / NL);
       const int item = (int)blockIdx.x + j * G, b = item / P.HV, hv = item % P.HV, hk = hv / P.G;
       const int64_t bh = (int64_t)b * P.HV + hv;
-      // small loads first, so their latency overlaps the landing wait
-      float gc = 0.f, gj = 0.f, qv = 0.f, kv = 0.f, vv = 0.f;
+      // small loads first, so their latency overlaps the waits
+      float gc = 0.f, qv = 0.f, kv = 0.f, vv = 0.f, g_lo = 0.f, g_hi = 0.f;
       if (GATE == GDN_GATE_SCALAR) {
         gc = P.g[bh];
-        if (pt < p) gj = P.ring_g[((int64_t)slot * P.HV + hv) * P.L + pt];
+        // every warp holds the cursor's log-gates: lane l has entries l and l + 32
+        const float *grow = P.ring_g + ((int64_t)slot * P.HV + hv) * P.L;
+        if (lane < p) g_lo = grow[lane];
+        if (lane + 32 < p) g_hi = grow[lane + 32];
       } else if (pt < D) {
         gc = P.g[bh * D + pt];
       }
@@ -351,54 +354,95 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         kv = load_as_f32(P.qkv, qbase + (int64_t)P.HK * D + (int64_t)hk * D + pt, P.qkv_dtype);
         vv = load_as_f32(P.qkv, qbase + 2 * (int64_t)P.HK * D + (int64_t)hv * D + pt, P.qkv_dtype);
       }
-      // Only the group leader waits for the landing zone; the go/stop word it
-      // leaves before the group barrier keeps every later group barrier uniform.
-      volatile uint32_t *go = misc + 2 + grp;
-      if (pt == 0) *go = wait_bar(bars.ld(s), u & 1, abort_flag, P.status) ? 1u : 0u;
+      // Only the leader waits (landing slot filled, info stage free); the
+      // go/stop word it leaves before the group barrier makes the whole group
+      // leave together, so the group's barriers stay uniform.
+      if (pt == 0)
+        *go = (leader_ok && wait_bar(bars.lf(l), ul & 1, abort_flag, P.status) &&
+               (u == 0 || wait_bar(bars.ine(s), (u - 1) & 1, abort_flag, P.status)))
+                  ? 1u
+                  : 0u;
       named_bar_sync(bar_id, 128);
       if (*go == 0u) break;
       uint8_t *st = stages + s * lay.stage_bytes;
       uint8_t *tA = st + lay.st_A, *tB = st + lay.st_B;
       float *f = reinterpret_cast<float *>(st + lay.st_f);
-      float *fq = f, *fk = f + D, *fke = f + 2 * D, *fa = f + 3 * D, *fA = f + 4 * D, *fv = f + 5 * D,
-            *fg = f + 6 * D, *gsc = f + 7 * D, *wsc = gsc + 64, *scal = wsc + 64, *red = scal + 8;
-      const uint8_t *land_d = st + lay.st_ld, *land_k = st + lay.st_lk;
-      const float *land_g = reinterpret_cast<const float *>(st + lay.st_lg);
+      float *fq = f, *fk = f + D, *fv = f + 2 * D, *fke = f + 3 * D, *fa = f + 4 * D, *fA = f + 5 * D,
+            *fg = f + 6 * D, *scal = f + NF * D;
+      const uint8_t *ld = lands + l * lay.land_bytes;
+      const uint8_t *land_d = ld + lay.ld_d, *land_k = ld + lay.ld_k, *lq = ld + lay.ld_q;
+      const float *land_g = reinterpret_cast<const float *>(ld + lay.ld_g);
       if (lay.qkv_bulk && pt < D) {
-        const uint8_t *lq = st + lay.st_lq;
         qv = load_as_f32(lq, pt, P.qkv_dtype);
         kv = load_as_f32(lq, D + pt, P.qkv_dtype);
         vv = load_as_f32(lq, 2 * D + pt, P.qkv_dtype);
       }
+      // q.q, k.k and k.q over the head, computed redundantly by every warp (no
+      // group barrier): lane l takes the channels l, l + 32, ...
+      float qq = 0.f, kk = 0.f, kq = 0.f;
+      for (int c = lane; c < D; c += 32) {
+        float qc, kc;
+        if (lay.qkv_bulk) {
+          qc = load_as_f32(lq, c, P.qkv_dtype);
+          kc = load_as_f32(lq, D + c, P.qkv_dtype);
+        } else {
+          const int64_t qbase = (int64_t)b * P.qkv_stride;
+          qc = load_as_f32(P.qkv, qbase + (int64_t)hk * D + c, P.qkv_dtype);
+          kc = load_as_f32(P.qkv, qbase + (int64_t)P.HK * D + (int64_t)hk * D + c, P.qkv_dtype);
+        }
+        qq = fmaf(qc, qc, qq);
+        kk = fmaf(kc, kc, kk);
+        kq = fmaf(kc, qc, kq);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        qq += __shfl_xor_sync(0xffffffffu, qq, o);
+        kk += __shfl_xor_sync(0xffffffffu, kk, o);
+        kq += __shfl_xor_sync(0xffffffffu, kq, o);
+      }
       if (P.qk_l2norm) {
-        const float2 nn = group_sum2(qv * qv, kv * kv, red, bar_id, pt);
-        qv = qv / sqrtf(nn.x + 1e-6f);
-        kv = kv / sqrtf(nn.y + 1e-6f);
+        const float nq = sqrtf(qq + 1e-6f), nk = sqrtf(kk + 1e-6f);
+        qv = qv / nq;
+        kv = kv / nk;
+        kq = kq / (nq * nk);
       }
       qv *= P.q_scale;
-      if (GATE == GDN_GATE_SCALAR && pt < p) gsc[pt] = gj;
-      const float kq = group_sum2(kv * qv, 0.f, red, bar_id, pt).x;  // also publishes gsc
+      kq *= P.q_scale;
 
       float A = 1.f;
       if (GATE == GDN_GATE_SCALAR) {
-        // w_j = exp(sum_{j<i<p} g_i), summed from the newest entry backwards
-        if (pt < p) {
-          float sfx = 0.f;
-          for (int i = p - 1; i > pt; --i) sfx += gsc[i];
-          wsc[pt] = expf(sfx);
-          if (pt == 0) scal[2] = expf(sfx + gsc[0]);
+        // Suffix sums of the log-gates by a warp scan (each warp on its own):
+        // afterwards lane l holds T_l = sum_{l<=i<p} g_i; w_j = exp(T_{j+1}),
+        // A = exp(T_0).
+        float t_lo = g_lo, t_hi = g_hi;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float a = __shfl_down_sync(0xffffffffu, t_hi, o);
+          if (lane + o < 32) t_hi += a;
         }
-        named_bar_sync(bar_id, 128);
-        if (p > 0) A = scal[2];
+        const float hi_total = __shfl_sync(0xffffffffu, t_hi, 0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float a = __shfl_down_sync(0xffffffffu, t_lo, o);
+          if (lane + o < 32) t_lo += a;
+        }
+        t_lo += hi_total;
+        A = p > 0 ? expf(__shfl_sync(0xffffffffu, t_lo, 0)) : 1.f;
+        // w for entry j lives in lane j (lo: j < 32, hi: j >= 32)
+        const float nxt_lo = __shfl_down_sync(0xffffffffu, t_lo, 1);
+        const float w_lo = expf(lane == 31 ? hi_total : nxt_lo);
+        const float nxt_hi = __shfl_down_sync(0xffffffffu, t_hi, 1);
+        const float w_hi = expf(lane == 31 ? 0.f : nxt_hi);
         // A row pt: w_j d_j[pt];  B row pt: k_j[pt]
         for (int h = 0; h < lay.KC; ++h) {
           float xa[EPC], xb[EPC];
 #pragma unroll
           for (int e2 = 0; e2 < EPC; ++e2) {
             const int jj = h * EPC + e2;
+            const float wj = __shfl_sync(0xffffffffu, jj < 32 ? w_lo : w_hi, jj & 31);
             xa[e2] = xb[e2] = 0.f;
             if (jj < p && pt < D) {
-              xa[e2] = wsc[jj] * load_as_f32(land_d, (int64_t)jj * D + pt, RING_DT);
+              xa[e2] = wj * load_as_f32(land_d, (int64_t)jj * D + pt, RING_DT);
               xb[e2] = load_as_f32(land_k, (int64_t)jj * D + pt, RING_DT);
             }
           }
@@ -429,57 +473,102 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       }
       // Epilogue inputs.
       if (pt < D) {
-        const float at = GATE == GDN_GATE_PER_K ? expf(gc) : 1.f;
-        fq[pt] = GATE == GDN_GATE_PER_K ? at * qv : qv;
         fk[pt] = kv;
-        fke[pt] = GATE == GDN_GATE_PER_K ? at * kv : kv;
-        fa[pt] = at;
-        fA[pt] = A;
         fv[pt] = vv;
-        fg[pt] = gc;
+        if (GATE == GDN_GATE_PER_K) {
+          const float at = expf(gc);
+          fq[pt] = at * qv;
+          fke[pt] = at * kv;
+          fa[pt] = at;
+          fA[pt] = A;
+          fg[pt] = gc;
+        } else {
+          fq[pt] = qv;
+        }
       }
       if (pt == 0) {
         scal[0] = GATE == GDN_GATE_SCALAR ? expf(gc) : 1.f;
         scal[1] = beta;
         scal[2] = A;
         scal[3] = kq;
+        scal[4] = gc;
       }
       fence_proxy_async_smem();
       named_bar_sync(bar_id, 128);
-      if (pt == 0) mbar_arrive(bars.inf(s));
+      if (pt == 0) {
+        // the landing slot has been read: fill it for the item that uses it next
+        if (land_next < nlive) {
+          land(land_next);
+          land_next += 2;
+        }
+        mbar_arrive(bars.inf(s));
+        // contraction into accumulator pg once the epilogue has read it out
+        const uint32_t ut = (uint32_t)(li >> 1);
+        if (ut > 0 && !wait_bar(bars.te(pg), (ut - 1) & 1, abort_flag, P.status)) {
+          leader_ok = false;
+        } else {
+          tc_fence_after();
+          if (p > 0) {
+            const uint32_t a0 = smem_addr(tA), b0 = smem_addr(tB);
+            const uint32_t sbo = (uint32_t)lay.KC * 128;
+            const int nsteps = (p + KSTEP - 1) / KSTEP;
+            for (int i = 0; i < nsteps; ++i)
+              tc_mma<KIND == 2 ? 1 : 0>(tmem + pg * D, make_sdesc(a0 + 256 * i, 128, sbo),
+                                        make_sdesc(b0 + 256 * i, 128, sbo), idesc, i > 0 ? 1u : 0u);
+            tc_commit(bars.tf(pg));
+          } else {
+            mbar_arrive(bars.tf(pg));
+          }
+          ++nmma;
+        }
+      }
       ++li;
     }
+    // an aborted CTA lets its last contraction and its landings finish first
+    if (pt == 0 && *abort_flag) {
+      if (nmma > 0) mbar_wait_bounded(bars.tf(pg), (uint32_t)(nmma - 1) & 1, kWaitLimitNs);
+      for (int k = land_next - 2; k >= 0 && k >= land_next - NL; k -= 2)
+        mbar_wait_bounded(bars.lf(k % NL), (uint32_t)(k / NL) & 1, kWaitLimitNs);
+    }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (2 groups)
+    // Group eg takes the items with li % 2 == eg and reads TMEM accumulator eg.
+    const int eg = (warp - 9) >> 2;
+    const int etid = tid - 288 - 128 * eg;  // 0 is the group's store thread
     const int q4 = warp & 3;
     const int r = 32 * q4 + lane;  // state row = TMEM lane
     const bool row_live = r < D;   // warp-uniform
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     int li = 0;
-    uint32_t use = 0, nflush = 0;
+    uint32_t nflush = 0;
     for (int j = 0; j < n; ++j) {
       const int2 e = table[j];
       const int item = (int)blockIdx.x + j * G, b = item / P.HV, hv = item % P.HV;
       const int64_t bh = (int64_t)b * P.HV + hv;
       if (!(e.y & 512)) {
-        if (row_live) store_from_f32(P.out, bh * D + r, P.out_dtype, 0.f);
+        if ((j & 1) == eg && row_live) store_from_f32(P.out, bh * D + r, P.out_dtype, 0.f);
+        continue;
+      }
+      if ((li & 1) != eg) {
+        ++li;
         continue;
       }
       const int p = e.y & 255, slot = e.x, flush = (e.y >> 8) & 1, s = li % NI, tb = li & 1;
       const uint32_t u = (uint32_t)(li / NI), ut = (uint32_t)(li >> 1);
-      if (!wait_bar(bars.inf(s), u & 1, abort_flag, P.status)) break;
-      if (!wait_bar(bars.tf(tb), ut & 1, abort_flag, P.status)) break;
+      const uint32_t use = (uint32_t)(NBOX * li);
+      if (!wait_bar_warp(bars.inf(s), u & 1, abort_flag, P.status)) break;
+      if (!wait_bar_warp(bars.tf(tb), ut & 1, abort_flag, P.status)) break;
       tc_fence_after();
       const float *f = reinterpret_cast<const float *>(stages + s * lay.stage_bytes + lay.st_f);
-      const float *fq = f, *fk = f + D, *fke = f + 2 * D, *fa = f + 3 * D, *fA = f + 4 * D, *fv = f + 5 * D,
-                  *fg = f + 6 * D, *scal = f + 7 * D + 128;
+      const float *fq = f, *fk = f + D, *fv = f + 2 * D, *fke = GATE == GDN_GATE_PER_K ? f + 3 * D : fk,
+                  *fa = f + 4 * D, *fA = f + 5 * D, *fg = f + 6 * D, *scal = f + NF * D;
       const float alpha = scal[0], beta = scal[1], A = scal[2], kq = scal[3];
       const uint32_t trow = tmem + tb * D + lane_off;
-      float sq[4] = {0.f, 0.f, 0.f, 0.f}, sk[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 sq01 = make_float2(0.f, 0.f), sq23 = sq01, sk01 = sq01, sk23 = sq01;
       bool ok = true;
       for (int c = 0; c < NBOX; ++c) {
         const int bs = (int)((use + c) % NB);
-        if (!(ok = wait_bar(bars.bf(bs), ((use + c) / NB) & 1, abort_flag, P.status))) break;
+        if (!(ok = wait_bar_warp(bars.bf(bs), ((use + c) / NB) & 1, abort_flag, P.status))) break;
         if (row_live) {
           float acc[32];
           if (p > 0) {
@@ -495,23 +584,25 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
             const int col = 32 * c + 4 * jc;
             const float4 q4v = *reinterpret_cast<const float4 *>(fq + col);
             const float4 k4v = *reinterpret_cast<const float4 *>(fke + col);
-            float4 A4 = make_float4(A, A, A, A);
-            if (GATE == GDN_GATE_PER_K) A4 = *reinterpret_cast<const float4 *>(fA + col);
-            const float e0 = fmaf(A4.x, x.x, acc[4 * jc + 0]);
-            const float e1 = fmaf(A4.y, x.y, acc[4 * jc + 1]);
-            const float e2 = fmaf(A4.z, x.z, acc[4 * jc + 2]);
-            const float e3 = fmaf(A4.w, x.w, acc[4 * jc + 3]);
-            sq[0] = fmaf(e0, q4v.x, sq[0]); sk[0] = fmaf(e0, k4v.x, sk[0]);
-            sq[1] = fmaf(e1, q4v.y, sq[1]); sk[1] = fmaf(e1, k4v.y, sk[1]);
-            sq[2] = fmaf(e2, q4v.z, sq[2]); sk[2] = fmaf(e2, k4v.z, sk[2]);
-            sq[3] = fmaf(e3, q4v.w, sq[3]); sk[3] = fmaf(e3, k4v.w, sk[3]);
+            float2 A01 = make_float2(A, A), A23 = A01;
+            if (GATE == GDN_GATE_PER_K) {
+              const float4 A4 = *reinterpret_cast<const float4 *>(fA + col);
+              A01 = make_float2(A4.x, A4.y);
+              A23 = make_float2(A4.z, A4.w);
+            }
+            const float2 e01 = ffma2(A01, make_float2(x.x, x.y), make_float2(acc[4 * jc], acc[4 * jc + 1]));
+            const float2 e23 = ffma2(A23, make_float2(x.z, x.w), make_float2(acc[4 * jc + 2], acc[4 * jc + 3]));
+            sq01 = ffma2(e01, make_float2(q4v.x, q4v.y), sq01);
+            sq23 = ffma2(e23, make_float2(q4v.z, q4v.w), sq23);
+            sk01 = ffma2(e01, make_float2(k4v.x, k4v.y), sk01);
+            sk23 = ffma2(e23, make_float2(k4v.z, k4v.w), sk23);
           }
         }
         if (!flush) mbar_arrive(bars.be(bs));
       }
       if (!ok) break;
-      float sqt = (sq[0] + sq[1]) + (sq[2] + sq[3]);
-      float skt = (sk[0] + sk[1]) + (sk[2] + sk[3]);
+      float sqt = (sq01.x + sq01.y) + (sq23.x + sq23.y);
+      float skt = (sk01.x + sk01.y) + (sk23.x + sk23.y);
       if (GATE == GDN_GATE_SCALAR) {
         sqt *= alpha;
         skt *= alpha;
@@ -522,6 +613,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       const int hk = hv / P.G;
       if (flush) {
         if (row_live) {
+          const float2 d2 = make_float2(d, d);
           for (int c = 0; c < NBOX; ++c) {
             const int bs = (int)((use + c) % NB);
             float acc[32];
@@ -538,24 +630,30 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
               const float4 x = *px;
               const int col = 32 * c + 4 * jc;
               const float4 k4 = *reinterpret_cast<const float4 *>(fk + col);
-              float4 A4 = make_float4(A, A, A, A), g4 = make_float4(alpha, alpha, alpha, alpha);
+              float2 A01 = make_float2(A, A), A23 = A01, g01 = make_float2(alpha, alpha), g23 = g01;
               if (GATE == GDN_GATE_PER_K) {
-                A4 = *reinterpret_cast<const float4 *>(fA + col);
-                g4 = *reinterpret_cast<const float4 *>(fa + col);
+                const float4 A4 = *reinterpret_cast<const float4 *>(fA + col);
+                const float4 g4 = *reinterpret_cast<const float4 *>(fa + col);
+                A01 = make_float2(A4.x, A4.y);
+                A23 = make_float2(A4.z, A4.w);
+                g01 = make_float2(g4.x, g4.y);
+                g23 = make_float2(g4.z, g4.w);
               }
-              float4 nv;
-              nv.x = fmaf(d, k4.x, fmaf(A4.x, x.x, acc[4 * jc + 0]) * g4.x);
-              nv.y = fmaf(d, k4.y, fmaf(A4.y, x.y, acc[4 * jc + 1]) * g4.y);
-              nv.z = fmaf(d, k4.z, fmaf(A4.z, x.z, acc[4 * jc + 2]) * g4.z);
-              nv.w = fmaf(d, k4.w, fmaf(A4.w, x.w, acc[4 * jc + 3]) * g4.w);
-              *px = nv;
+              const float2 e01 = ffma2(A01, make_float2(x.x, x.y), make_float2(acc[4 * jc], acc[4 * jc + 1]));
+              const float2 e23 = ffma2(A23, make_float2(x.z, x.w), make_float2(acc[4 * jc + 2], acc[4 * jc + 3]));
+              const float2 n01 = ffma2(d2, make_float2(k4.x, k4.y), fmul2(e01, g01));
+              const float2 n23 = ffma2(d2, make_float2(k4.z, k4.w), fmul2(e23, g23));
+              *px = make_float4(n01.x, n01.y, n23.x, n23.y);
             }
           }
         }
+        // Two flush barriers per group, used by the group's alternate flush
+        // items: a thread of the group can run one item ahead of another, and
+        // its arrival for the next flush item must not count toward this one.
         fence_proxy_async_smem();
-        const uint32_t fbar = flush_bar0 + 8u * (nflush & 1);
+        const uint32_t fbar = bars.fl(2 * eg + (int)(nflush & 1));
         mbar_arrive(fbar);
-        if (tid == 320) {  // one thread stores the rewritten boxes once all rows are in
+        if (etid == 0) {  // one thread stores the rewritten boxes once all rows are in
           if (!wait_bar(fbar, (nflush >> 1) & 1, abort_flag, P.status)) break;
           const int row0 = (slot * P.HV + hv) * D;
           for (int c = 0; c < NBOX; ++c)
@@ -572,19 +670,18 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
           if (hv % P.G == 0)
             store_from_f32(P.ring_k, (((int64_t)slot * P.HK + hk) * P.L + p) * D + r, RING_DT, fk[r]);
         }
-        if (GATE == GDN_GATE_SCALAR && tid == 320) P.ring_g[((int64_t)slot * P.HV + hv) * P.L + p] = fg[0];
+        if (GATE == GDN_GATE_SCALAR && etid == 0) P.ring_g[((int64_t)slot * P.HV + hv) * P.L + p] = scal[4];
       }
       tc_fence_before();
       mbar_arrive(bars.te(tb));
       mbar_arrive(bars.ine(s));
-      use += NBOX;
       ++li;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 2 * D);
   }
