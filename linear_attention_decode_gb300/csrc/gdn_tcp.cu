@@ -6,7 +6,7 @@
 //   warp 0       producer: streams each item's fp32 checkpoint S0 [V, K] by TMA,
 //                one [V x 32] box (128-byte swizzled) at a time, through a ring
 //                of NB box slots (box_full / box_empty); it also allocates the
-//                2 x K TMEM columns (two accumulators);
+//                4 x K TMEM columns (four accumulators, two per group);
 //   warps 1-8    two prep warpgroups taking alternate items.  A group's leader
 //                bulk-copies the first p ring entries (d, k; KDA also g) and,
 //                when aligned, q, k, v of its items two group-items ahead into
@@ -15,16 +15,19 @@
 //                ([P1] Design 1 and 7)
 //                      GDN  A[v][j] = w_j d_j[v],  B[c][j] = k_j[c]
 //                      KDA  A[v][j] = d_j[v],      B[c][j] = w_j[c] k_j[c]
-//                plus the epilogue's vectors, written into an info stage
-//                (info_full / info_empty); the group leader then issues the
-//                replay contraction tcgen05.mma into the group's accumulator;
+//                into a tile stage, plus the epilogue's vectors into a field
+//                stage (info_full / info_empty); the group leader then issues the
+//                replay contraction tcgen05.mma into one of the group's two
+//                accumulators (alternating), so the contraction of the group's
+//                next item overlaps the epilogue of its current one;
 //   warps 9-16   two epilogue warpgroups, group g taking the items of prep group
 //                g and reading accumulator g: thread r owns state row r (TMEM
 //                lane r).  It adds A S0[r][:] (KDA: S0[r][:] o A) to dS[r][:],
 //                contracts with q and k in registers (packed fp32x2 FMAs), writes
 //                out[r] = alpha Sq + d (k^T q) with d = beta (v - alpha Sk); a
-//                flush item rewrites its box rows with alpha S + d k^T and
-//                TMA-stores them, otherwise (d, k, g) are appended to the ring.
+//                flush item reads its box row and accumulator a second time and
+//                stores row r of alpha S + d k^T straight to the checkpoint,
+//                otherwise (d, k, g) are appended to the ring.
 // Every wait is bounded: a wait that runs out raises a CTA-wide abort flag and
 // GDN_DEV_TIMEOUT; all roles then leave their loops, the producer and the MMA
 // issuers wait (bounded) for their own copies and contractions still in
@@ -39,19 +42,13 @@ namespace gdn {
 
 constexpr int kTcpThreads = 544;  // 17 warps
 constexpr int kItemsMax = 256;    // items one CTA may own (sets the table size)
-#ifndef GDN_TCP_STAGES
-#define GDN_TCP_STAGES 3  // info stages (operand tiles + epilogue vectors)
-#endif
-#ifndef GDN_TCP_LANDING
-#define GDN_TCP_LANDING 4  // landing slots (raw ring rows and q/k/v)
-#endif
 
 struct TcpLayout {
-  int KD, KC, NI, NL, NB;
+  int KD, KC, NT, NF, NL, NB;
   int qkv_bulk;  // 1: q, k, v arrive by bulk copy (16-byte aligned rows)
-  uint32_t box_bytes, stage_bytes, land_bytes;
-  uint32_t off_stage, off_land, off_table, off_bars, total;
-  uint32_t st_A, st_B, st_f;        // inside an info stage
+  uint32_t box_bytes, tile_bytes, field_bytes, land_bytes;
+  uint32_t off_tile, off_field, off_land, off_table, off_bars, total;
+  uint32_t t_B;                     // B operand inside a tile stage (A at 0)
   uint32_t ld_d, ld_k, ld_g, ld_q;  // inside a landing slot
 };
 
@@ -59,10 +56,10 @@ struct TcpLayout {
 // total decay per channel and the current log-gate.  Then 8 scalars.
 __host__ __device__ inline int field_floats(int D, int gate) { return (gate == GDN_GATE_PER_K ? 7 : 3) * D + 8; }
 
-// Shared memory: NB checkpoint boxes | NI info stages | NL landing slots | item
-// table | barriers.
+// Shared memory: NB checkpoint boxes | NT operand tile stages | NF field stages
+// | NL landing slots | item table | barriers.
 static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, int qkv_bytes, int qkv_bulk,
-                            int smem_budget) {
+                            int NT, int NL, int smem_budget) {
   TcpLayout t{};
   const int es = kind == 2 ? 4 : 2;
   const int kstep = 32 / es;
@@ -71,10 +68,9 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
   t.KC = t.KD * es / 16;
   t.qkv_bulk = qkv_bulk;
   t.box_bytes = (uint32_t)D * 128;
-  t.st_A = 0;
-  t.st_B = (uint32_t)(128 * t.KD * es);
-  t.st_f = t.st_B + (uint32_t)(D * t.KD * es);
-  t.stage_bytes = (t.st_f + (uint32_t)field_floats(D, gate) * 4 + 127) & ~127u;
+  t.t_B = (uint32_t)(128 * t.KD * es);
+  t.tile_bytes = (t.t_B + (uint32_t)(D * t.KD * es) + 127) & ~127u;
+  t.field_bytes = ((uint32_t)field_floats(D, gate) * 4 + 127) & ~127u;
   t.ld_d = 0;
   t.ld_k = t.ld_d + (uint32_t)(depth * D * ring_bytes);
   t.ld_g = t.ld_k + (uint32_t)(depth * D * ring_bytes);
@@ -82,29 +78,47 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
   t.land_bytes = (t.ld_q + (uint32_t)(qkv_bulk ? 3 * D * qkv_bytes : 0) + 127) & ~127u;
   const uint32_t table = (uint32_t)kItemsMax * 8 + (uint32_t)kItemsMax * 4;  // table + live list
   const uint32_t bars = 640;
-  t.NI = GDN_TCP_STAGES;
-  t.NL = GDN_TCP_LANDING;
-  const long rest = (long)smem_budget - (long)t.NI * t.stage_bytes - (long)t.NL * t.land_bytes - table - bars;
+  t.NT = NT;
+  t.NF = NT + 4;  // a group's fields live from its prep until its epilogue, up to NT + 4 items later
+  t.NL = NL;
+  const long rest = (long)smem_budget - (long)t.NT * t.tile_bytes - (long)t.NF * t.field_bytes -
+                    (long)t.NL * t.land_bytes - table - bars;
   t.NB = rest > 0 ? (int)(rest / t.box_bytes) : 0;
   if (t.NB > 16) t.NB = 16;
-  t.off_stage = (uint32_t)t.NB * t.box_bytes;
-  t.off_land = t.off_stage + (uint32_t)t.NI * t.stage_bytes;
+  t.off_tile = (uint32_t)t.NB * t.box_bytes;
+  t.off_field = t.off_tile + (uint32_t)t.NT * t.tile_bytes;
+  t.off_land = t.off_field + (uint32_t)t.NF * t.field_bytes;
   t.off_table = t.off_land + (uint32_t)t.NL * t.land_bytes;
   t.off_bars = t.off_table + table;
   t.total = t.off_bars + bars;
   return t;
 }
 
+// The first (tile stages, landing slots) choice that leaves room for two items'
+// checkpoint boxes plus one more; else the one with the most boxes.
+static TcpLayout tcp_pick_layout(int D, int kind, int gate, int L, int ring_bytes, int qkv_bytes, int qkv_bulk,
+                                 int smem_budget) {
+  static const int cand[4][2] = {{4, 4}, {2, 4}, {4, 2}, {2, 2}};
+  const int want = 2 * (D / 32) + 1;
+  TcpLayout best{};
+  for (const auto &c : cand) {
+    const TcpLayout t = tcp_layout(D, kind, gate, L, ring_bytes, qkv_bytes, qkv_bulk, c[0], c[1], smem_budget);
+    if (t.NB >= want) return t;
+    if (t.NB > best.NB) best = t;
+  }
+  return best;
+}
+
 struct TcpBars {
-  uint32_t box_full, box_empty, land_full, info_full, info_empty, tmem_full, tmem_empty, flush;
+  uint32_t box_full, box_empty, land_full, info_full, info_empty, tile_empty, tmem_full, tmem_empty;
   __device__ uint32_t bf(int i) const { return box_full + 8 * i; }
   __device__ uint32_t be(int i) const { return box_empty + 8 * i; }
   __device__ uint32_t lf(int i) const { return land_full + 8 * i; }
   __device__ uint32_t inf(int i) const { return info_full + 8 * i; }
   __device__ uint32_t ine(int i) const { return info_empty + 8 * i; }
+  __device__ uint32_t tle(int i) const { return tile_empty + 8 * i; }
   __device__ uint32_t tf(int i) const { return tmem_full + 8 * i; }
   __device__ uint32_t te(int i) const { return tmem_empty + 8 * i; }
-  __device__ uint32_t fl(int i) const { return flush + 8 * i; }
 };
 
 // Bounded wait that also gives up when another thread raised the abort flag.
@@ -173,7 +187,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   constexpr int NBOX = D / 32;
   constexpr int BOX_BYTES = D * 128;
   constexpr int RB = RING_DT == GDN_F32 ? 4 : 2;
-  constexpr int NF = GATE == GDN_GATE_PER_K ? 7 : 3;  // epilogue vectors per item
+  constexpr int NVEC = GATE == GDN_GATE_PER_K ? 7 : 3;  // epilogue vectors per item
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -183,7 +197,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   const int T = P.B * P.HV;
   const int G = gridDim.x;
   const int n = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / G + 1 : 0;
-  const int NB = lay.NB, NI = lay.NI, NL = lay.NL;
+  const int NB = lay.NB, NT = lay.NT, NF = lay.NF, NL = lay.NL;
   const int qes = P.qkv_dtype == GDN_F32 ? 4 : 2;
 
   if (smem_addr(smem) & 1023u) {  // the 128-byte swizzle assumes a 1024-byte aligned base
@@ -198,13 +212,13 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   bars.box_empty = bars.box_full + 8u * NB;
   bars.land_full = bars.box_empty + 8u * NB;
   bars.info_full = bars.land_full + 8u * NL;
-  bars.info_empty = bars.info_full + 8u * NI;
-  bars.tmem_full = bars.info_empty + 8u * NI;
-  bars.tmem_empty = bars.tmem_full + 16u;
-  bars.flush = bars.tmem_empty + 16u;  // two per epilogue group (see the epilogue)
+  bars.info_empty = bars.info_full + 8u * NF;
+  bars.tile_empty = bars.info_empty + 8u * NF;
+  bars.tmem_full = bars.tile_empty + 8u * NT;
+  bars.tmem_empty = bars.tmem_full + 32u;  // four accumulators
   // misc[0] TMEM base, misc[1] abort flag, misc[2..3] prep-group go/stop words,
   // misc[4] number of live items
-  uint32_t *misc = reinterpret_cast<uint32_t *>(bar_mem + 2 * NB + NL + 2 * NI + 8);
+  uint32_t *misc = reinterpret_cast<uint32_t *>(bar_mem + 2 * NB + NL + 2 * NF + NT + 8);
   int *live_j = reinterpret_cast<int *>(table + kItemsMax);  // j of the li-th live item
   volatile uint32_t *abort_flag = misc + 1;
 
@@ -221,20 +235,20 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       mbar_init(bars.be(i), 128);
     }
     for (int i = 0; i < NL; ++i) mbar_init(bars.lf(i), 1);
-    for (int i = 0; i < NI; ++i) {
+    for (int i = 0; i < NF; ++i) {
       mbar_init(bars.inf(i), 1);
       mbar_init(bars.ine(i), 128);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NT; ++i) mbar_init(bars.tle(i), 1);
+    for (int i = 0; i < 4; ++i) {
       mbar_init(bars.tf(i), 1);
       mbar_init(bars.te(i), 128);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(bars.fl(i), 128);
     misc[1] = 0u;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_addr(misc), 2 * D);
+    tmem_alloc(smem_addr(misc), 4 * D);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -253,7 +267,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   __syncthreads();
   const uint32_t tmem = misc[0];
   uint8_t *boxes = smem;
-  uint8_t *stages = smem + lay.off_stage;
+  uint8_t *tiles = smem + lay.off_tile;
+  uint8_t *fields = smem + lay.off_field;
   uint8_t *lands = smem + lay.off_land;
 
   if (warp == 0) {
@@ -286,14 +301,16 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   } else if (warp < 9) {
     // ------------------------------------------------------------ prep + MMA
     // Group pg takes the live items with li % 2 == pg; its leader also issues
-    // the item's contraction into TMEM accumulator pg.
+    // the item's contraction into TMEM accumulator 2 pg + (li / 2) % 2.
     const int pg = (warp - 1) >> 2;
     const int pt = tid - 32 - 128 * pg;  // 0..127: operand row / key channel
     const uint32_t bar_id = 1 + pg;
     const uint32_t idesc = make_idesc(KIND, D);
     volatile uint32_t *go = misc + 2 + pg;
     bool leader_ok = true;  // leader only: false after a wait ran out
-    int li = 0, nmma = 0, land_next = pg;  // leader: next live item to land
+    int li = 0, land_next = pg;  // leader: next live item to land
+    int last_acc = -1;           // leader: accumulator and use count of its last contraction
+    uint32_t last_use = 0;
     const int nlive = (int)misc[4];
     // The group's landing slots (li % NL with NL = 4: two per group) are filled
     // by its own leader two group-items ahead: right after the group has read a
@@ -332,8 +349,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         ++li;
         continue;
       }
-      const int p = e.y & 255, slot = e.x, s = li % NI, l = li % NL;
-      const uint32_t u = (uint32_t)(li / NI), ul = (uint32_t)(li / NL);
+      const int p = e.y & 255, slot = e.x, s = li % NF, t = li % NT, l = li % NL;
+      const uint32_t u = (uint32_t)(li / NF), ut = (uint32_t)(li / NT), ul = (uint32_t)(li / NL);
       const int item = (int)blockIdx.x + j * G, b = item / P.HV, hv = item % P.HV, hk = hv / P.G;
       const int64_t bh = (int64_t)b * P.HV + hv;
       // small loads first, so their latency overlaps the waits
@@ -354,21 +371,22 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         kv = load_as_f32(P.qkv, qbase + (int64_t)P.HK * D + (int64_t)hk * D + pt, P.qkv_dtype);
         vv = load_as_f32(P.qkv, qbase + 2 * (int64_t)P.HK * D + (int64_t)hv * D + pt, P.qkv_dtype);
       }
-      // Only the leader waits (landing slot filled, info stage free); the
+      // Only the leader waits (landing slot filled, tile stage read by its last
+      // contraction, field stage free); the
       // go/stop word it leaves before the group barrier makes the whole group
       // leave together, so the group's barriers stay uniform.
       if (pt == 0)
         *go = (leader_ok && wait_bar(bars.lf(l), ul & 1, abort_flag, P.status) &&
+               (ut == 0 || wait_bar(bars.tle(t), (ut - 1) & 1, abort_flag, P.status)) &&
                (u == 0 || wait_bar(bars.ine(s), (u - 1) & 1, abort_flag, P.status)))
                   ? 1u
                   : 0u;
       named_bar_sync(bar_id, 128);
       if (*go == 0u) break;
-      uint8_t *st = stages + s * lay.stage_bytes;
-      uint8_t *tA = st + lay.st_A, *tB = st + lay.st_B;
-      float *f = reinterpret_cast<float *>(st + lay.st_f);
+      uint8_t *tA = tiles + t * lay.tile_bytes, *tB = tA + lay.t_B;
+      float *f = reinterpret_cast<float *>(fields + s * lay.field_bytes);
       float *fq = f, *fk = f + D, *fv = f + 2 * D, *fke = f + 3 * D, *fa = f + 4 * D, *fA = f + 5 * D,
-            *fg = f + 6 * D, *scal = f + NF * D;
+            *fg = f + 6 * D, *scal = f + NVEC * D;
       const uint8_t *ld = lands + l * lay.land_bytes;
       const uint8_t *land_d = ld + lay.ld_d, *land_k = ld + lay.ld_k, *lq = ld + lay.ld_q;
       const float *land_g = reinterpret_cast<const float *>(ld + lay.ld_g);
@@ -502,9 +520,10 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
           land_next += 2;
         }
         mbar_arrive(bars.inf(s));
-        // contraction into accumulator pg once the epilogue has read it out
-        const uint32_t ut = (uint32_t)(li >> 1);
-        if (ut > 0 && !wait_bar(bars.te(pg), (ut - 1) & 1, abort_flag, P.status)) {
+        // contraction into accumulator acc once the epilogue has read it out
+        const int acc = 2 * pg + ((li >> 1) & 1);
+        const uint32_t ua = (uint32_t)(li >> 2);
+        if (ua > 0 && !wait_bar(bars.te(acc), (ua - 1) & 1, abort_flag, P.status)) {
           leader_ok = false;
         } else {
           tc_fence_after();
@@ -513,26 +532,30 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
             const uint32_t sbo = (uint32_t)lay.KC * 128;
             const int nsteps = (p + KSTEP - 1) / KSTEP;
             for (int i = 0; i < nsteps; ++i)
-              tc_mma<KIND == 2 ? 1 : 0>(tmem + pg * D, make_sdesc(a0 + 256 * i, 128, sbo),
+              tc_mma<KIND == 2 ? 1 : 0>(tmem + acc * D, make_sdesc(a0 + 256 * i, 128, sbo),
                                         make_sdesc(b0 + 256 * i, 128, sbo), idesc, i > 0 ? 1u : 0u);
-            tc_commit(bars.tf(pg));
+            tc_commit(bars.tf(acc));
+            tc_commit(bars.tle(t));
           } else {
-            mbar_arrive(bars.tf(pg));
+            mbar_arrive(bars.tf(acc));
+            mbar_arrive(bars.tle(t));
           }
-          ++nmma;
+          last_acc = acc;
+          last_use = ua;
         }
       }
       ++li;
     }
     // an aborted CTA lets its last contraction and its landings finish first
     if (pt == 0 && *abort_flag) {
-      if (nmma > 0) mbar_wait_bounded(bars.tf(pg), (uint32_t)(nmma - 1) & 1, kWaitLimitNs);
+      if (last_acc >= 0) mbar_wait_bounded(bars.tf(last_acc), last_use & 1, kWaitLimitNs);
       for (int k = land_next - 2; k >= 0 && k >= land_next - NL; k -= 2)
         mbar_wait_bounded(bars.lf(k % NL), (uint32_t)(k / NL) & 1, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ epilogue (2 groups)
-    // Group eg takes the items with li % 2 == eg and reads TMEM accumulator eg.
+    // Group eg takes the items with li % 2 == eg and reads TMEM accumulator
+    // 2 eg + (li / 2) % 2.
     const int eg = (warp - 9) >> 2;
     const int etid = tid - 288 - 128 * eg;  // 0 is the group's store thread
     const int q4 = warp & 3;
@@ -540,7 +563,6 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     const bool row_live = r < D;   // warp-uniform
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     int li = 0;
-    uint32_t nflush = 0;
     for (int j = 0; j < n; ++j) {
       const int2 e = table[j];
       const int item = (int)blockIdx.x + j * G, b = item / P.HV, hv = item % P.HV;
@@ -553,15 +575,16 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         ++li;
         continue;
       }
-      const int p = e.y & 255, slot = e.x, flush = (e.y >> 8) & 1, s = li % NI, tb = li & 1;
-      const uint32_t u = (uint32_t)(li / NI), ut = (uint32_t)(li >> 1);
+      const int p = e.y & 255, slot = e.x, flush = (e.y >> 8) & 1, s = li % NF;
+      const int tb = 2 * eg + ((li >> 1) & 1);
+      const uint32_t u = (uint32_t)(li / NF), ut = (uint32_t)(li >> 2);
       const uint32_t use = (uint32_t)(NBOX * li);
       if (!wait_bar_warp(bars.inf(s), u & 1, abort_flag, P.status)) break;
       if (!wait_bar_warp(bars.tf(tb), ut & 1, abort_flag, P.status)) break;
       tc_fence_after();
-      const float *f = reinterpret_cast<const float *>(stages + s * lay.stage_bytes + lay.st_f);
+      const float *f = reinterpret_cast<const float *>(fields + s * lay.field_bytes);
       const float *fq = f, *fk = f + D, *fv = f + 2 * D, *fke = GATE == GDN_GATE_PER_K ? f + 3 * D : fk,
-                  *fa = f + 4 * D, *fA = f + 5 * D, *fg = f + 6 * D, *scal = f + NF * D;
+                  *fa = f + 4 * D, *fA = f + 5 * D, *fg = f + 6 * D, *scal = f + NVEC * D;
       const float alpha = scal[0], beta = scal[1], A = scal[2], kq = scal[3];
       const uint32_t trow = tmem + tb * D + lane_off;
       float2 sq01 = make_float2(0.f, 0.f), sq23 = sq01, sk01 = sq01, sk23 = sq01;
@@ -601,6 +624,10 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         if (!flush) mbar_arrive(bars.be(bs));
       }
       if (!ok) break;
+      if (!flush) {  // only a flush item reads its accumulator again
+        tc_fence_before();
+        mbar_arrive(bars.te(tb));
+      }
       float sqt = (sq01.x + sq01.y) + (sq23.x + sq23.y);
       float skt = (sk01.x + sk01.y) + (sk23.x + sk23.y);
       if (GATE == GDN_GATE_SCALAR) {
@@ -612,10 +639,14 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       if (row_live) store_from_f32(P.out, bh * D + r, P.out_dtype, fmaf(d, kq, sqt));
       const int hk = hv / P.G;
       if (flush) {
-        if (row_live) {
-          const float2 d2 = make_float2(d, d);
-          for (int c = 0; c < NBOX; ++c) {
-            const int bs = (int)((use + c) % NB);
+        // second pass over the boxes: row r of alpha S + d k^T goes straight to
+        // the checkpoint (512 contiguous bytes per thread), and each box is
+        // handed back to the producer once read
+        const float2 d2 = make_float2(d, d);
+        float *srow = P.state + (((int64_t)slot * P.HV + hv) * D + r) * D;
+        for (int c = 0; c < NBOX; ++c) {
+          const int bs = (int)((use + c) % NB);
+          if (row_live) {
             float acc[32];
             if (p > 0) {
               tmem_ld32(trow + 32 * c, acc);
@@ -623,11 +654,10 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) acc[i] = 0.f;
             }
-            uint8_t *rowp = boxes + bs * BOX_BYTES + r * 128;
+            const uint8_t *rowp = boxes + bs * BOX_BYTES + r * 128;
 #pragma unroll
             for (int jc = 0; jc < 8; ++jc) {
-              float4 *px = reinterpret_cast<float4 *>(rowp + ((jc ^ (r & 7)) << 4));
-              const float4 x = *px;
+              const float4 x = *reinterpret_cast<const float4 *>(rowp + ((jc ^ (r & 7)) << 4));
               const int col = 32 * c + 4 * jc;
               const float4 k4 = *reinterpret_cast<const float4 *>(fk + col);
               float2 A01 = make_float2(A, A), A23 = A01, g01 = make_float2(alpha, alpha), g23 = g01;
@@ -643,26 +673,13 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
               const float2 e23 = ffma2(A23, make_float2(x.z, x.w), make_float2(acc[4 * jc + 2], acc[4 * jc + 3]));
               const float2 n01 = ffma2(d2, make_float2(k4.x, k4.y), fmul2(e01, g01));
               const float2 n23 = ffma2(d2, make_float2(k4.z, k4.w), fmul2(e23, g23));
-              *px = make_float4(n01.x, n01.y, n23.x, n23.y);
+              *reinterpret_cast<float4 *>(srow + col) = make_float4(n01.x, n01.y, n23.x, n23.y);
             }
           }
+          mbar_arrive(bars.be(bs));
         }
-        // Two flush barriers per group, used by the group's alternate flush
-        // items: a thread of the group can run one item ahead of another, and
-        // its arrival for the next flush item must not count toward this one.
-        fence_proxy_async_smem();
-        const uint32_t fbar = bars.fl(2 * eg + (int)(nflush & 1));
-        mbar_arrive(fbar);
-        if (etid == 0) {  // one thread stores the rewritten boxes once all rows are in
-          if (!wait_bar(fbar, (nflush >> 1) & 1, abort_flag, P.status)) break;
-          const int row0 = (slot * P.HV + hv) * D;
-          for (int c = 0; c < NBOX; ++c)
-            tma_store_2d(&tmap, 32 * c, row0, smem_addr(boxes + (int)((use + c) % NB) * BOX_BYTES));
-          bulk_commit();
-          bulk_wait_read_all();
-          for (int c = 0; c < NBOX; ++c) mbar_arrive_count(bars.be((int)((use + c) % NB)), 128);
-        }
-        ++nflush;
+        tc_fence_before();
+        mbar_arrive(bars.te(tb));
       } else {
         if (row_live) {
           store_from_f32(P.ring_d, (((int64_t)slot * P.HV + hv) * P.L + p) * D + r, RING_DT, d);
@@ -672,8 +689,6 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         }
         if (GATE == GDN_GATE_SCALAR && etid == 0) P.ring_g[((int64_t)slot * P.HV + hv) * P.L + p] = scal[4];
       }
-      tc_fence_before();
-      mbar_arrive(bars.te(tb));
       mbar_arrive(bars.ine(s));
       ++li;
     }
@@ -683,7 +698,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * D);
+    tmem_dealloc(tmem, 4 * D);
   }
 }
 
@@ -732,7 +747,7 @@ cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUte
   const int T = P.B * P.HV;
   int grid = sms > 0 && sms < T ? sms : T;
   if ((T + grid - 1) / grid > kItemsMax) grid = (T + kItemsMax - 1) / kItemsMax;
-  const TcpLayout lay = tcp_layout(D, kind, gate, P.L, ring_bytes, qes, qkv_bulk, optin);
+  const TcpLayout lay = tcp_pick_layout(D, kind, gate, P.L, ring_bytes, qes, qkv_bulk, optin);
   if (lay.NB < D / 32 + 1 || lay.total > (uint32_t)optin) return cudaErrorNotSupported;
   if (D == 128)
     return gate == GDN_GATE_SCALAR ? launch_tcp_ring<128, 0>(P, map, lay, grid, s)
