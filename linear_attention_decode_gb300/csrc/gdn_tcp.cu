@@ -129,6 +129,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // (fewer threads hammering the barrier unit).
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                               uint32_t *status) {
+  if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity) ? 1 : 0)) return true;
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status);
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -151,6 +152,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       return false;
     }
   }
+}
+
+// One arrival for the whole warp once all its lanes are past this point (the
+// consumer barriers count warps, not threads: fewer atomics on one word).
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 template <int KIND>
@@ -232,17 +240,17 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < NB; ++i) {
       mbar_init(bars.bf(i), 1);
-      mbar_init(bars.be(i), 128);
+      mbar_init(bars.be(i), 4);  // one arrival per epilogue warp
     }
     for (int i = 0; i < NL; ++i) mbar_init(bars.lf(i), 1);
     for (int i = 0; i < NF; ++i) {
       mbar_init(bars.inf(i), 1);
-      mbar_init(bars.ine(i), 128);
+      mbar_init(bars.ine(i), 4);
     }
     for (int i = 0; i < NT; ++i) mbar_init(bars.tle(i), 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(bars.tf(i), 1);
-      mbar_init(bars.te(i), 128);
+      mbar_init(bars.te(i), 4);
     }
     misc[1] = 0u;
     fence_mbar_init();
@@ -621,12 +629,12 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
             sk23 = ffma2(e23, make_float2(k4v.z, k4v.w), sk23);
           }
         }
-        if (!flush) mbar_arrive(bars.be(bs));
+        if (!flush) warp_arrive(bars.be(bs));
       }
       if (!ok) break;
       if (!flush) {  // only a flush item reads its accumulator again
         tc_fence_before();
-        mbar_arrive(bars.te(tb));
+        warp_arrive(bars.te(tb));
       }
       float sqt = (sq01.x + sq01.y) + (sq23.x + sq23.y);
       float skt = (sk01.x + sk01.y) + (sk23.x + sk23.y);
@@ -639,11 +647,12 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       if (row_live) store_from_f32(P.out, bh * D + r, P.out_dtype, fmaf(d, kq, sqt));
       const int hk = hv / P.G;
       if (flush) {
-        // second pass over the boxes: row r of alpha S + d k^T goes straight to
-        // the checkpoint (512 contiguous bytes per thread), and each box is
-        // handed back to the producer once read
+        // second pass over the boxes: row r of alpha S + d k^T replaces row r of
+        // the box; the warp then stores its 32 rows of the box to the checkpoint
+        // as whole 128-byte row segments (four per instruction) and hands the
+        // box back to the producer
         const float2 d2 = make_float2(d, d);
-        float *srow = P.state + (((int64_t)slot * P.HV + hv) * D + r) * D;
+        float *gwarp = P.state + (((int64_t)slot * P.HV + hv) * D + 32 * q4) * D + 4 * (lane & 7);
         for (int c = 0; c < NBOX; ++c) {
           const int bs = (int)((use + c) % NB);
           if (row_live) {
@@ -654,10 +663,11 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) acc[i] = 0.f;
             }
-            const uint8_t *rowp = boxes + bs * BOX_BYTES + r * 128;
+            uint8_t *rowp = boxes + bs * BOX_BYTES + r * 128;
 #pragma unroll
             for (int jc = 0; jc < 8; ++jc) {
-              const float4 x = *reinterpret_cast<const float4 *>(rowp + ((jc ^ (r & 7)) << 4));
+              float4 *px = reinterpret_cast<float4 *>(rowp + ((jc ^ (r & 7)) << 4));
+              const float4 x = *px;
               const int col = 32 * c + 4 * jc;
               const float4 k4 = *reinterpret_cast<const float4 *>(fk + col);
               float2 A01 = make_float2(A, A), A23 = A01, g01 = make_float2(alpha, alpha), g23 = g01;
@@ -673,13 +683,22 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
               const float2 e23 = ffma2(A23, make_float2(x.z, x.w), make_float2(acc[4 * jc + 2], acc[4 * jc + 3]));
               const float2 n01 = ffma2(d2, make_float2(k4.x, k4.y), fmul2(e01, g01));
               const float2 n23 = ffma2(d2, make_float2(k4.z, k4.w), fmul2(e23, g23));
-              *reinterpret_cast<float4 *>(srow + col) = make_float4(n01.x, n01.y, n23.x, n23.y);
+              *px = make_float4(n01.x, n01.y, n23.x, n23.y);
+            }
+            __syncwarp();
+            // lanes 8i .. 8i+7 take the eight 16-byte chunks of one row
+            const uint8_t *wbox = boxes + bs * BOX_BYTES + 32 * q4 * 128;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int rr = 4 * k + (lane >> 3);  // row within the warp's 32
+              const float4 v = *reinterpret_cast<const float4 *>(wbox + rr * 128 + (((lane & 7) ^ (rr & 7)) << 4));
+              *reinterpret_cast<float4 *>(gwarp + (int64_t)rr * D + 32 * c) = v;
             }
           }
-          mbar_arrive(bars.be(bs));
+          warp_arrive(bars.be(bs));
         }
         tc_fence_before();
-        mbar_arrive(bars.te(tb));
+        warp_arrive(bars.te(tb));
       } else {
         if (row_live) {
           store_from_f32(P.ring_d, (((int64_t)slot * P.HV + hv) * P.L + p) * D + r, RING_DT, d);
@@ -689,7 +708,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         }
         if (GATE == GDN_GATE_SCALAR && etid == 0) P.ring_g[((int64_t)slot * P.HV + hv) * P.L + p] = scal[4];
       }
-      mbar_arrive(bars.ine(s));
+      warp_arrive(bars.ine(s));
       ++li;
     }
   }
