@@ -62,19 +62,22 @@ struct RowInfo {
   int p;      // ring entries to replay
   int flush;  // 1: write the checkpoint, no ring append
   bool live;
+  uint32_t bad;  // status bit of an invalid slot or cursor, else 0
 };
 
 __device__ __forceinline__ RowInfo resolve_row(const DecodeParams &P, int b, bool report) {
-  RowInfo r{-1, 0, 0, false};
+  RowInfo r{-1, 0, 0, false, 0u};
   int slot = P.idx[b];
   if (slot < 0) return r;
   if (slot >= P.N) {
-    if (report) set_status(P.status, GDN_DEV_BAD_SLOT);
+    r.bad = GDN_DEV_BAD_SLOT;
+    if (report) set_status(P.status, r.bad);
     return r;
   }
   int p = P.write_pos[slot];
   if (p < 0 || p >= P.L) {
-    if (report) set_status(P.status, GDN_DEV_BAD_WRITE_POS);
+    r.bad = GDN_DEV_BAD_WRITE_POS;
+    if (report) set_status(P.status, r.bad);
     return r;
   }
   r.slot = slot;

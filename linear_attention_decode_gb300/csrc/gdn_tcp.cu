@@ -77,7 +77,7 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
   t.ld_q = t.ld_g + (uint32_t)(gate == GDN_GATE_PER_K ? depth * D * 4 : 0);
   t.land_bytes = (t.ld_q + (uint32_t)(qkv_bulk ? 3 * D * qkv_bytes : 0) + 127) & ~127u;
   const uint32_t table = (uint32_t)kItemsMax * 8 + (uint32_t)kItemsMax * 4;  // table + live list
-  const uint32_t bars = 640;
+  const uint32_t bars = 1024;  // barriers, then misc words and the dealing's counters
   t.NT = NT;
   t.NF = NT + 4;  // a group's fields live from its prep until its epilogue, up to NT + 4 items later
   t.NL = NL;
@@ -199,9 +199,9 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Items (row b, value head hv) = b * HV + hv are dealt round-robin: CTA c takes
-  // c, c + G, c + 2G, ...  A flushing row's heads (about twice the work) thus
-  // spread over HV different CTAs instead of piling up on one or two.
+  // Items are the (row b, value head hv) pairs, laid out in one sequence and
+  // dealt round-robin: CTA c takes positions c, c + G, c + 2G, ... (see the
+  // dealing below).
   const int T = P.B * P.HV;
   const int G = gridDim.x;
   const int n = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / G + 1 : 0;
@@ -225,17 +225,111 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   bars.tmem_full = bars.tile_empty + 8u * NT;
   bars.tmem_empty = bars.tmem_full + 32u;  // four accumulators
   // misc[0] TMEM base, misc[1] abort flag, misc[2..3] prep-group go/stop words,
-  // misc[4] number of live items
+  // misc[4] number of live items, misc[8..] the dealing's counters
   uint32_t *misc = reinterpret_cast<uint32_t *>(bar_mem + 2 * NB + NL + 2 * NF + NT + 8);
-  int *live_j = reinterpret_cast<int *>(table + kItemsMax);  // j of the li-th live item
+  int *titem = reinterpret_cast<int *>(table + kItemsMax);  // b * HV + hv of table entry j
   volatile uint32_t *abort_flag = misc + 1;
 
-  // --- item table: slot, cursor, flush decision of every item of this CTA ---
-  for (int j = tid; j < n; j += kTcpThreads) {
-    const int item = (int)blockIdx.x + j * G, b = item / P.HV, hv = item % P.HV;
-    const RowInfo ri = resolve_row(P, b, hv == 0);
-    if (hv == 0 && P.flushed) P.flushed[b] = ri.live ? (uint8_t)ri.flush : 0;
-    table[j] = make_int2(ri.slot, ri.p | (ri.flush << 8) | ((ri.live ? 1 : 0) << 9));
+  // --- dealing: the item table of this CTA ---
+  // Every CTA classifies every row: live without flush (0), live with flush (1)
+  // or dead (2: padding, or an invalid slot or cursor).  Items (b, hv) form one
+  // sequence: the flush items, then the other live ones, then the dead ones,
+  // each group in row order; item t goes to CTA t % G.  Every CTA thus gets
+  // the same share (to one) of flush items, each about 1.5x the work of
+  // another.  Inside a CTA the flush items are spread evenly among its other
+  // live items (a merge of the two by (2 rank + 1) / count, non-flush first on
+  // a tie) and the dead ones come last.
+  int *cnt = reinterpret_cast<int *>(misc + 8);  // [3] row counts, [3] carries, [3][32] per warp
+  int *carry = cnt + 3, *wc = cnt + 6;
+  constexpr int NW = kTcpThreads / 32;
+  // Enters row b (category cat, rank among its category's rows) into the table
+  // if this CTA holds some of its heads.  Sizes here stay far below 2^31.
+  auto place = [&](const RowInfo &ri, int b, int cat, int rank, int NNF, int NFL) {
+    const int F = NFL * P.HV, M = NNF * P.HV, c = (int)blockIdx.x;
+    const int t_lo = rank * P.HV + (cat == 1 ? 0 : (cat == 0 ? F : F + M));
+    const int nf = c < F ? (F - 1 - c) / G + 1 : 0;              // this CTA's flush items
+    const int nn = (c < F + M ? (F + M - 1 - c) / G + 1 : 0) - nf;  // and its other live items
+    for (int t = t_lo + ((c - t_lo) % G + G) % G; t < t_lo + P.HV; t += G) {
+      const int q = (t - c) / G;  // rank among this CTA's items of the sequence
+      int j = q;
+      if (cat == 1) {  // other live items ahead: (2r + 1) nf <= (2q + 1) nn
+        const int z = (2 * q + 1) * nn / nf;
+        j = q + (z >= 1 ? min(nn, (z - 1) / 2 + 1) : 0);
+      } else if (cat == 0) {  // flush items ahead: (2f + 1) nn < (2r + 1) nf, r = q - nf
+        const int r = q - nf, y = ((2 * r + 1) * nf - 1) / nn;
+        j = r + (y >= 1 ? min(nf, (y - 1) / 2 + 1) : 0);
+      }
+      const int hv = t - t_lo;
+      if (hv == 0) {  // the CTA holding head 0 reports the row
+        if (ri.bad) set_status(P.status, ri.bad);
+        if (P.flushed) P.flushed[b] = ri.live ? (uint8_t)ri.flush : 0;
+      }
+      table[j] = make_int2(ri.slot, ri.p | (ri.flush << 8) | ((ri.live ? 1 : 0) << 9));
+      titem[j] = b * P.HV + hv;
+    }
+  };
+  // category of row b (3: past the end) and its rank within the warp
+  auto classify = [&](const RowInfo &ri, bool in, int &rank) {
+    const int cat = in ? (ri.live ? ri.flush : 2) : 3;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const uint32_t m = __ballot_sync(0xffffffffu, cat == k);
+      if (cat == k) rank = __popc(m & ((1u << lane) - 1u));
+      if (lane == 0) wc[k * 32 + warp] = __popc(m);
+    }
+    return cat;
+  };
+  int NNF = 0, NFL = 0;
+  if (P.B <= kTcpThreads) {  // one row per thread: one pass, one barrier
+    const bool in = tid < P.B;
+    const RowInfo ri = in ? resolve_row(P, tid, false) : RowInfo{-1, 0, 0, false, 0u};
+    int rank = 0;
+    const int cat = classify(ri, in, rank);
+    __syncthreads();
+    for (int w = 0; w < NW; ++w) {
+      NNF += wc[w];
+      NFL += wc[32 + w];
+      if (w < warp && cat < 3) rank += wc[cat * 32 + w];
+    }
+    if (cat < 3) place(ri, tid, cat, rank, NNF, NFL);
+  } else {  // a pass to count the categories, then one to rank and place the rows
+    if (tid < 6) cnt[tid] = 0;
+    __syncthreads();
+    for (int base = 0; base < P.B; base += kTcpThreads) {
+      const bool in = base + tid < P.B;
+      const RowInfo ri = in ? resolve_row(P, base + tid, false) : RowInfo{-1, 0, 0, false, 0u};
+      int rank = 0;
+      const int cat = classify(ri, in, rank);
+      if (lane == 0)
+        for (int k = 0; k < 3; ++k)
+          if (wc[k * 32 + warp]) atomicAdd(&cnt[k], wc[k * 32 + warp]);
+      __syncthreads();  // wc is reused by the next chunk
+    }
+    NNF = cnt[0];
+    NFL = cnt[1];
+    for (int base = 0; base < P.B; base += kTcpThreads) {
+      const bool in = base + tid < P.B;
+      const RowInfo ri = in ? resolve_row(P, base + tid, false) : RowInfo{-1, 0, 0, false, 0u};
+      int rank = 0;
+      const int cat = classify(ri, in, rank);
+      __syncthreads();
+      if (cat < 3) {
+        rank += carry[cat];
+        for (int w = 0; w < warp; ++w) rank += wc[cat * 32 + w];
+        place(ri, base + tid, cat, rank, NNF, NFL);
+      }
+      __syncthreads();
+      if (tid < 3) {
+        int t = 0;
+        for (int w = 0; w < NW; ++w) t += wc[tid * 32 + w];
+        carry[tid] += t;
+      }
+      __syncthreads();
+    }
+  }
+  if (tid == 0) {
+    const int lv = (NNF + NFL) * P.HV;  // live positions come first
+    misc[4] = (int)blockIdx.x < lv ? (uint32_t)((lv - 1 - (int)blockIdx.x) / G + 1) : 0u;
   }
   if (tid == 0) {
     for (int i = 0; i < NB; ++i) {
@@ -262,17 +356,6 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) {  // live items in order: live_j[li] = table index of the li-th live item
-    int cnt = 0;
-    for (int base = 0; base < n; base += 32) {
-      const bool live = base + lane < n && (table[base + lane].y & 512);
-      const uint32_t m = __ballot_sync(0xffffffffu, live);
-      if (live) live_j[cnt + __popc(m & ((1u << lane) - 1u))] = base + lane;
-      cnt += __popc(m);
-    }
-    if (lane == 0) misc[4] = (uint32_t)cnt;
-  }
-  __syncthreads();
   const uint32_t tmem = misc[0];
   uint8_t *boxes = smem;
   uint8_t *tiles = smem + lay.off_tile;
@@ -289,7 +372,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       for (int j = 0; j < n && ok; ++j) {
         const int2 e = table[j];
         if (!(e.y & 512)) continue;
-        const int hv = ((int)blockIdx.x + j * G) % P.HV;
+        const int hv = titem[j] % P.HV;
         const int slot = e.x;
         // checkpoint boxes
         const int row0 = (slot * P.HV + hv) * D;
@@ -324,9 +407,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     // by its own leader two group-items ahead: right after the group has read a
     // slot, the copies for the item that uses it next are issued.
     auto land = [&](int lj) {
-      const int jl = live_j[lj];
-      const int2 el = table[jl];
-      const int itl = (int)blockIdx.x + jl * G, bl = itl / P.HV, hvl = itl % P.HV, hkl = hvl / P.G;
+      const int2 el = table[lj];  // the live items are the table's first entries
+      const int itl = titem[lj], bl = itl / P.HV, hvl = itl % P.HV, hkl = hvl / P.G;
       const int pl = el.y & 255, sl = el.x, l = lj % NL;
       uint8_t *ld = lands + l * lay.land_bytes;
       const uint32_t ring_bytes = (uint32_t)(pl * D * RB);
@@ -359,7 +441,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       }
       const int p = e.y & 255, slot = e.x, s = li % NF, t = li % NT, l = li % NL;
       const uint32_t u = (uint32_t)(li / NF), ut = (uint32_t)(li / NT), ul = (uint32_t)(li / NL);
-      const int item = (int)blockIdx.x + j * G, b = item / P.HV, hv = item % P.HV, hk = hv / P.G;
+      const int item = titem[j], b = item / P.HV, hv = item % P.HV, hk = hv / P.G;
       const int64_t bh = (int64_t)b * P.HV + hv;
       // small loads first, so their latency overlaps the waits
       float gc = 0.f, qv = 0.f, kv = 0.f, vv = 0.f, g_lo = 0.f, g_hi = 0.f;
@@ -522,11 +604,6 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       fence_proxy_async_smem();
       named_bar_sync(bar_id, 128);
       if (pt == 0) {
-        // the landing slot has been read: fill it for the item that uses it next
-        if (land_next < nlive) {
-          land(land_next);
-          land_next += 2;
-        }
         mbar_arrive(bars.inf(s));
         // contraction into accumulator acc once the epilogue has read it out
         const int acc = 2 * pg + ((li >> 1) & 1);
@@ -550,6 +627,11 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
           }
           last_acc = acc;
           last_use = ua;
+          // the landing slot has been read: fill it for the item that uses it next
+          if (land_next < nlive) {
+            land(land_next);
+            land_next += 2;
+          }
         }
       }
       ++li;
@@ -573,7 +655,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     int li = 0;
     for (int j = 0; j < n; ++j) {
       const int2 e = table[j];
-      const int item = (int)blockIdx.x + j * G, b = item / P.HV, hv = item % P.HV;
+      const int item = titem[j], b = item / P.HV, hv = item % P.HV;
       const int64_t bh = (int64_t)b * P.HV + hv;
       if (!(e.y & 512)) {
         if ((j & 1) == eg && row_live) store_from_f32(P.out, bh * D + r, P.out_dtype, 0.f);
