@@ -76,7 +76,7 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
   t.ld_g = t.ld_k + (uint32_t)(depth * D * ring_bytes);
   t.ld_q = t.ld_g + (uint32_t)(gate == GDN_GATE_PER_K ? depth * D * 4 : 0);
   t.land_bytes = (t.ld_q + (uint32_t)(qkv_bulk ? 3 * D * qkv_bytes : 0) + 127) & ~127u;
-  const uint32_t table = (uint32_t)kItemsMax * 8 + (uint32_t)kItemsMax * 4;  // table + live list
+  const uint32_t table = (uint32_t)kItemsMax * 16;  // item table
   const uint32_t bars = 1024;  // barriers, then misc words and the dealing's counters
   t.NT = NT;
   t.NF = NT + 4;  // a group's fields live from its prep until its epilogue, up to NT + 4 items later
@@ -120,6 +120,39 @@ struct TcpBars {
   __device__ uint32_t tf(int i) const { return tmem_full + 8 * i; }
   __device__ uint32_t te(int i) const { return tmem_empty + 8 * i; }
 };
+
+// Position in a ring of n slots walked in order, packed in one register:
+// bits 0-15 the slot, bit 16 the lap's parity (the mbarrier phase in which the
+// slot's "full" barrier completes), bit 17 set once past the first lap (a slot
+// must then first be released).
+struct RingPos {
+  uint32_t v;
+  __device__ int i() const { return (int)(v & 0xffffu); }
+  __device__ uint32_t ph() const { return (v >> 16) & 1u; }
+  __device__ bool lapped() const { return (v >> 17) != 0u; }
+  __device__ void init(int start, int n) {
+    v = 0u;
+    advance(start, n);
+  }
+  __device__ void advance(int k, int n) {
+    int i = (int)(v & 0xffffu) + k;
+    uint32_t hi = v & 0x30000u;
+    while (i >= n) {
+      i -= n;
+      hi = (hi ^ 0x10000u) | 0x20000u;
+    }
+    v = hi | (uint32_t)i;
+  }
+};
+
+// An item table entry: x slot, y p | flush << 8 | live << 9 | writes-k << 10,
+// z row b, w value head hv | key head hk << 16.
+__device__ __forceinline__ int tab_p(const int4 &e) { return e.y & 255; }
+__device__ __forceinline__ int tab_flush(const int4 &e) { return (e.y >> 8) & 1; }
+__device__ __forceinline__ bool tab_live(const int4 &e) { return (e.y & 512) != 0; }
+__device__ __forceinline__ bool tab_kw(const int4 &e) { return (e.y & 1024) != 0; }
+__device__ __forceinline__ int tab_hv(const int4 &e) { return e.w & 0xffff; }
+__device__ __forceinline__ int tab_hk(const int4 &e) { return e.w >> 16; }
 
 // Bounded wait that also gives up when another thread raised the abort flag.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
@@ -212,7 +245,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     if (tid == 0) set_status(P.status, GDN_DEV_INTERNAL);
     return;
   }
-  int2 *table = reinterpret_cast<int2 *>(smem + lay.off_table);
+  int4 *table = reinterpret_cast<int4 *>(smem + lay.off_table);
   uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + lay.off_bars);
   const uint32_t bar0 = smem_addr(bar_mem);
   TcpBars bars;
@@ -227,7 +260,6 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   // misc[0] TMEM base, misc[1] abort flag, misc[2..3] prep-group go/stop words,
   // misc[4] number of live items, misc[8..] the dealing's counters
   uint32_t *misc = reinterpret_cast<uint32_t *>(bar_mem + 2 * NB + NL + 2 * NF + NT + 8);
-  int *titem = reinterpret_cast<int *>(table + kItemsMax);  // b * HV + hv of table entry j
   volatile uint32_t *abort_flag = misc + 1;
 
   // --- dealing: the item table of this CTA ---
@@ -264,8 +296,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         if (ri.bad) set_status(P.status, ri.bad);
         if (P.flushed) P.flushed[b] = ri.live ? (uint8_t)ri.flush : 0;
       }
-      table[j] = make_int2(ri.slot, ri.p | (ri.flush << 8) | ((ri.live ? 1 : 0) << 9));
-      titem[j] = b * P.HV + hv;
+      table[j] = make_int4(ri.slot, ri.p | (ri.flush << 8) | ((ri.live ? 1 : 0) << 9) | ((hv % P.G == 0) << 10), b,
+                           hv | ((hv / P.G) << 16));
     }
   };
   // category of row b (3: past the end) and its rank within the warp
@@ -367,23 +399,20 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&tmap);
       uint32_t use = 0;
-      int li = 0;
+      RingPos bp;
+      bp.init(0, NB);
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
-        const int2 e = table[j];
-        if (!(e.y & 512)) continue;
-        const int hv = titem[j] % P.HV;
-        const int slot = e.x;
+        const int4 e = table[j];
+        if (!tab_live(e)) continue;
         // checkpoint boxes
-        const int row0 = (slot * P.HV + hv) * D;
+        const int row0 = (e.x * P.HV + tab_hv(e)) * D;
         for (int c = 0; c < NBOX; ++c, ++use) {
-          const int bs = (int)(use % NB);
-          const uint32_t ub = use / NB;
-          if (ub > 0 && !(ok = wait_bar(bars.be(bs), (ub - 1) & 1, abort_flag, P.status))) break;
-          mbar_arrive_expect_tx(bars.bf(bs), BOX_BYTES);
-          tma_load_2d(smem_addr(boxes + bs * BOX_BYTES), &tmap, 32 * c, row0, bars.bf(bs));
+          if (bp.lapped() && !(ok = wait_bar(bars.be(bp.i()), bp.ph() ^ 1u, abort_flag, P.status))) break;
+          mbar_arrive_expect_tx(bars.bf(bp.i()), BOX_BYTES);
+          tma_load_2d(smem_addr(boxes + bp.i() * BOX_BYTES), &tmap, 32 * c, row0, bars.bf(bp.i()));
+          bp.advance(1, NB);
         }
-        ++li;
       }
       if (*abort_flag)  // let this thread's copies still in flight land first
         for (uint32_t k = use > (uint32_t)NB ? use - NB : 0u; k < use; ++k)
@@ -406,10 +435,13 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     // The group's landing slots (li % NL with NL = 4: two per group) are filled
     // by its own leader two group-items ahead: right after the group has read a
     // slot, the copies for the item that uses it next are issued.
+    RingPos lp;  // landing slot of the next item to land
+    lp.init(pg, NL);
     auto land = [&](int lj) {
-      const int2 el = table[lj];  // the live items are the table's first entries
-      const int itl = titem[lj], bl = itl / P.HV, hvl = itl % P.HV, hkl = hvl / P.G;
-      const int pl = el.y & 255, sl = el.x, l = lj % NL;
+      const int4 el = table[lj];  // the live items are the table's first entries
+      const int bl = el.z, hvl = tab_hv(el), hkl = tab_hk(el);
+      const int pl = tab_p(el), sl = el.x, l = lp.i();
+      lp.advance(2, NL);
       uint8_t *ld = lands + l * lay.land_bytes;
       const uint32_t ring_bytes = (uint32_t)(pl * D * RB);
       const uint32_t gbytes = GATE == GDN_GATE_PER_K ? (uint32_t)(pl * D * 4) : 0u;
@@ -432,16 +464,24 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     };
     if (pt == 0)
       for (; land_next < nlive && land_next < pg + NL; land_next += 2) land(land_next);
+    RingPos fp, tp, cp;  // field stage, tile stage, landing slot of this group's next item
+    fp.init(pg, NF);
+    tp.init(pg, NT);
+    cp.init(pg, NL);
     for (int j = 0; j < n; ++j) {
-      const int2 e = table[j];
-      if (!(e.y & 512)) continue;
+      const int4 e = table[j];
+      if (!tab_live(e)) continue;
       if ((li & 1) != pg) {
         ++li;
         continue;
       }
-      const int p = e.y & 255, slot = e.x, s = li % NF, t = li % NT, l = li % NL;
-      const uint32_t u = (uint32_t)(li / NF), ut = (uint32_t)(li / NT), ul = (uint32_t)(li / NL);
-      const int item = titem[j], b = item / P.HV, hv = item % P.HV, hk = hv / P.G;
+      const int p = tab_p(e), slot = e.x, s = fp.i(), t = tp.i(), l = cp.i();
+      const uint32_t ph_f = fp.ph(), ph_t = tp.ph(), ph_l = cp.ph();
+      const bool lap_f = fp.lapped(), lap_t = tp.lapped();
+      fp.advance(2, NF);
+      tp.advance(2, NT);
+      cp.advance(2, NL);
+      const int b = e.z, hv = tab_hv(e), hk = tab_hk(e);
       const int64_t bh = (int64_t)b * P.HV + hv;
       // small loads first, so their latency overlaps the waits
       float gc = 0.f, qv = 0.f, kv = 0.f, vv = 0.f, g_lo = 0.f, g_hi = 0.f;
@@ -466,9 +506,9 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       // go/stop word it leaves before the group barrier makes the whole group
       // leave together, so the group's barriers stay uniform.
       if (pt == 0)
-        *go = (leader_ok && wait_bar(bars.lf(l), ul & 1, abort_flag, P.status) &&
-               (ut == 0 || wait_bar(bars.tle(t), (ut - 1) & 1, abort_flag, P.status)) &&
-               (u == 0 || wait_bar(bars.ine(s), (u - 1) & 1, abort_flag, P.status)))
+        *go = (leader_ok && wait_bar(bars.lf(l), ph_l, abort_flag, P.status) &&
+               (!lap_t || wait_bar(bars.tle(t), ph_t ^ 1u, abort_flag, P.status)) &&
+               (!lap_f || wait_bar(bars.ine(s), ph_f ^ 1u, abort_flag, P.status)))
                   ? 1u
                   : 0u;
       named_bar_sync(bar_id, 128);
@@ -653,11 +693,14 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     const bool row_live = r < D;   // warp-uniform
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     int li = 0;
+    RingPos fp, bp;  // field stage and first checkpoint box of this group's next item
+    fp.init(eg, NF);
+    bp.init(NBOX * eg, NB);
     for (int j = 0; j < n; ++j) {
-      const int2 e = table[j];
-      const int item = titem[j], b = item / P.HV, hv = item % P.HV;
+      const int4 e = table[j];
+      const int b = e.z, hv = tab_hv(e);
       const int64_t bh = (int64_t)b * P.HV + hv;
-      if (!(e.y & 512)) {
+      if (!tab_live(e)) {
         if ((j & 1) == eg && row_live) store_from_f32(P.out, bh * D + r, P.out_dtype, 0.f);
         continue;
       }
@@ -665,11 +708,14 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         ++li;
         continue;
       }
-      const int p = e.y & 255, slot = e.x, flush = (e.y >> 8) & 1, s = li % NF;
+      const int p = tab_p(e), slot = e.x, flush = tab_flush(e), s = fp.i();
+      const uint32_t ph_f = fp.ph();
+      fp.advance(2, NF);
       const int tb = 2 * eg + ((li >> 1) & 1);
-      const uint32_t u = (uint32_t)(li / NF), ut = (uint32_t)(li >> 2);
-      const uint32_t use = (uint32_t)(NBOX * li);
-      if (!wait_bar_warp(bars.inf(s), u & 1, abort_flag, P.status)) break;
+      const uint32_t ut = (uint32_t)(li >> 2);
+      const RingPos box0 = bp;
+      bp.advance(2 * NBOX, NB);
+      if (!wait_bar_warp(bars.inf(s), ph_f, abort_flag, P.status)) break;
       if (!wait_bar_warp(bars.tf(tb), ut & 1, abort_flag, P.status)) break;
       tc_fence_after();
       const float *f = reinterpret_cast<const float *>(fields + s * lay.field_bytes);
@@ -679,9 +725,10 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       const uint32_t trow = tmem + tb * D + lane_off;
       float2 sq01 = make_float2(0.f, 0.f), sq23 = sq01, sk01 = sq01, sk23 = sq01;
       bool ok = true;
-      for (int c = 0; c < NBOX; ++c) {
-        const int bs = (int)((use + c) % NB);
-        if (!(ok = wait_bar_warp(bars.bf(bs), ((use + c) / NB) & 1, abort_flag, P.status))) break;
+      RingPos bq = box0;
+      for (int c = 0; c < NBOX; ++c, bq.advance(1, NB)) {
+        const int bs = bq.i();
+        if (!(ok = wait_bar_warp(bars.bf(bs), bq.ph(), abort_flag, P.status))) break;
         if (row_live) {
           float acc[32];
           if (p > 0) {
@@ -727,7 +774,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       const float v_r = row_live ? fv[r] : 0.f;
       const float d = beta * (v_r - skt);
       if (row_live) store_from_f32(P.out, bh * D + r, P.out_dtype, fmaf(d, kq, sqt));
-      const int hk = hv / P.G;
+      const int hk = tab_hk(e);
       if (flush) {
         // second pass over the boxes: row r of alpha S + d k^T replaces row r of
         // the box; the warp then stores its 32 rows of the box to the checkpoint
@@ -735,8 +782,9 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         // box back to the producer
         const float2 d2 = make_float2(d, d);
         float *gwarp = P.state + (((int64_t)slot * P.HV + hv) * D + 32 * q4) * D + 4 * (lane & 7);
-        for (int c = 0; c < NBOX; ++c) {
-          const int bs = (int)((use + c) % NB);
+        bq = box0;
+        for (int c = 0; c < NBOX; ++c, bq.advance(1, NB)) {
+          const int bs = bq.i();
           if (row_live) {
             float acc[32];
             if (p > 0) {
@@ -785,7 +833,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         if (row_live) {
           store_from_f32(P.ring_d, (((int64_t)slot * P.HV + hv) * P.L + p) * D + r, RING_DT, d);
           if (GATE == GDN_GATE_PER_K) P.ring_g[(((int64_t)slot * P.HV + hv) * P.L + p) * D + r] = fg[r];
-          if (hv % P.G == 0)
+          if (tab_kw(e))
             store_from_f32(P.ring_k, (((int64_t)slot * P.HK + hk) * P.L + p) * D + r, RING_DT, fk[r]);
         }
         if (GATE == GDN_GATE_SCALAR && etid == 0) P.ring_g[((int64_t)slot * P.HV + hv) * P.L + p] = scal[4];
@@ -845,6 +893,7 @@ cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUte
   const int qkv_bulk =
       ((reinterpret_cast<uintptr_t>(P.qkv) & 15u) == 0 && ((P.qkv_stride * qes) & 15) == 0) ? 1 : 0;
   if (gate == GDN_GATE_PER_K && (reinterpret_cast<uintptr_t>(P.ring_g) & 15u) != 0) return cudaErrorNotSupported;
+  if (P.HV >= 32768) return cudaErrorNotSupported;  // the item table packs hv and hk into 16 bits each
   const int T = P.B * P.HV;
   int grid = sms > 0 && sms < T ? sms : T;
   if ((T + grid - 1) / grid > kItemsMax) grid = (T + kItemsMax - 1) / kItemsMax;
