@@ -13,6 +13,9 @@
 
 namespace gdn {
 
+// Longest sleep (ns) inside one mbarrier.try_wait.
+constexpr uint32_t kTryWaitSuspendNs = 1000000u;
+
 // Parameters of one decode / fold launch, already checked on the host.
 struct DecodeParams {
   int N, HV, HK, G, L;         // slots, value heads, key heads, HV/HK, ring length
@@ -43,6 +46,27 @@ __device__ __forceinline__ float load_as_f32(const void *p, int64_t i, int dtype
   if (dtype == GDN_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
   if (dtype == GDN_F16) return __half2float(reinterpret_cast<const __half *>(p)[i]);
   return reinterpret_cast<const float *>(p)[i];
+}
+
+// Three loads of the same dtype as fp32 (one dtype dispatch for all three).
+__device__ __forceinline__ void load3_as_f32(const void *p, int64_t i0, int64_t i1, int64_t i2, int dtype,
+                                             float &a, float &b, float &c) {
+  if (dtype == GDN_BF16) {
+    const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(p);
+    a = __bfloat162float(q[i0]);
+    b = __bfloat162float(q[i1]);
+    c = __bfloat162float(q[i2]);
+  } else if (dtype == GDN_F16) {
+    const __half *q = reinterpret_cast<const __half *>(p);
+    a = __half2float(q[i0]);
+    b = __half2float(q[i1]);
+    c = __half2float(q[i2]);
+  } else {
+    const float *q = reinterpret_cast<const float *>(p);
+    a = q[i0];
+    b = q[i1];
+    c = q[i2];
+  }
 }
 
 // Store with round-to-nearest-even to the destination type.
@@ -201,12 +225,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
+  // The thread may sleep in the instruction until the phase completes, for at
+  // most the hint (ns), so a waiting warp takes no issue slots meanwhile.
   asm volatile(
       "{\n\t.reg .pred P1;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, P1;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kTryWaitSuspendNs)
       : "memory");
   return done != 0;
 }
@@ -257,6 +283,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                    dst),
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// Asynchronous 4-byte copy global -> shared (both 4-byte aligned).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed; the arrival is not added to the barrier's expected count, so the
+// barrier must have been initialised to include it.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // 2-D tiled TMA store of one box from shared memory (bulk-group completion).

@@ -53,8 +53,10 @@ struct TcpLayout {
 };
 
 // Epilogue vectors of an item (floats): q, k, v for GDN; KDA adds a o k, a, the
-// total decay per channel and the current log-gate.  Then 8 scalars.
-__host__ __device__ inline int field_floats(int D, int gate) { return (gate == GDN_GATE_PER_K ? 7 : 3) * D + 8; }
+// total decay per channel and the current log-gate.  Then 16 scalars: alpha,
+// beta, A, the current log-gate, and at 8..11 the four prep warps' partial
+// sums of k.q.
+__host__ __device__ inline int field_floats(int D, int gate) { return (gate == GDN_GATE_PER_K ? 7 : 3) * D + 16; }
 
 // Shared memory: NB checkpoint boxes | NT operand tile stages | NF field stages
 // | NL landing slots | item table | barriers.
@@ -239,6 +241,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   const int G = gridDim.x;
   const int n = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / G + 1 : 0;
   const int NB = lay.NB, NT = lay.NT, NF = lay.NF, NL = lay.NL;
+  const int NBg = NB / 2;  // checkpoint box slots per epilogue group
   const int qes = P.qkv_dtype == GDN_F32 ? 4 : 2;
 
   if (smem_addr(smem) & 1023u) {  // the 128-byte swizzle assumes a 1024-byte aligned base
@@ -398,25 +401,35 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&tmap);
-      uint32_t use = 0;
-      RingPos bp;
-      bp.init(0, NB);
+      // Each epilogue group has its own NBg box slots (its items' boxes only),
+      // so consecutive users of a slot are always the same group: a slot's
+      // barrier can then never be waited on a lap ahead of its last phase.
+      uint32_t ug[2] = {0u, 0u};
+      RingPos bpg[2];
+      bpg[0].init(0, NBg);
+      bpg[1].init(0, NBg);
+      int li = 0;  // live items seen so far
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
         const int4 e = table[j];
         if (!tab_live(e)) continue;
         // checkpoint boxes
         const int row0 = (e.x * P.HV + tab_hv(e)) * D;
-        for (int c = 0; c < NBOX; ++c, ++use) {
-          if (bp.lapped() && !(ok = wait_bar(bars.be(bp.i()), bp.ph() ^ 1u, abort_flag, P.status))) break;
-          mbar_arrive_expect_tx(bars.bf(bp.i()), BOX_BYTES);
-          tma_load_2d(smem_addr(boxes + bp.i() * BOX_BYTES), &tmap, 32 * c, row0, bars.bf(bp.i()));
-          bp.advance(1, NB);
+        const int g = li & 1;
+        for (int c = 0; c < NBOX; ++c, ++ug[g]) {
+          RingPos &bp = bpg[g];
+          const int bs = g * NBg + bp.i();
+          if (bp.lapped() && !(ok = wait_bar(bars.be(bs), bp.ph() ^ 1u, abort_flag, P.status))) break;
+          mbar_arrive_expect_tx(bars.bf(bs), BOX_BYTES);
+          tma_load_2d(smem_addr(boxes + bs * BOX_BYTES), &tmap, 32 * c, row0, bars.bf(bs));
+          bp.advance(1, NBg);
         }
+        ++li;
       }
       if (*abort_flag)  // let this thread's copies still in flight land first
-        for (uint32_t k = use > (uint32_t)NB ? use - NB : 0u; k < use; ++k)
-          mbar_wait_bounded(bars.bf((int)(k % NB)), (k / NB) & 1, kWaitLimitNs);
+        for (int g = 0; g < 2; ++g)
+          for (uint32_t k = ug[g] > (uint32_t)NBg ? ug[g] - NBg : 0u; k < ug[g]; ++k)
+            mbar_wait_bounded(bars.bf(g * NBg + (int)(k % NBg)), (k / NBg) & 1, kWaitLimitNs);
     }
   } else if (warp < 9) {
     // ------------------------------------------------------------ prep + MMA
@@ -497,9 +510,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       const float beta = P.beta[bh];
       if (!lay.qkv_bulk && pt < D) {
         const int64_t qbase = (int64_t)b * P.qkv_stride;
-        qv = load_as_f32(P.qkv, qbase + (int64_t)hk * D + pt, P.qkv_dtype);
-        kv = load_as_f32(P.qkv, qbase + (int64_t)P.HK * D + (int64_t)hk * D + pt, P.qkv_dtype);
-        vv = load_as_f32(P.qkv, qbase + 2 * (int64_t)P.HK * D + (int64_t)hv * D + pt, P.qkv_dtype);
+        load3_as_f32(P.qkv, qbase + (int64_t)hk * D + pt, qbase + (int64_t)P.HK * D + (int64_t)hk * D + pt,
+                     qbase + 2 * (int64_t)P.HK * D + (int64_t)hv * D + pt, P.qkv_dtype, qv, kv, vv);
       }
       // Only the leader waits (landing slot filled, tile stage read by its last
       // contraction, field stage free); the
@@ -520,44 +532,57 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       const uint8_t *ld = lands + l * lay.land_bytes;
       const uint8_t *land_d = ld + lay.ld_d, *land_k = ld + lay.ld_k, *lq = ld + lay.ld_q;
       const float *land_g = reinterpret_cast<const float *>(ld + lay.ld_g);
-      if (lay.qkv_bulk && pt < D) {
-        qv = load_as_f32(lq, pt, P.qkv_dtype);
-        kv = load_as_f32(lq, D + pt, P.qkv_dtype);
-        vv = load_as_f32(lq, 2 * D + pt, P.qkv_dtype);
-      }
-      // q.q, k.k and k.q over the head, computed redundantly by every warp (no
-      // group barrier): lane l takes the channels l, l + 32, ...
-      float qq = 0.f, kk = 0.f, kq = 0.f;
-      for (int c = lane; c < D; c += 32) {
-        float qc, kc;
-        if (lay.qkv_bulk) {
-          qc = load_as_f32(lq, c, P.qkv_dtype);
-          kc = load_as_f32(lq, D + c, P.qkv_dtype);
-        } else {
-          const int64_t qbase = (int64_t)b * P.qkv_stride;
-          qc = load_as_f32(P.qkv, qbase + (int64_t)hk * D + c, P.qkv_dtype);
-          kc = load_as_f32(P.qkv, qbase + (int64_t)P.HK * D + (int64_t)hk * D + c, P.qkv_dtype);
-        }
-        qq = fmaf(qc, qc, qq);
-        kk = fmaf(kc, kc, kk);
-        kq = fmaf(kc, qc, kq);
-      }
+      if (lay.qkv_bulk && pt < D) load3_as_f32(lq, pt, D + pt, 2 * D + pt, P.qkv_dtype, qv, kv, vv);
+      float kq;
+      if (!P.qk_l2norm) {
+        // k.q: this thread's channel, summed over the warp; the epilogue adds
+        // the four warps' partial sums
+        qv *= P.q_scale;
+        kq = qv * kv;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        qq += __shfl_xor_sync(0xffffffffu, qq, o);
-        kk += __shfl_xor_sync(0xffffffffu, kk, o);
-        kq += __shfl_xor_sync(0xffffffffu, kq, o);
-      }
-      if (P.qk_l2norm) {
+        for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+      } else {
+        // in-kernel norm: q.q, k.k and k.q over the whole head, computed
+        // redundantly by every warp (lane l takes the channels l, l + 32, ...);
+        // warp 0 carries the sum of k.q
+        float qq = 0.f, kk = 0.f;
+        kq = 0.f;
+        for (int c = lane; c < D; c += 32) {
+          float qc, kc, unused;
+          if (lay.qkv_bulk) {
+            load3_as_f32(lq, c, D + c, D + c, P.qkv_dtype, qc, kc, unused);
+          } else {
+            const int64_t qbase = (int64_t)b * P.qkv_stride;
+            load3_as_f32(P.qkv, qbase + (int64_t)hk * D + c, qbase + (int64_t)P.HK * D + (int64_t)hk * D + c,
+                         qbase + (int64_t)P.HK * D + (int64_t)hk * D + c, P.qkv_dtype, qc, kc, unused);
+          }
+          qq = fmaf(qc, qc, qq);
+          kk = fmaf(kc, kc, kk);
+          kq = fmaf(kc, qc, kq);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          qq += __shfl_xor_sync(0xffffffffu, qq, o);
+          kk += __shfl_xor_sync(0xffffffffu, kk, o);
+          kq += __shfl_xor_sync(0xffffffffu, kq, o);
+        }
         const float nq = sqrtf(qq + 1e-6f), nk = sqrtf(kk + 1e-6f);
-        qv = qv / nq;
+        qv = qv / nq * P.q_scale;
         kv = kv / nk;
-        kq = kq / (nq * nk);
+        kq = (pt >> 5) == 0 ? kq / (nq * nk) * P.q_scale : 0.f;
       }
-      qv *= P.q_scale;
-      kq *= P.q_scale;
 
+      // Operand rows, newest entry first (GDN: A row pt w_j d_j[pt], B row pt
+      // k_j[pt]; KDA: A row pt d_j[pt], B row pt w_j[pt] k_j[pt]).  Entries
+      // j >= p are zero (selected, never multiplied: stale ring rows may hold
+      // anything); their loads read row min(j, p - 1) of the slot.  The
+      // weights w_j are rounded to the operand type right after, so the fast
+      // exponential's error (of order 1e-6 relative for the sums seen here) is
+      // far below that rounding; A, which scales the fp32 checkpoint, uses
+      // the accurate one.
       float A = 1.f;
+      const int jmax = p > 0 ? p - 1 : 0;
+      const int ptc = pt < D ? pt : 0;
       if (GATE == GDN_GATE_SCALAR) {
         // Suffix sums of the log-gates by a warp scan (each warp on its own):
         // afterwards lane l holds T_l = sum_{l<=i<p} g_i; w_j = exp(T_{j+1}),
@@ -578,21 +603,21 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         A = p > 0 ? expf(__shfl_sync(0xffffffffu, t_lo, 0)) : 1.f;
         // w for entry j lives in lane j (lo: j < 32, hi: j >= 32)
         const float nxt_lo = __shfl_down_sync(0xffffffffu, t_lo, 1);
-        const float w_lo = expf(lane == 31 ? hi_total : nxt_lo);
+        const float w_lo = __expf(lane == 31 ? hi_total : nxt_lo);
         const float nxt_hi = __shfl_down_sync(0xffffffffu, t_hi, 1);
-        const float w_hi = expf(lane == 31 ? 0.f : nxt_hi);
-        // A row pt: w_j d_j[pt];  B row pt: k_j[pt]
+        const float w_hi = __expf(lane == 31 ? 0.f : nxt_hi);
         for (int h = 0; h < lay.KC; ++h) {
           float xa[EPC], xb[EPC];
 #pragma unroll
           for (int e2 = 0; e2 < EPC; ++e2) {
             const int jj = h * EPC + e2;
+            const int jc = jj < jmax ? jj : jmax;
+            const bool valid = jj < p && pt < D;
             const float wj = __shfl_sync(0xffffffffu, jj < 32 ? w_lo : w_hi, jj & 31);
-            xa[e2] = xb[e2] = 0.f;
-            if (jj < p && pt < D) {
-              xa[e2] = wj * load_as_f32(land_d, (int64_t)jj * D + pt, RING_DT);
-              xb[e2] = load_as_f32(land_k, (int64_t)jj * D + pt, RING_DT);
-            }
+            const float dj = load_as_f32(land_d, (int64_t)jc * D + ptc, RING_DT);
+            const float kj = load_as_f32(land_k, (int64_t)jc * D + ptc, RING_DT);
+            xa[e2] = valid ? wj * dj : 0.f;
+            xb[e2] = valid ? kj : 0.f;
           }
           put_chunk<KIND, EPC>(tA, pt, h, lay.KC, xa);
           if (pt < D) put_chunk<KIND, EPC>(tB, pt, h, lay.KC, xb);
@@ -606,13 +631,15 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
 #pragma unroll
           for (int e2 = EPC - 1; e2 >= 0; --e2) {
             const int jj = h * EPC + e2;
-            xa[e2] = xb[e2] = 0.f;
-            if (jj < p && pt < D) {
-              const float wj = expf(sfx);
-              sfx += land_g[jj * D + pt];
-              xa[e2] = load_as_f32(land_d, (int64_t)jj * D + pt, RING_DT);
-              xb[e2] = wj * load_as_f32(land_k, (int64_t)jj * D + pt, RING_DT);
-            }
+            const int jc = jj < jmax ? jj : jmax;
+            const bool valid = jj < p && pt < D;
+            const float wj = __expf(sfx);
+            const float gj = land_g[jc * D + ptc];
+            const float dj = load_as_f32(land_d, (int64_t)jc * D + ptc, RING_DT);
+            const float kj = load_as_f32(land_k, (int64_t)jc * D + ptc, RING_DT);
+            sfx += valid ? gj : 0.f;
+            xa[e2] = valid ? dj : 0.f;
+            xb[e2] = valid ? wj * kj : 0.f;
           }
           put_chunk<KIND, EPC>(tA, pt, h, lay.KC, xa);
           if (pt < D) put_chunk<KIND, EPC>(tB, pt, h, lay.KC, xb);
@@ -634,11 +661,11 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
           fq[pt] = qv;
         }
       }
+      if (lane == 0) scal[8 + (pt >> 5)] = kq;
       if (pt == 0) {
         scal[0] = GATE == GDN_GATE_SCALAR ? expf(gc) : 1.f;
         scal[1] = beta;
         scal[2] = A;
-        scal[3] = kq;
         scal[4] = gc;
       }
       fence_proxy_async_smem();
@@ -695,7 +722,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     int li = 0;
     RingPos fp, bp;  // field stage and first checkpoint box of this group's next item
     fp.init(eg, NF);
-    bp.init(NBOX * eg, NB);
+    bp.init(0, NBg);
     for (int j = 0; j < n; ++j) {
       const int4 e = table[j];
       const int b = e.z, hv = tab_hv(e);
@@ -714,20 +741,20 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       const int tb = 2 * eg + ((li >> 1) & 1);
       const uint32_t ut = (uint32_t)(li >> 2);
       const RingPos box0 = bp;
-      bp.advance(2 * NBOX, NB);
+      bp.advance(NBOX, NBg);
       if (!wait_bar_warp(bars.inf(s), ph_f, abort_flag, P.status)) break;
       if (!wait_bar_warp(bars.tf(tb), ut & 1, abort_flag, P.status)) break;
       tc_fence_after();
       const float *f = reinterpret_cast<const float *>(fields + s * lay.field_bytes);
       const float *fq = f, *fk = f + D, *fv = f + 2 * D, *fke = GATE == GDN_GATE_PER_K ? f + 3 * D : fk,
                   *fa = f + 4 * D, *fA = f + 5 * D, *fg = f + 6 * D, *scal = f + NVEC * D;
-      const float alpha = scal[0], beta = scal[1], A = scal[2], kq = scal[3];
+      const float alpha = scal[0], beta = scal[1], A = scal[2], kq = (scal[8] + scal[9]) + (scal[10] + scal[11]);
       const uint32_t trow = tmem + tb * D + lane_off;
       float2 sq01 = make_float2(0.f, 0.f), sq23 = sq01, sk01 = sq01, sk23 = sq01;
       bool ok = true;
       RingPos bq = box0;
-      for (int c = 0; c < NBOX; ++c, bq.advance(1, NB)) {
-        const int bs = bq.i();
+      for (int c = 0; c < NBOX; ++c, bq.advance(1, NBg)) {
+        const int bs = eg * NBg + bq.i();
         if (!(ok = wait_bar_warp(bars.bf(bs), bq.ph(), abort_flag, P.status))) break;
         if (row_live) {
           float acc[32];
@@ -783,8 +810,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         const float2 d2 = make_float2(d, d);
         float *gwarp = P.state + (((int64_t)slot * P.HV + hv) * D + 32 * q4) * D + 4 * (lane & 7);
         bq = box0;
-        for (int c = 0; c < NBOX; ++c, bq.advance(1, NB)) {
-          const int bs = bq.i();
+        for (int c = 0; c < NBOX; ++c, bq.advance(1, NBg)) {
+          const int bs = eg * NBg + bq.i();
           if (row_live) {
             float acc[32];
             if (p > 0) {
@@ -898,7 +925,7 @@ cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUte
   int grid = sms > 0 && sms < T ? sms : T;
   if ((T + grid - 1) / grid > kItemsMax) grid = (T + kItemsMax - 1) / kItemsMax;
   const TcpLayout lay = tcp_pick_layout(D, kind, gate, P.L, ring_bytes, qes, qkv_bulk, optin);
-  if (lay.NB < D / 32 + 1 || lay.total > (uint32_t)optin) return cudaErrorNotSupported;
+  if (lay.NB < 2 * (D / 32) || lay.total > (uint32_t)optin) return cudaErrorNotSupported;
   if (D == 128)
     return gate == GDN_GATE_SCALAR ? launch_tcp_ring<128, 0>(P, map, lay, grid, s)
                                    : launch_tcp_ring<128, 1>(P, map, lay, grid, s);
