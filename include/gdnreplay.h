@@ -3,9 +3,9 @@
  * decode with the ReplaySSM checkpoint + ring cache, for one GB300 (sm_103a).
  *
  * C ABI.  Every pointer in a call below is a DEVICE pointer unless its comment
- * says otherwise.  Every buffer is owned by the caller; the library allocates
- * no device memory and never synchronises: each call enqueues kernels on
- * `stream` and returns.  Host-side argument checks run before any launch and
+ * says otherwise.  Every buffer, scratch workspace included, is owned by the
+ * caller; the library allocates no device memory and never synchronises: each
+ * call enqueues kernels on `stream` and returns.  Host-side argument checks run before any launch and
  * return GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED with nothing enqueued; a
  * launch failure returns GDN_ERR_CUDA.  gdn_last_error() gives the calling
  * thread's message for its last failing call.
@@ -152,6 +152,23 @@ GDN_API gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gd
                                   const int32_t *write_pos, const uint8_t *force_flush,
                                   const gdn_step_t *step, int32_t recon, uint8_t *flushed_out,
                                   uint32_t *dev_status, gdn_stream_t stream);
+
+/* gdn_replayssm_decode of the forward's last layer followed by
+ * gdn_replayssm_advance for the same rows, with the same results as the two
+ * calls: the cursors are read before any is advanced.  On the tensor-core path
+ * both happen in one launch (every block reads the cursors first; the last
+ * block to finish advances them), otherwise in two.  write_pos is read and
+ * written.  workspace: a caller-owned device buffer of
+ * GDN_DECODE_ADVANCE_WORKSPACE_BYTES, 4-byte aligned, zeroed once before its
+ * first use; every call leaves it zero again.  Calls that share a workspace
+ * must not overlap on the GPU (e.g. on two streams).  Other arguments as in
+ * gdn_replayssm_decode. */
+#define GDN_DECODE_ADVANCE_WORKSPACE_BYTES 4
+GDN_API gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
+                                          int32_t *write_pos, const uint8_t *force_flush,
+                                          const gdn_step_t *step, int32_t recon, uint8_t *flushed_out,
+                                          uint32_t *workspace, uint32_t *dev_status,
+                                          gdn_stream_t stream);
 
 /* Cursor advance, once per forward after all layers ([P1] Design 3):
  * write_pos[s] <- (write_pos[s] == L-1 or force_flush[b]) ? 0 : write_pos[s] + 1

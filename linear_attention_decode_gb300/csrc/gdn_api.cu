@@ -157,10 +157,55 @@ gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gdn_layer_
     e = gdn::launch_ffma_decode(P, desc->k_dim, desc->gate, true, (cudaStream_t)stream);
   } else {
     const char *why = nullptr;
-    e = gdn::launch_tc_decode(P, desc->k_dim, desc->gate, (cudaStream_t)stream, &why);
+    bool fused = false;
+    e = gdn::launch_tc_decode(P, desc->k_dim, desc->gate, (cudaStream_t)stream, &why, &fused);
     if (e != cudaSuccess && why) return fail(GDN_ERR_CUDA, why);
   }
   return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_replayssm_decode launch");
+}
+
+gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
+                                          int32_t *write_pos, const uint8_t *force_flush,
+                                          const gdn_step_t *step, int32_t recon, uint8_t *flushed_out,
+                                          uint32_t *workspace, uint32_t *dev_status, gdn_stream_t stream) {
+  gdn_status_t st = check_desc(desc);
+  if (st != GDN_OK) return st;
+  if ((st = check_step(desc, step)) != GDN_OK) return st;
+  if ((st = check_cache(desc, cache)) != GDN_OK) return st;
+  if (!write_pos) return fail(GDN_ERR_INVALID_ARG, "write_pos is NULL");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+    return fail(GDN_ERR_INVALID_ARG, "workspace must be a 4-byte aligned device pointer");
+  if (recon != GDN_RECON_TENSOR && recon != GDN_RECON_FFMA)
+    return fail(GDN_ERR_INVALID_ARG, "recon must be GDN_RECON_TENSOR or GDN_RECON_FFMA");
+  if (step->batch == 0) return GDN_OK;
+  gdn::DecodeParams P = base_params(desc);
+  fill_step(P, step);
+  P.state = cache->state;
+  P.ring_d = cache->ring_d;
+  P.ring_k = cache->ring_k;
+  P.ring_g = cache->ring_g;
+  P.write_pos = write_pos;
+  P.force_flush = force_flush;
+  P.flushed = flushed_out;
+  P.status = dev_status;
+  cudaError_t e;
+  bool fused = false;
+  if (recon == GDN_RECON_FFMA) {
+    e = gdn::launch_ffma_decode(P, desc->k_dim, desc->gate, true, (cudaStream_t)stream);
+  } else {
+    P.sync = workspace;
+    P.write_pos_w = write_pos;
+    const char *why = nullptr;
+    e = gdn::launch_tc_decode(P, desc->k_dim, desc->gate, (cudaStream_t)stream, &why, &fused);
+    if (e != cudaSuccess && why) return fail(GDN_ERR_CUDA, why);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "gdn_replayssm_decode_advance launch");
+  if (!fused) {  // the kernel that ran left the cursors alone: advance them in a second launch
+    e = gdn::launch_advance(step->ssm_state_indices, step->batch, force_flush, desc->num_slots, desc->ring_len,
+                            write_pos, dev_status, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_replayssm_decode_advance: advance launch");
+  }
+  return GDN_OK;
 }
 
 gdn_status_t gdn_replayssm_advance(const int32_t *ssm_state_indices, int32_t batch,

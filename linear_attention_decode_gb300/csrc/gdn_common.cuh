@@ -40,6 +40,11 @@ struct DecodeParams {
   uint8_t *flushed;            // [B] or null
   uint32_t *status;            // or null
   const int32_t *slots;        // fold: [n]
+  // decode + advance in one launch (persistent tensor-core kernel only): a
+  // completion counter in caller workspace (zero between launches), and the
+  // cursors the last CTA to finish advances; both null otherwise
+  uint32_t *sync;
+  int32_t *write_pos_w;
 };
 
 __device__ __forceinline__ float load_as_f32(const void *p, int64_t i, int dtype) {

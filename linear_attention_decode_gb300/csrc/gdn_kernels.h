@@ -13,7 +13,10 @@ cudaError_t launch_ffma_decode(const DecodeParams &P, int D, int gate, bool repl
 
 // ReplaySSM decode with the replay sum on the tensor cores (tcgen05) and the
 // checkpoint streamed by TMA.  Writes a reason into *why on a host-side failure.
-cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why);
+// With P.sync set, *fused tells whether the launched kernel also advanced the
+// cursors (the persistent kernel does; the one-CTA-per-head fallback does not).
+cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why,
+                             bool *fused);
 
 // Persistent warp-specialised variant of the above (one CTA per SM).  Returns
 // cudaErrorNotSupported, with nothing launched, when its shared-memory layout

@@ -315,7 +315,9 @@ static cudaError_t launch_kind(const DecodeParams &P, const CUtensorMap &map, si
   return launch_t<D, GATE, 2, GDN_F32>(P, map, smem, s);
 }
 
-cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why) {
+cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why,
+                             bool *fused) {
+  *fused = false;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) {
     *why = "cuTensorMapEncodeTiled is not available from the driver";
@@ -336,7 +338,10 @@ cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_
     return cudaErrorInvalidValue;
   }
   const cudaError_t e = launch_tcp_decode(P, D, gate, map, s);
-  if (e != cudaErrorNotSupported) return e;
+  if (e != cudaErrorNotSupported) {
+    *fused = e == cudaSuccess && P.sync != nullptr;
+    return e;
+  }
   const int kind = kind_of(P.ring_dtype);
   const size_t smem = tc_layout(D, kind, P.L).total;
   if (D == 128)

@@ -47,7 +47,7 @@ struct TcpLayout {
   int KD, KC, NT, NF, NL, NB;
   int qkv_bulk;  // 1: q, k, v arrive by bulk copy (16-byte aligned rows)
   uint32_t box_bytes, tile_bytes, field_bytes, land_bytes;
-  uint32_t off_tile, off_field, off_land, off_table, off_bars, total;
+  uint32_t off_tile, off_field, off_land, off_table, off_adv, off_bars, total;
   uint32_t t_B;                     // B operand inside a tile stage (A at 0)
   uint32_t ld_d, ld_k, ld_g, ld_q;  // inside a landing slot
 };
@@ -79,19 +79,21 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
   t.ld_q = t.ld_g + (uint32_t)(gate == GDN_GATE_PER_K ? depth * D * 4 : 0);
   t.land_bytes = (t.ld_q + (uint32_t)(qkv_bulk ? 3 * D * qkv_bytes : 0) + 127) & ~127u;
   const uint32_t table = (uint32_t)kItemsMax * 16;  // item table
+  const uint32_t adv = (uint32_t)kTcpThreads * 4;  // the rows' next cursors (decode + advance)
   const uint32_t bars = 1024;  // barriers, then misc words and the dealing's counters
   t.NT = NT;
   t.NF = NT + 4;  // a group's fields live from its prep until its epilogue, up to NT + 4 items later
   t.NL = NL;
   const long rest = (long)smem_budget - (long)t.NT * t.tile_bytes - (long)t.NF * t.field_bytes -
-                    (long)t.NL * t.land_bytes - table - bars;
+                    (long)t.NL * t.land_bytes - table - adv - bars;
   t.NB = rest > 0 ? (int)(rest / t.box_bytes) : 0;
   if (t.NB > 16) t.NB = 16;
   t.off_tile = (uint32_t)t.NB * t.box_bytes;
   t.off_field = t.off_tile + (uint32_t)t.NT * t.tile_bytes;
   t.off_land = t.off_field + (uint32_t)t.NF * t.field_bytes;
   t.off_table = t.off_land + (uint32_t)t.NL * t.land_bytes;
-  t.off_bars = t.off_table + table;
+  t.off_adv = t.off_table + table;
+  t.off_bars = t.off_adv + adv;
   t.total = t.off_bars + bars;
   return t;
 }
@@ -249,6 +251,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     return;
   }
   int4 *table = reinterpret_cast<int4 *>(smem + lay.off_table);
+  // decode + advance: row b's slot << 7 | next cursor, or -1 (single-pass dealing)
+  int *advq = reinterpret_cast<int *>(smem + lay.off_adv);
   uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + lay.off_bars);
   const uint32_t bar0 = smem_addr(bar_mem);
   TcpBars bars;
@@ -261,7 +265,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   bars.tmem_full = bars.tile_empty + 8u * NT;
   bars.tmem_empty = bars.tmem_full + 32u;  // four accumulators
   // misc[0] TMEM base, misc[1] abort flag, misc[2..3] prep-group go/stop words,
-  // misc[4] number of live items, misc[8..] the dealing's counters
+  // misc[4] number of live items, misc[7] last CTA to finish (decode +
+  // advance), misc[8..] the dealing's counters
   uint32_t *misc = reinterpret_cast<uint32_t *>(bar_mem + 2 * NB + NL + 2 * NF + NT + 8);
   volatile uint32_t *abort_flag = misc + 1;
 
@@ -318,6 +323,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   if (P.B <= kTcpThreads) {  // one row per thread: one pass, one barrier
     const bool in = tid < P.B;
     const RowInfo ri = in ? resolve_row(P, tid, false) : RowInfo{-1, 0, 0, false, 0u};
+    if (P.sync) advq[tid] = (in && ri.live) ? ((ri.slot << 7) | (ri.flush ? 0 : ri.p + 1)) : -1;
     int rank = 0;
     const int cat = classify(ri, in, rank);
     __syncthreads();
@@ -876,6 +882,32 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 4 * D);
   }
+
+  // Decode + advance ([P1] Design 3): every CTA read the cursors while dealing,
+  // long before it got here; the last CTA to finish advances them and leaves
+  // the counter at zero for the next launch.  No CTA waits for another.
+  if (P.sync) {
+    if (tid == 0) {
+      __threadfence();
+      misc[7] = atomicAdd(P.sync, 1u) == (uint32_t)(G - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (misc[7]) {
+      __threadfence();
+      if (P.B <= kTcpThreads) {
+        if (tid < P.B) {
+          const int q = advq[tid];
+          if (q >= 0) P.write_pos_w[q >> 7] = q & 127;
+        }
+      } else {
+        for (int b = tid; b < P.B; b += kTcpThreads) {
+          const RowInfo ri = resolve_row(P, b, false);
+          if (ri.live) P.write_pos_w[ri.slot] = ri.flush ? 0 : ri.p + 1;
+        }
+      }
+      if (tid == 0) *P.sync = 0u;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -921,6 +953,7 @@ cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUte
       ((reinterpret_cast<uintptr_t>(P.qkv) & 15u) == 0 && ((P.qkv_stride * qes) & 15) == 0) ? 1 : 0;
   if (gate == GDN_GATE_PER_K && (reinterpret_cast<uintptr_t>(P.ring_g) & 15u) != 0) return cudaErrorNotSupported;
   if (P.HV >= 32768) return cudaErrorNotSupported;  // the item table packs hv and hk into 16 bits each
+  if (P.sync && P.N >= (1 << 24)) return cudaErrorNotSupported;  // decode + advance packs the slot in 24 bits
   const int T = P.B * P.HV;
   int grid = sms > 0 && sms < T ? sms : T;
   if ((T + grid - 1) / grid > kItemsMax) grid = (T + kItemsMax - 1) / kItemsMax;

@@ -29,7 +29,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = declared_entry_points()
-    for n in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_advance",
+    for n in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_decode_advance", "gdn_replayssm_advance",
               "gdn_replayssm_flush", "gdn_replayssm_reset_slots", "gdn_status_str", "gdn_last_error"):
         assert n in names
 
@@ -104,3 +104,23 @@ def test_empty_calls_are_no_ops(lib):
 def test_status_strings(lib):
     assert lib.gdn_status_str(0).decode() == "ok"
     assert "invalid" in lib.gdn_status_str(1).decode()
+
+
+def test_decode_advance_checks_its_workspace(lib):
+    d = _desc()
+    cache = Bd._Cache(0x1000, 0x1000, 0x1000, 0x1000)
+    f = lib.gdn_replayssm_decode_advance
+    # no workspace, misaligned workspace, no write_pos, unknown recon: rejected before any launch
+    for wp, ws, recon in ((0x1000, None, 0), (0x1000, 0x1002, 0), (None, 0x1000, 0), (0x1000, 0x1000, 9)):
+        assert f(ctypes.byref(d), ctypes.byref(cache), wp, None, ctypes.byref(_step()), recon, None, ws,
+                 None, None) == 1, lib.gdn_last_error().decode()
+    assert f(ctypes.byref(_desc(k_dim=96, v_dim=96)), ctypes.byref(cache), 0x1000, None, ctypes.byref(_step()),
+             0, None, 0x1000, None, None) == 2
+    assert f(ctypes.byref(d), ctypes.byref(cache), 0x1000, None, ctypes.byref(_step(batch=0)), 0, None, 0x1000,
+             None, None) == 0
+
+
+def test_workspace_size_constant_matches_the_header():
+    text = open(os.path.join(ROOT, "include", "gdnreplay.h")).read()
+    m = re.search(r"#define GDN_DECODE_ADVANCE_WORKSPACE_BYTES (\d+)", text)
+    assert m and int(m.group(1)) == Bd.DECODE_ADVANCE_WORKSPACE_BYTES

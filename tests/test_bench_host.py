@@ -45,7 +45,9 @@ def test_launch_bytes_counts_padding_rows():
     w = I.QWEN3NEXT_LAYER
     one = bench.launch_bytes(w, [3], [False], 2, 0)
     assert bench.launch_bytes(w, [3], [False], 2, 4) == one + 4 * w.HV * w.V * 2
-    assert one == w.HV * bench.head_step_bytes(128, 128, 2, 3, False, 2, 2, 2)
+    # the live row's cursor is read and written once by the fused advance
+    assert one == w.HV * bench.head_step_bytes(128, 128, 2, 3, False, 2, 2, 2) + 8
+    assert bench.launch_bytes(w, [3], [False], 2, 0, cursors=False) == one - 8
 
 
 def _rank(rank, world, port, q):
