@@ -170,6 +170,27 @@ GDN_API gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, 
                                           uint32_t *workspace, uint32_t *dev_status,
                                           gdn_stream_t stream);
 
+/* gdn_replayssm_decode_advance without a caller workspace, for callers that
+ * cannot allocate device memory: an engine that has reserved the whole device
+ * for its own state and KV pools, a plugin whose host owns every allocation,
+ * code that must not trigger cudaMalloc's implicit synchronisation.  The pages
+ * have no counterpart; it exists only for such callers.
+ * The scratch (one completion counter, GDN_DECODE_ADVANCE_WORKSPACE_BYTES)
+ * comes from a 256-byte array compiled into the library, which every GPU that
+ * loads the library keeps until the process exits; a call whose scratch need
+ * exceeded it would be rejected with GDN_ERR_UNSUPPORTED.  The first call on a
+ * device (the current one) looks the array's address up and clears it,
+ * synchronously: make that first call before any stream capture.  All calls on
+ * a device share the array, and every launch that runs to its end leaves the
+ * counter at zero; calls that overlap on the GPU (e.g. on two streams) race on
+ * it and must not be issued.  Nothing is allocated.  Arguments and results as
+ * in gdn_replayssm_decode_advance. */
+GDN_API gdn_status_t gdn_replayssm_decode_advance_noalloc(const gdn_layer_desc_t *desc,
+                                                  const gdn_layer_cache_t *cache, int32_t *write_pos,
+                                                  const uint8_t *force_flush, const gdn_step_t *step,
+                                                  int32_t recon, uint8_t *flushed_out,
+                                                  uint32_t *dev_status, gdn_stream_t stream);
+
 /* Cursor advance, once per forward after all layers ([P1] Design 3):
  * write_pos[s] <- (write_pos[s] == L-1 or force_flush[b]) ? 0 : write_pos[s] + 1
  * for each row b with s = ssm_state_indices[b] >= 0.  force_flush may be NULL. */

@@ -93,11 +93,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_packed_decode.argtypes = [dp, vp, sp, u32p, vp]
         lib.gdn_replayssm_decode.argtypes = [dp, cp, vp, vp, sp, i32, vp, u32p, vp]
         lib.gdn_replayssm_decode_advance.argtypes = [dp, cp, vp, vp, sp, i32, vp, vp, u32p, vp]
+        lib.gdn_replayssm_decode_advance_noalloc.argtypes = [dp, cp, vp, vp, sp, i32, vp, u32p, vp]
         lib.gdn_replayssm_advance.argtypes = [vp, i32, vp, i32, i32, vp, u32p, vp]
         lib.gdn_replayssm_flush.argtypes = [dp, cp, vp, vp, i32, u32p, vp]
         lib.gdn_replayssm_reset_slots.argtypes = [vp, i32, vp, i32, u32p, vp]
         for f in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_decode_advance",
-                  "gdn_replayssm_advance", "gdn_replayssm_flush", "gdn_replayssm_reset_slots"):
+                  "gdn_replayssm_decode_advance_noalloc", "gdn_replayssm_advance", "gdn_replayssm_flush",
+                  "gdn_replayssm_reset_slots"):
             getattr(lib, f).restype = ctypes.c_int
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
@@ -219,6 +221,24 @@ def gdn_replayssm_decode_advance(desc: LayerDesc, cache: Cache, write_pos: torch
         _dev(flushed_out, "flushed_out", (B,), torch.uint8, optional=True),
         _dev(workspace, "workspace", (DECODE_ADVANCE_WORKSPACE_BYTES // 4,), torch.int32),
         _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_decode_advance")
+
+
+def gdn_replayssm_decode_advance_noalloc(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor,
+                                         force_flush: Optional[torch.Tensor], step: Step,
+                                         recon: int = RECON_TENSOR, flushed_out: Optional[torch.Tensor] = None,
+                                         dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """gdn_replayssm_decode_advance with the library's own scratch: for callers
+    that cannot allocate device memory (see the C declaration)."""
+    B = step.ssm_state_indices.shape[0]
+    c = _pack_cache(desc, cache)
+    s = _pack_step(desc, step)
+    _check(load_library().gdn_replayssm_decode_advance_noalloc(
+        ctypes.byref(desc), ctypes.byref(c),
+        _dev(write_pos, "write_pos", (desc.num_slots,), torch.int32),
+        _dev(force_flush, "force_flush", (B,), torch.uint8, optional=True),
+        ctypes.byref(s), int(recon),
+        _dev(flushed_out, "flushed_out", (B,), torch.uint8, optional=True),
+        _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_decode_advance_noalloc")
 
 
 def gdn_replayssm_advance(ssm_state_indices: torch.Tensor, force_flush: Optional[torch.Tensor],

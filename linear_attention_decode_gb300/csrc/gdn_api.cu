@@ -100,6 +100,10 @@ gdn_status_t check_cache(const gdn_layer_desc_t *d, const gdn_layer_cache_t *c) 
 
 }  // namespace
 
+namespace gdn {
+void set_last_error(const char *msg) { g_last_error = msg; }
+}  // namespace gdn
+
 extern "C" {
 
 const char *gdn_status_str(gdn_status_t s) {

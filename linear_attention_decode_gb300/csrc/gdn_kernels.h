@@ -34,4 +34,8 @@ cudaError_t launch_reset(int32_t *write_pos, int N, const int32_t *slots, int n,
 // Dynamic shared memory of one tensor-core decode CTA (bytes).
 size_t tc_smem_bytes(int D, int gate, int ring_dtype, int L);
 
+// Sets the calling thread's gdn_last_error() text (for entry points defined
+// outside the C ABI file).
+void set_last_error(const char *msg);
+
 }  // namespace gdn
