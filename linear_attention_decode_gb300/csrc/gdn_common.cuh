@@ -218,6 +218,12 @@ __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) 
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch: wait until the grid this one depends on has
+// completed and its memory is visible (a no-op without such a dependency), and
+// allow the grid that depends on this one to be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Barrier among `nthreads` threads (whole warps) on hardware barrier `id` (1..15).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

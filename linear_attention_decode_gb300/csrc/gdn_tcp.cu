@@ -270,6 +270,36 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   uint32_t *misc = reinterpret_cast<uint32_t *>(bar_mem + 2 * NB + NL + 2 * NF + NT + 8);
   volatile uint32_t *abort_flag = misc + 1;
 
+  // Set-up that reads nothing an earlier kernel writes: barriers, TMEM, the
+  // tensor map.  With a programmatic dependency on the previous launch in the
+  // stream it overlaps that launch's tail; everything after the dependency
+  // wait (the cursors, the rows, the cache) sees the previous launch complete.
+  if (tid == 0) {
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(bars.bf(i), 1);
+      mbar_init(bars.be(i), 4);  // one arrival per epilogue warp
+    }
+    for (int i = 0; i < NL; ++i) mbar_init(bars.lf(i), 1);
+    for (int i = 0; i < NF; ++i) {
+      mbar_init(bars.inf(i), 1);
+      mbar_init(bars.ine(i), 4);
+    }
+    for (int i = 0; i < NT; ++i) mbar_init(bars.tle(i), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bars.tf(i), 1);
+      mbar_init(bars.te(i), 4);
+    }
+    misc[1] = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(misc), 4 * D);
+    tmem_relinquish();
+  }
+  if (tid == 32) prefetch_tensormap(&tmap);
+  grid_launch_dependents();
+  grid_dependency_wait();
+
   // --- dealing: the item table of this CTA ---
   // Every CTA classifies every row: live without flush (0), live with flush (1)
   // or dead (2: padding, or an invalid slot or cursor).  Items (b, hv) form one
@@ -372,28 +402,6 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     const int lv = (NNF + NFL) * P.HV;  // live positions come first
     misc[4] = (int)blockIdx.x < lv ? (uint32_t)((lv - 1 - (int)blockIdx.x) / G + 1) : 0u;
   }
-  if (tid == 0) {
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(bars.bf(i), 1);
-      mbar_init(bars.be(i), 4);  // one arrival per epilogue warp
-    }
-    for (int i = 0; i < NL; ++i) mbar_init(bars.lf(i), 1);
-    for (int i = 0; i < NF; ++i) {
-      mbar_init(bars.inf(i), 1);
-      mbar_init(bars.ine(i), 4);
-    }
-    for (int i = 0; i < NT; ++i) mbar_init(bars.tle(i), 1);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(bars.tf(i), 1);
-      mbar_init(bars.te(i), 4);
-    }
-    misc[1] = 0u;
-    fence_mbar_init();
-  }
-  if (warp == 0) {
-    tmem_alloc(smem_addr(misc), 4 * D);
-    tmem_relinquish();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -406,7 +414,6 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensormap(&tmap);
       // Each epilogue group has its own NBg box slots (its items' boxes only),
       // so consecutive users of a slot are always the same group: a slot's
       // barrier can then never be waited on a lap ahead of its last phase.
@@ -927,7 +934,21 @@ static cudaError_t launch_tcp_t(const DecodeParams &P, const CUtensorMap &map, c
   auto kern = tcp_decode_kernel<D, GATE, KIND, RING_DT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.total);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kTcpThreads, lay.total, s>>>(P, map, lay);
+  // Programmatic stream serialisation: the kernel's set-up may start while the
+  // previous launch in the stream finishes; it reads no input before
+  // griddepcontrol.wait, which returns once that launch has completed.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTcpThreads);
+  cfg.dynamicSmemBytes = lay.total;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, P, map, lay);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
