@@ -9,8 +9,9 @@ uniformly over [0, L) so flush and append rows mix in every launch.  Every step
 reads 512 MiB of checkpoint (4x the 129 MB L2), so no L2 flush is needed.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       [--workload headline|qwen3next_layer|kda_layer|sweep:B:L:f16|f32] [--recon tensor|ffma]
+       [--workload headline|qwen3next_layer|kda_layer|stack30|sweep:B:L:f16|f32] [--recon tensor|ffma]
        [--kernel-only]   (timed decode loop only: for profiling and sweeps)
+       [--sweep [--sweep-batches 1,8,...] [--sweep-lens 1,4,...]]  (one JSON line per point)
 Under torchrun each rank runs an independent replica on its own GPU (the
 path has no exchange step); rank 0 prints one JSON line.
 """
@@ -284,10 +285,151 @@ def pick_workload(name):
         return I.with_(I.QWEN3NEXT_LAYER, staggered=True)
     if name == "kda_layer":
         return I.with_(I.KDA_LAYER, staggered=True)
+    if name == "stack30":
+        return I.with_(I.STACK30, staggered=True)
     if name.startswith("sweep:"):
         _, B, L, rd = name.split(":")
         return I.sweep_point(int(B), int(L), {"f16": F16, "f32": F32, "bf16": BF16}[rd])
     raise SystemExit(f"unknown workload {name}")
+
+
+def measure_replay(w, K, warmup, recon, dev, layers=1):
+    """Kernel-only timing of K steps of `layers` layers sharing one cursor array:
+    gdn_replayssm_decode on every layer but the last, gdn_replayssm_decode_advance
+    on the last.  Inputs are resident on the device; nothing else runs between
+    launches.  Returns per-launch and per-step figures with the algorithmic bytes."""
+    import numpy as np
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import inputs as I
+
+    gen = I.generator(w.seed, dev)
+    wp = I.write_pos(gen, w, dev)
+    caches = []
+    for _ in range(layers):
+        c = I.cache(gen, w, wp, dev)
+        caches.append(Bd.Cache(c.state, c.ring_d, c.ring_k, c.ring_g))
+    idx = I.indices(gen, w.B, w.N, w.n_pad, dev)
+    rows = idx.shape[0]
+    desc = Bd.layer_desc(w.N, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, ring_dtype=w.ring_dtype)
+    pool = [I.step_inputs(gen, w, dev) for _ in range(4)]
+    out = torch.empty((rows, w.HV, w.V), dtype=torch.bfloat16, device=dev)
+    steps_in = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out) for b in pool]
+    stream = torch.cuda.current_stream()
+    adv_ws = Bd.decode_advance_workspace(dev)
+    idx_h = idx.cpu().numpy()
+    wp_h = wp.cpu().numpy().copy()
+    ob = 2
+
+    def step(i):
+        si = steps_in[i % len(steps_in)]
+        for layer in range(layers - 1):
+            Bd.gdn_replayssm_decode(desc, caches[layer], wp, None, si, recon, None, None, stream)
+        Bd.gdn_replayssm_decode_advance(desc, caches[-1], wp, None, si, adv_ws, recon, None, None, stream)
+
+    def host_advance():
+        live = idx_h[idx_h >= 0]
+        p = wp_h[live]
+        wp_h[live] = np.where(p == w.L - 1, 0, p + 1)
+
+    for i in range(warmup):
+        step(i)
+        host_advance()
+    total = 0.0
+    for i in range(K):
+        live = idx_h[idx_h >= 0]
+        p = wp_h[live]
+        per_layer = launch_bytes(w, p, p == w.L - 1, ob, int((idx_h < 0).sum()), cursors=False)
+        total += layers * per_layer + 8 * len(live)
+        host_advance()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(K):
+        step(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(wp.cpu().numpy(), wp_h), "device cursors diverged from the advance rule"
+    step_s = a.elapsed_time(b) / 1e3 / K
+    launch_s = step_s / layers
+    peak, _ = measured_hbm_peak()
+    gbs = total / K / step_s / 1e9
+    return {"workload": w.name, "layers": layers, "B": w.B, "L": w.L,
+            "ring": {0: "f32", 1: "bf16", 2: "f16"}[w.ring_dtype], "steps": K,
+            "ms_per_step": step_s * 1e3, "ms_per_launch": launch_s * 1e3,
+            "head_steps_per_s_per_layer": w.B * w.HV / launch_s, "tokens_per_s_per_layer": w.B / launch_s,
+            "algorithmic_bytes_per_step": total / K, "hbm_gbs_algorithmic": gbs, "frac": gbs / peak,
+            "frac_of_8tbs": gbs / 8000.0}
+
+
+def measure_packed(w, K, dev):
+    """The in-repo packed decode (reads and writes the state every step) on the
+    workload's shapes: kernel-only, K launches back to back."""
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import inputs as I
+
+    gen = I.generator(w.seed + 7, dev)
+    st = I.state(gen, w.N, w.HV, w.V, w.K, dev)
+    idx = I.indices(gen, w.B, w.N, w.n_pad, dev)
+    rows = idx.shape[0]
+    desc = Bd.layer_desc(w.N, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, ring_dtype=w.ring_dtype)
+    si = I.step_inputs(gen, w, dev)
+    out = torch.empty((rows, w.HV, w.V), dtype=torch.bfloat16, device=dev)
+    step = Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out)
+    stream = torch.cuda.current_stream()
+    for _ in range(4):
+        Bd.gdn_packed_decode(desc, st, step, None, stream)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        Bd.gdn_packed_decode(desc, st, step, None, stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    s = a.elapsed_time(b) / 1e3 / K
+    nbytes = (w.B * w.HV * packed_head_step_bytes(w.K, w.V, w.HV // w.HK, 2, 2, w.gate == Bd.GATE_PER_K)
+              + (rows - w.B) * w.HV * w.V * 2)
+    peak, _ = measured_hbm_peak()
+    return {"ms_per_launch": s * 1e3, "head_steps_per_s": w.B * w.HV / s, "tokens_per_s": w.B / s,
+            "hbm_gbs_algorithmic": nbytes / s / 1e9, "frac": nbytes / s / 1e9 / peak}
+
+
+def run_sweep(args):
+    """Batch x ring-length x ring-dtype sweep of one GDN layer (HV=32, HK=16,
+    K=V=128, staggered cursors): one JSON line per point, the replay decode +
+    advance beside the packed decode on the same batch size."""
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import build as cuda_build
+    from linear_attention_decode_gb300 import inputs as I
+    from linear_attention_decode_gb300.constants import F16, F32
+
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cuda_build.build()
+    Bd.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    batches = [int(x) for x in args.sweep_batches.split(",")]
+    lens = [int(x) for x in args.sweep_lens.split(",")]
+    packed = {}
+    for B in batches:
+        for L in lens:
+            for ring in (F16, F32):
+                w = I.sweep_point(B, L, ring)
+                K = max(2 * L * 8, 128)
+                r = measure_replay(w, K, max(args.warmup, 2 * L), Bd.RECON_TENSOR, dev)
+                if B not in packed:
+                    packed[B] = measure_packed(w, 64, dev)
+                r["packed"] = packed[B]
+                r["replay_speedup_vs_packed"] = packed[B]["ms_per_launch"] / r["ms_per_launch"]
+                print(json.dumps(r), flush=True)
+                torch.cuda.empty_cache()
+    return 0
 
 
 def run_ours(args):
@@ -307,6 +449,16 @@ def run_ours(args):
     Bd.load_library()
     dev = torch.device("cuda", torch.cuda.current_device())
     w = pick_workload(args.workload)
+    if args.workload == "stack30":
+        # the 30-layer forward: 30 launches a step, the last one also advancing
+        if not args.kernel_only:
+            raise SystemExit("--workload stack30 is measured with --kernel-only")
+        r = measure_replay(w, args.steps, args.warmup, Bd.RECON_TENSOR, dev, layers=w.layers)
+        if rank == 0:
+            print(json.dumps(r))
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
     recon = Bd.RECON_FFMA if args.recon == "ffma" else Bd.RECON_TENSOR
     rb = 4 if w.ring_dtype == Bd.F32 else 2
     gen = I.generator(w.seed + rank, dev)
@@ -481,6 +633,10 @@ def main():
     ap.add_argument("--workload", default="headline")
     ap.add_argument("--recon", choices=["tensor", "ffma"], default="tensor")
     ap.add_argument("--kernel-only", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="batch x ring length x ring dtype sweep of one layer (one JSON line per point)")
+    ap.add_argument("--sweep-batches", default="1,8,64,128,256,512")
+    ap.add_argument("--sweep-lens", default="1,4,8,16,32")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--ref-budget", type=float, default=60.0,
@@ -490,6 +646,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 
