@@ -24,7 +24,7 @@ _SO = os.path.join(_HERE, "liboracle.so")
 
 F64, F32, F16, BF16 = 0, 1, 2, 3
 GATE_SCALAR, GATE_PER_K = 0, 1
-BAD_SLOT, BAD_WRITE_POS = 1, 2
+BAD_SLOT, BAD_WRITE_POS, BAD_ACCEPTED = 1, 2, 16
 
 
 def compile_source(src: str, out: str) -> str:
@@ -69,6 +69,10 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_replay_advance.argtypes = [ctypes.c_int, ctypes.c_int, ip, bp,
                                           ctypes.c_int, ip, up]
     lib.oracle_replay_fold.argtypes = [gp, dp, dp, dp, dp, ip, ctypes.c_int, ip, up]
+    lib.oracle_spec_verify.argtypes = [gp, dp, dp, dp, dp, ip, ctypes.c_int, ctypes.c_int, ip,
+                                       dp, dp, dp, ctypes.c_double, ctypes.c_int, dp, up]
+    lib.oracle_spec_commit.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ip, ip,
+                                       ip, ip, up]
     return lib
 
 
@@ -228,3 +232,32 @@ def replay_fold(G: Geom, cache: Cache, write_pos, slots) -> int:
     _lib().oracle_replay_fold(ctypes.byref(G), _d(cache.state), _d(cache.ring_d), _d(cache.ring_k),
                               _d(cache.ring_g), _i(wp), sl.shape[0], _i(sl), ctypes.byref(st))
     return st.value
+
+
+def spec_verify(G: Geom, cache: Cache, write_pos, indices, T: int, mixed_qkv, g, beta,
+                q_scale: float = 1.0, qk_l2norm: int = 0):
+    """Verify window of T tokens per row (token t of row b at row b*T + t of the
+    inputs); the ring gets the window's entries, checkpoint and cursors stay.
+    Returns (o [B*T, HV, V], status)."""
+    wp = np.ascontiguousarray(np.asarray(write_pos, dtype=np.int32))
+    idx = np.ascontiguousarray(np.asarray(indices, dtype=np.int32))
+    qkv, gg, bb = f64(mixed_qkv), f64(g), f64(beta)
+    B = idx.shape[0]
+    o = np.zeros((B * T, G.HV, G.V))
+    st = ctypes.c_uint(0)
+    _lib().oracle_spec_verify(ctypes.byref(G), _d(cache.state), _d(cache.ring_d), _d(cache.ring_k),
+                              _d(cache.ring_g), _i(wp), B, int(T), _i(idx), _d(qkv), _d(gg), _d(bb),
+                              float(q_scale), int(qk_l2norm), _d(o), ctypes.byref(st))
+    return o, st.value
+
+
+def spec_commit(N: int, L: int, T: int, indices, accepted, write_pos: np.ndarray):
+    """Move the cursors over the accepted tokens; write_pos (int32) updated in
+    place. Returns (flush_slots [B], status)."""
+    idx = np.ascontiguousarray(np.asarray(indices, dtype=np.int32))
+    acc = np.ascontiguousarray(np.asarray(accepted, dtype=np.int32))
+    fs = np.zeros(idx.shape[0], dtype=np.int32)
+    st = ctypes.c_uint(0)
+    _lib().oracle_spec_commit(N, L, int(T), idx.shape[0], _i(idx), _i(acc), _i(write_pos), _i(fs),
+                              ctypes.byref(st))
+    return fs, st.value

@@ -366,3 +366,73 @@ int oracle_replay_fold(const oracle_geom *G, double *state, const double *ring_d
     free(S);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Speculative-decode verify window and commit ([P3] "Core concept" and       */
+/* "Design notes"): one checkpoint plus the ring; a window of T tokens is     */
+/* decoded from the committed ring and the window's own earlier tokens, every */
+/* token's (d, k, g) goes into the ring after the committed entries, and a    */
+/* rejected draft is dropped by not moving the cursor over it.                */
+/* ------------------------------------------------------------------------- */
+
+/* Window decode of B rows x T tokens.  Token t of row b is row b*T + t of
+ * mixed_qkv / g / beta / o.  For a row with slot s and p = write_pos[s]
+ * (requires p + T <= L - 1, the ring's capacity outside a flush step), token t
+ * is exactly the non-flush decode of oracle_replay_decode at cursor p + t, so
+ * it sees the committed entries and the window's entries p .. p + t - 1; its
+ * (d, k, g) is written at ring position p + t.  Neither the checkpoint nor the
+ * cursor changes.  A row outside that range sets ORACLE_BAD_WRITE_POS and is
+ * treated as padding (zeros). */
+int oracle_spec_verify(const oracle_geom *G, double *state, double *ring_d, double *ring_k,
+                       double *ring_g, const int *write_pos, int B, int T, const int *indices,
+                       const double *mixed_qkv, const double *g, const double *beta,
+                       double q_scale, int qk_l2norm, double *o, unsigned *status)
+{
+    int HV = G->HV, V = G->V, K = G->K;
+    size_t gsz = G->gate == ORACLE_GATE_PER_K ? (size_t)HV * K : (size_t)HV;
+    int *cursor = malloc(sizeof(int) * (size_t)G->N);
+    for (int b = 0; b < B; b++) {
+        int slot = indices[b];
+        int ok = slot >= 0 && slot < G->N;
+        if (slot >= G->N) *status |= ORACLE_BAD_SLOT;
+        int p = ok ? write_pos[slot] : 0;
+        if (ok && (p < 0 || p + T > G->L - 1)) { *status |= ORACLE_BAD_WRITE_POS; ok = 0; }
+        for (int t = 0; t < T; t++) {
+            size_t row = (size_t)b * T + t;
+            if (!ok) {
+                for (size_t e = 0; e < (size_t)HV * V; e++) o[row * HV * V + e] = 0.0;
+                continue;
+            }
+            cursor[slot] = p + t;
+            int idx1 = slot;
+            oracle_replay_decode(G, state, ring_d, ring_k, ring_g, cursor, 1, &idx1, NULL,
+                                 mixed_qkv + row * row_len(G), g + row * gsz, beta + row * HV,
+                                 q_scale, qk_l2norm, o + row * HV * V, NULL, status);
+        }
+    }
+    free(cursor);
+    return 0;
+}
+
+/* Commit after verification: row b accepted accepted[b] of its T window
+ * tokens (0 <= a <= T).  The cursor moves over the accepted entries only, so
+ * the rejected drafts are rolled back by the move itself; when the next window
+ * would not fit (cursor + T > L - 1) flush_slots[b] = slot (fold that slot's
+ * ring into its checkpoint on every layer, then reset its cursor), else -1.
+ * Padding rows get -1. */
+int oracle_spec_commit(int N, int L, int T, int B, const int *indices, const int *accepted,
+                       int *write_pos, int *flush_slots, unsigned *status)
+{
+    for (int b = 0; b < B; b++) {
+        int slot = indices[b];
+        flush_slots[b] = -1;
+        if (slot < 0) continue;
+        if (slot >= N) { *status |= ORACLE_BAD_SLOT; continue; }
+        int p = write_pos[slot], a = accepted[b];
+        if (p < 0 || p + T > L - 1) { *status |= ORACLE_BAD_WRITE_POS; continue; }
+        if (a < 0 || a > T) { *status |= ORACLE_BAD_ACCEPTED; continue; }
+        write_pos[slot] = p + a;
+        if (p + a + T > L - 1) flush_slots[b] = slot;
+    }
+    return 0;
+}

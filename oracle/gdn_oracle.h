@@ -23,7 +23,7 @@ extern "C" {
 
 enum { ORACLE_F64 = 0, ORACLE_F32 = 1, ORACLE_F16 = 2, ORACLE_BF16 = 3 };
 enum { ORACLE_GATE_SCALAR = 0, ORACLE_GATE_PER_K = 1 };
-enum { ORACLE_BAD_SLOT = 1u, ORACLE_BAD_WRITE_POS = 2u };
+enum { ORACLE_BAD_SLOT = 1u, ORACLE_BAD_WRITE_POS = 2u, ORACLE_BAD_ACCEPTED = 16u };
 
 typedef struct {
     int N, HV, HK, K, V, L;
@@ -60,6 +60,16 @@ int oracle_replay_advance(int N, int B, const int *indices, const unsigned char 
 int oracle_replay_fold(const oracle_geom *G, double *state, const double *ring_d,
                        const double *ring_k, const double *ring_g, const int *write_pos,
                        int n, const int *slots, unsigned *status);
+
+/* Speculative verify window (B rows x T tokens, token t of row b at row b*T+t)
+ * and the commit that moves the cursors over the accepted tokens. */
+int oracle_spec_verify(const oracle_geom *G, double *state, double *ring_d, double *ring_k,
+                       double *ring_g, const int *write_pos, int B, int T, const int *indices,
+                       const double *mixed_qkv, const double *g, const double *beta,
+                       double q_scale, int qk_l2norm, double *o, unsigned *status);
+
+int oracle_spec_commit(int N, int L, int T, int B, const int *indices, const int *accepted,
+                       int *write_pos, int *flush_slots, unsigned *status);
 
 #ifdef __cplusplus
 }

@@ -476,4 +476,95 @@ def pin_q_scale_is_linear_and_l2norm_scale_free():
     assert np.max(np.abs(a - base)) > 1e-3  # the norm does change un-normalised inputs
 
 
+# ---------------------------------------------------------------------------
+# Speculative verify window and commit (vLLM #49887 "ReplaySSM: cache SSM
+# inputs for faster Gated DeltaNet speculative decode": Core concept, Design
+# notes).  Checked against the sequential recurrence run from the committed
+# state: every window token's output, every cached correction, the cursor move
+# and the fold that follows.
+# ---------------------------------------------------------------------------
+
+def _spec_matches_recurrence(gate):
+    HV, HK, K, V, L, T, windows = 4, 2, K5, V3, 9, 3, 12
+    N, slot = 2, 1
+    G = O.geom(N, HV, HK, K, V, L, gate=gate, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(200 + gate)
+    S0 = r.standard_normal((HV, V, K)) * 0.3
+    gk = (K,) if gate else ()
+    cache = O.Cache(np.zeros((N, HV, V, K)), np.full((N, HV, L, V), np.nan),
+                    np.full((N, HK, L, K), np.nan), np.full((N, HV, L) + gk, np.nan))
+    cache.state[slot] = S0
+    wp = np.zeros(N, dtype=np.int32)
+    S_ref = [S0[h].copy() for h in range(HV)]  # the committed state, by the recurrence
+    flushes = 0
+    for w in range(windows):
+        seq = _Seq(300 + 10 * gate + w, T, HV, HK, K, V, gate)
+        p = int(wp[slot])
+        rows = np.concatenate([seq.row(t) for t in range(T)])
+        o, st = O.spec_verify(G, cache, wp, [slot], T, rows, seq.g, seq.beta)
+        assert st == 0 and int(wp[slot]) == p, "verify moved the cursor"
+        # reference: the window decoded one token at a time from the committed state
+        S_win = [S_ref[h].copy() for h in range(HV)]
+        for t in range(T):
+            for h in range(HV):
+                hk = h // (HV // HK)
+                fn = O.kda_step if gate else O.gdn_step
+                y, u = fn(S_win[h], seq.q[t][hk], seq.k[t][hk], seq.v[t][h], seq.g[t][h], seq.beta[t][h])
+                _close(o[t, h], y, 1e-12, f"window {w} token {t} head {h} output")
+                _close(cache.ring_d[slot, h, p + t], u, 1e-12, f"window {w} token {t} cached correction")
+        accepted = int(r.integers(0, T + 1))
+        fs, st = O.spec_commit(N, L, T, [slot], [accepted], wp)
+        assert st == 0 and int(wp[slot]) == p + accepted
+        assert int(fs[0]) == (slot if p + accepted + T > L - 1 else -1)
+        # the committed state moves over the accepted tokens only
+        S_acc = [S_ref[h].copy() for h in range(HV)]
+        for t in range(accepted):
+            for h in range(HV):
+                hk = h // (HV // HK)
+                fn = O.kda_step if gate else O.gdn_step
+                fn(S_acc[h], seq.q[t][hk], seq.k[t][hk], seq.v[t][h], seq.g[t][h], seq.beta[t][h])
+        S_ref = S_acc
+        for h in range(HV):
+            _close(O.replay_state(G, cache, slot, h, int(wp[slot])), S_ref[h], 1e-12,
+                   f"window {w}: committed state rebuilt from checkpoint + ring")
+        if fs[0] >= 0:  # the fold the commit asked for, then the cursor reset
+            assert O.replay_fold(G, cache, wp, fs) == 0
+            wp[slot] = 0
+            flushes += 1
+            for h in range(HV):
+                _close(cache.state[slot, h], S_ref[h], 1e-12, f"window {w}: folded checkpoint")
+    assert flushes >= 2, "the sequence should cross several folds"
+    assert np.all(cache.state[0] == 0.0) and np.all(np.isnan(cache.ring_d[0])), "slot 0 was touched"
+
+
+def pin_spec_window_is_the_recurrence_gdn():
+    _spec_matches_recurrence(O.GATE_SCALAR)
+
+
+def pin_spec_window_is_the_recurrence_kda():
+    _spec_matches_recurrence(O.GATE_PER_K)
+
+
+def pin_spec_bad_rows():
+    """Padding rows give zeros and touch nothing; a window that does not fit
+    the ring (p + T > L - 1), a slot past the pool and an accepted count outside
+    [0, T] are reported and touch nothing."""
+    HV, HK, K, V, L, T = 2, 1, 4, 3, 6, 3
+    N = 3
+    G = O.geom(N, HV, HK, K, V, L, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(400)
+    cache = O.Cache(r.standard_normal((N, HV, V, K)), np.full((N, HV, L, V), np.nan),
+                    np.full((N, HK, L, K), np.nan), np.full((N, HV, L), np.nan))
+    before = cache.copy()
+    seq = _Seq(401, T, HV, HK, K, V, 0)
+    rows = np.concatenate([seq.row(t) for t in range(T)])
+    wp = np.array([0, 3, 0], dtype=np.int32)  # slot 1: 3 + 3 > 5
+    for idx, want in (([-1], 0), ([7], O.BAD_SLOT), ([1], O.BAD_WRITE_POS)):
+        o, st = O.spec_verify(G, cache, wp, idx, T, rows, seq.g, seq.beta)
+        assert st == want and np.all(o == 0.0), f"rows {idx}"
+    assert np.array_equal(cache.state, before.state) and np.all(np.isnan(cache.ring_d))
+    fs, st = O.spec_commit(N, L, T, [0, -1, 2], [T + 1, 1, -1], wp)
+    assert st == O.BAD_ACCEPTED and list(fs) == [-1, -1, -1] and list(wp) == [0, 3, 0]
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

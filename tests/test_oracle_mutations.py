@@ -68,6 +68,18 @@ MUTATIONS = [
     ("f16_mantissa_width",
      "case ORACLE_F16:  return round_binary(x, 10, -14, 15);",
      "case ORACLE_F16:  return round_binary(x, 11, -14, 15);"),
+    ("spec_window_ignores_own_tokens",
+     "cursor[slot] = p + t;",
+     "cursor[slot] = p;"),
+    ("spec_commit_moves_over_rejected",
+     "write_pos[slot] = p + a;",
+     "write_pos[slot] = p + T;"),
+    ("spec_fold_rule_one_late",
+     "if (p + a + T > L - 1) flush_slots[b] = slot;",
+     "if (p + a + T > L) flush_slots[b] = slot;"),
+    ("spec_capacity_one_more",
+     "if (ok && (p < 0 || p + T > G->L - 1)) { *status |= ORACLE_BAD_WRITE_POS; ok = 0; }",
+     "if (ok && (p < 0 || p + T > G->L)) { *status |= ORACLE_BAD_WRITE_POS; ok = 0; }"),
 ]
 
 
