@@ -83,6 +83,7 @@ typedef enum { GDN_RECON_TENSOR = 0, GDN_RECON_FFMA = 1 } gdn_recon_t;
 #define GDN_DEV_BAD_WRITE_POS 2u /* write_pos[slot] outside [0, ring_len)           */
 #define GDN_DEV_TIMEOUT       4u /* an on-chip wait gave up (row output is garbage) */
 #define GDN_DEV_INTERNAL      8u /* shared memory not aligned as the kernel assumes  */
+#define GDN_DEV_BAD_ACCEPTED 16u /* a spec commit's accepted count outside [0, window] */
 
 /* One layer's geometry.  Built: k_dim == v_dim in {64, 128}; 1 <= ring_len <= 64;
  * state_dtype GDN_F32; ring_dtype GDN_F32, GDN_F16 or GDN_BF16. */
@@ -212,6 +213,48 @@ GDN_API gdn_status_t gdn_replayssm_flush(const gdn_layer_desc_t *desc, const gdn
  * copy-on-write, [P1] Design 3 and 5).  Negative entries are skipped. */
 GDN_API gdn_status_t gdn_replayssm_reset_slots(int32_t *write_pos, int32_t num_slots,
                                        const int32_t *slots, int32_t n,
+                                       uint32_t *dev_status, gdn_stream_t stream);
+
+/* One speculative verify step: B rows of T tokens each; token t of row b is
+ * input / output row b*T + t ([P3] Core concept).  Device pointers. */
+typedef struct {
+    const void *mixed_qkv;            /* [B*T, row] in qkv_dtype (row layout as gdn_step_t) */
+    int32_t qkv_dtype;                /* gdn_dtype_t                                         */
+    int64_t qkv_row_stride;           /* elements between token rows                         */
+    const float *g;                   /* [B*T, HV] (GDN) or [B*T, HV, K] (KDA)               */
+    const float *beta;                /* [B*T, HV]                                           */
+    const int32_t *ssm_state_indices; /* [B] row -> slot; negative = padding row             */
+    int32_t batch;                    /* B >= 0                                              */
+    int32_t window;                   /* T, 1 <= T <= min(ring_len - 1, 32)                   */
+    float q_scale;                    /* as in gdn_step_t                                    */
+    int32_t qk_l2norm;                /* as in gdn_step_t                                    */
+    void *out;                        /* [B*T, HV, V] in out_dtype                           */
+    int32_t out_dtype;                /* gdn_dtype_t                                         */
+} gdn_spec_step_t;
+
+/* Speculative verify window of one layer ([P3] Core concept, Design notes).
+ * Row b with slot s and p = write_pos[s] (requires p + T <= L - 1) decodes its
+ * T tokens from the checkpoint and the committed entries j < p: token t is the
+ * non-flush decode at cursor p + t, seeing the window's earlier tokens as
+ * cached entries; its output goes to out row b*T + t and its (d, k, g) to ring
+ * position p + t (k once per key head).  The checkpoint and write_pos are not
+ * changed: after the target model has accepted a tokens, call
+ * gdn_replayssm_spec_commit.  A row whose window does not fit sets
+ * GDN_DEV_BAD_WRITE_POS and is treated as padding (zeros).  Replay on the CUDA
+ * cores in fp32. */
+GDN_API gdn_status_t gdn_replayssm_spec_verify(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
+                                       const int32_t *write_pos, const gdn_spec_step_t *step,
+                                       uint32_t *dev_status, gdn_stream_t stream);
+
+/* Commit after a verify window, once per forward ([P3] "rollback is a cursor
+ * move"): write_pos[s] += accepted[b] (0 <= accepted[b] <= window); rejected
+ * drafts stay in the ring past the cursor and are never read.  flush_slots[b]
+ * ([B] int32) receives s when the next window would not fit
+ * (write_pos[s] + window > L - 1), else -1: pass it to gdn_replayssm_flush for
+ * every layer and then to gdn_replayssm_reset_slots.  Padding rows get -1. */
+GDN_API gdn_status_t gdn_replayssm_spec_commit(const int32_t *ssm_state_indices, const int32_t *accepted,
+                                       int32_t batch, int32_t window, int32_t num_slots,
+                                       int32_t ring_len, int32_t *write_pos, int32_t *flush_slots,
                                        uint32_t *dev_status, gdn_stream_t stream);
 
 /* Static text for a status code (host). */

@@ -19,7 +19,7 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdnreplay.so")
 
-from .constants import (BF16, DEV_BAD_SLOT, DEV_BAD_WRITE_POS, DEV_INTERNAL, DEV_TIMEOUT,  # noqa: F401
+from .constants import (BF16, DEV_BAD_ACCEPTED, DEV_BAD_SLOT, DEV_BAD_WRITE_POS, DEV_INTERNAL, DEV_TIMEOUT,  # noqa: F401
                         F16, F32, GATE_PER_K, GATE_SCALAR, GDN_DTYPE, RECON_FFMA, RECON_TENSOR,
                         TORCH_DTYPE)
 
@@ -39,6 +39,15 @@ class LayerDesc(ctypes.Structure):
 class _Cache(ctypes.Structure):
     _fields_ = [("state", ctypes.c_void_p), ("ring_d", ctypes.c_void_p),
                 ("ring_k", ctypes.c_void_p), ("ring_g", ctypes.c_void_p)]
+
+
+class _SpecStep(ctypes.Structure):
+    _fields_ = [("mixed_qkv", ctypes.c_void_p), ("qkv_dtype", ctypes.c_int32),
+                ("qkv_row_stride", ctypes.c_int64), ("g", ctypes.c_void_p),
+                ("beta", ctypes.c_void_p), ("ssm_state_indices", ctypes.c_void_p),
+                ("batch", ctypes.c_int32), ("window", ctypes.c_int32), ("q_scale", ctypes.c_float),
+                ("qk_l2norm", ctypes.c_int32), ("out", ctypes.c_void_p),
+                ("out_dtype", ctypes.c_int32)]
 
 
 class _Step(ctypes.Structure):
@@ -95,11 +104,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_replayssm_decode_advance.argtypes = [dp, cp, vp, vp, sp, i32, vp, vp, u32p, vp]
         lib.gdn_replayssm_decode_advance_noalloc.argtypes = [dp, cp, vp, vp, sp, i32, vp, u32p, vp]
         lib.gdn_replayssm_advance.argtypes = [vp, i32, vp, i32, i32, vp, u32p, vp]
+        lib.gdn_replayssm_spec_verify.argtypes = [dp, cp, vp, ctypes.POINTER(_SpecStep), u32p, vp]
+        lib.gdn_replayssm_spec_commit.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, u32p, vp]
         lib.gdn_replayssm_flush.argtypes = [dp, cp, vp, vp, i32, u32p, vp]
         lib.gdn_replayssm_reset_slots.argtypes = [vp, i32, vp, i32, u32p, vp]
         for f in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_decode_advance",
                   "gdn_replayssm_decode_advance_noalloc", "gdn_replayssm_advance", "gdn_replayssm_flush",
-                  "gdn_replayssm_reset_slots"):
+                  "gdn_replayssm_reset_slots", "gdn_replayssm_spec_verify", "gdn_replayssm_spec_commit"):
             getattr(lib, f).restype = ctypes.c_int
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
@@ -239,6 +250,44 @@ def gdn_replayssm_decode_advance_noalloc(desc: LayerDesc, cache: Cache, write_po
         ctypes.byref(s), int(recon),
         _dev(flushed_out, "flushed_out", (B,), torch.uint8, optional=True),
         _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_decode_advance_noalloc")
+
+
+def gdn_replayssm_spec_verify(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor, window: int,
+                              step: Step, dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Speculative verify window: `step` holds B*T token rows (token t of row b
+    at row b*T + t) and ssm_state_indices [B]; out is [B*T, HV, V]."""
+    T = int(window)
+    B = step.ssm_state_indices.shape[0]
+    HV, HK, K, V = desc.num_v_heads, desc.num_k_heads, desc.k_dim, desc.v_dim
+    q = step.mixed_qkv
+    if not q.is_cuda or q.dim() != 2 or q.shape[0] != B * T or q.stride(1) != 1:
+        raise GdnError("mixed_qkv must be a CUDA [B*T, row] tensor with unit inner stride")
+    if q.shape[1] < 2 * HK * K + HV * V:
+        raise GdnError("mixed_qkv rows are shorter than 2*HK*K + HV*V")
+    if q.dtype not in GDN_DTYPE or step.out.dtype not in GDN_DTYPE:
+        raise GdnError("mixed_qkv and out must be fp32, bf16 or fp16")
+    gshape = (B * T, HV, K) if desc.gate == GATE_PER_K else (B * T, HV)
+    s = _SpecStep(q.data_ptr() if B else None, GDN_DTYPE[q.dtype], q.stride(0) if B * T > 1 else q.shape[1],
+                  _dev(step.g, "g", gshape, torch.float32), _dev(step.beta, "beta", (B * T, HV), torch.float32),
+                  _dev(step.ssm_state_indices, "ssm_state_indices", (B,), torch.int32), B, T,
+                  float(step.q_scale), int(bool(step.qk_l2norm)),
+                  _dev(step.out, "out", (B * T, HV, V)), GDN_DTYPE[step.out.dtype])
+    c = _pack_cache(desc, cache)
+    _check(load_library().gdn_replayssm_spec_verify(
+        ctypes.byref(desc), ctypes.byref(c), _dev(write_pos, "write_pos", (desc.num_slots,), torch.int32),
+        ctypes.byref(s), _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_spec_verify")
+
+
+def gdn_replayssm_spec_commit(ssm_state_indices: torch.Tensor, accepted: torch.Tensor, window: int,
+                              num_slots: int, ring_len: int, write_pos: torch.Tensor, flush_slots: torch.Tensor,
+                              dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    B = ssm_state_indices.shape[0]
+    _check(load_library().gdn_replayssm_spec_commit(
+        _dev(ssm_state_indices, "ssm_state_indices", (B,), torch.int32),
+        _dev(accepted, "accepted", (B,), torch.int32), B, int(window), int(num_slots), int(ring_len),
+        _dev(write_pos, "write_pos", (num_slots,), torch.int32),
+        _dev(flush_slots, "flush_slots", (B,), torch.int32), _status_ptr(dev_status), _stream(stream)),
+        "gdn_replayssm_spec_commit")
 
 
 def gdn_replayssm_advance(ssm_state_indices: torch.Tensor, force_flush: Optional[torch.Tensor],

@@ -212,6 +212,65 @@ gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, const gd
   return GDN_OK;
 }
 
+gdn_status_t gdn_replayssm_spec_verify(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
+                                       const int32_t *write_pos, const gdn_spec_step_t *step,
+                                       uint32_t *dev_status, gdn_stream_t stream) {
+  gdn_status_t st = check_desc(desc);
+  if (st != GDN_OK) return st;
+  if ((st = check_cache(desc, cache)) != GDN_OK) return st;
+  if (!step) return fail(GDN_ERR_INVALID_ARG, "step is NULL");
+  if (!write_pos) return fail(GDN_ERR_INVALID_ARG, "write_pos is NULL");
+  if (step->batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch must be >= 0");
+  if (step->window < 1 || step->window > desc->ring_len - 1)
+    return fail(GDN_ERR_INVALID_ARG, "window must be in [1, ring_len - 1]");
+  if (step->window > 32) return fail(GDN_ERR_UNSUPPORTED, "built for window <= 32");
+  if (step->batch == 0) return GDN_OK;
+  if (!step->mixed_qkv || !step->g || !step->beta || !step->ssm_state_indices || !step->out)
+    return fail(GDN_ERR_INVALID_ARG, "step has a NULL input or output pointer");
+  if (!dtype_ok(step->qkv_dtype) || !dtype_ok(step->out_dtype))
+    return fail(GDN_ERR_INVALID_ARG, "unknown qkv or out dtype");
+  const int64_t row = 2 * (int64_t)desc->num_k_heads * desc->k_dim + (int64_t)desc->num_v_heads * desc->v_dim;
+  if (step->qkv_row_stride < row) return fail(GDN_ERR_INVALID_ARG, "qkv_row_stride is shorter than 2*HK*K + HV*V");
+  if ((int64_t)step->batch * step->window * desc->num_v_heads >= (int64_t)1 << 31)
+    return fail(GDN_ERR_UNSUPPORTED, "batch * window * num_v_heads must be < 2^31");
+  gdn::DecodeParams P = base_params(desc);
+  P.qkv = step->mixed_qkv;
+  P.qkv_dtype = step->qkv_dtype;
+  P.qkv_stride = step->qkv_row_stride;
+  P.g = step->g;
+  P.beta = step->beta;
+  P.idx = step->ssm_state_indices;
+  P.B = step->batch;
+  P.T = step->window;
+  P.q_scale = step->q_scale;
+  P.qk_l2norm = step->qk_l2norm;
+  P.out = step->out;
+  P.out_dtype = step->out_dtype;
+  P.state = cache->state;
+  P.ring_d = cache->ring_d;
+  P.ring_k = cache->ring_k;
+  P.ring_g = cache->ring_g;
+  P.write_pos = write_pos;
+  P.status = dev_status;
+  cudaError_t e = gdn::launch_spec_verify(P, desc->k_dim, desc->gate, (cudaStream_t)stream);
+  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_replayssm_spec_verify launch");
+}
+
+gdn_status_t gdn_replayssm_spec_commit(const int32_t *ssm_state_indices, const int32_t *accepted,
+                                       int32_t batch, int32_t window, int32_t num_slots,
+                                       int32_t ring_len, int32_t *write_pos, int32_t *flush_slots,
+                                       uint32_t *dev_status, gdn_stream_t stream) {
+  if (batch < 0 || num_slots <= 0 || ring_len <= 1 || window < 1 || window > ring_len - 1)
+    return fail(GDN_ERR_INVALID_ARG,
+                "batch >= 0, num_slots > 0, ring_len > 1 and 1 <= window <= ring_len - 1 are required");
+  if (batch == 0) return GDN_OK;
+  if (!ssm_state_indices || !accepted || !write_pos || !flush_slots)
+    return fail(GDN_ERR_INVALID_ARG, "ssm_state_indices, accepted, write_pos and flush_slots must be set");
+  cudaError_t e = gdn::launch_spec_commit(ssm_state_indices, accepted, batch, window, num_slots, ring_len,
+                                          write_pos, flush_slots, dev_status, (cudaStream_t)stream);
+  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_replayssm_spec_commit launch");
+}
+
 gdn_status_t gdn_replayssm_advance(const int32_t *ssm_state_indices, int32_t batch,
                                    const uint8_t *force_flush, int32_t num_slots, int32_t ring_len,
                                    int32_t *write_pos, uint32_t *dev_status, gdn_stream_t stream) {

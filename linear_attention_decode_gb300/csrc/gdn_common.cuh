@@ -45,6 +45,7 @@ struct DecodeParams {
   // cursors the last CTA to finish advances; both null otherwise
   uint32_t *sync;
   int32_t *write_pos_w;
+  int T;  // speculative verify: tokens per row (token t of row b is input row b * T + t)
 };
 
 __device__ __forceinline__ float load_as_f32(const void *p, int64_t i, int dtype) {

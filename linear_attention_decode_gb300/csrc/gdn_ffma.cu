@@ -249,6 +249,198 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const DecodeParams P) {
   }
 }
 
+// Speculative verify window ([P3] Core concept, Design notes): row b's T
+// tokens are decoded from the checkpoint and the first p = write_pos[slot]
+// ring entries, token t as the non-flush decode at cursor p + t would decode
+// it: its output uses the exact correction d_t, and the state carried to token
+// t + 1 takes d_t and k_t as they are cached at ring position p + t (rounded
+// to the ring type), as a committed entry would be replayed.  Needs
+// p + T <= L - 1; neither the checkpoint nor the cursor changes.  The state row
+// recurrence is row-separable, so each state row is rebuilt once and carried
+// through the window in registers.
+template <int D, int GATE>
+__global__ void __launch_bounds__(kThreads) spec_verify_kernel(const DecodeParams P) {
+  constexpr int M = D / 32;
+  constexpr int ROWS_PER_WARP = D / 4;
+  const int b = blockIdx.x / P.HV, hv = blockIdx.x % P.HV;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int rg = lane >> 3, cg = lane & 7;
+  const int T = P.T;
+  extern __shared__ float4 smem_f4[];
+  // window vectors: q (a o q for KDA), k, v, a (KDA), k rounded to the ring type; scalars
+  float *wq = reinterpret_cast<float *>(smem_f4);
+  float *wk = wq + T * D, *wv_ = wk + T * D, *wa = wv_ + T * D, *wkr = wa + T * D;
+  float *wsc = wkr + T * D;  // [T][4]: alpha, beta, k.q
+  float *Acol = wsc + 4 * T, *red = Acol + D, *wv = red + 8, *Dw = wv + 64;
+  float *Kr = Dw + (P.L - 1) * D;
+  float *q = Kr + (P.L - 1) * D, *k = q + D, *v = k + D;  // scratch for one token's inputs
+
+  int slot = P.idx[b];
+  bool live = slot >= 0;
+  int p = 0;
+  if (slot >= P.N) {
+    if (hv == 0 && t == 0) set_status(P.status, GDN_DEV_BAD_SLOT);
+    live = false;
+  } else if (live) {
+    p = P.write_pos[slot];
+    if (p < 0 || p + T > P.L - 1) {
+      if (hv == 0 && t == 0) set_status(P.status, GDN_DEV_BAD_WRITE_POS);
+      live = false;
+    }
+  }
+  if (!live) {  // padding row: zeros for every window token, no cache access
+    for (int tok = 0; tok < T; ++tok)
+      if (t < D) store_from_f32(P.out, (((int64_t)b * T + tok) * P.HV + hv) * D + t, P.out_dtype, 0.f);
+    return;
+  }
+
+  // Window inputs, token by token (load_qkv reduces over the CTA).
+  for (int tok = 0; tok < T; ++tok) {
+    const int row = b * T + tok;
+    const int64_t bh = (int64_t)row * P.HV + hv;
+    const float kq = load_qkv<D>(P, row, hv, q, k, v, red);
+    if (t < D) {
+      float a = 1.f;
+      if (GATE == GDN_GATE_PER_K) a = expf(P.g[bh * D + t]);
+      wq[tok * D + t] = GATE == GDN_GATE_PER_K ? a * q[t] : q[t];
+      wk[tok * D + t] = k[t];
+      wv_[tok * D + t] = v[t];
+      wa[tok * D + t] = a;
+      // the key as the ring caches it (and as a later token replays it)
+      float kr = k[t];
+      if (P.ring_dtype == GDN_F16) kr = __half2float(__float2half_rn(kr));
+      else if (P.ring_dtype == GDN_BF16) kr = __bfloat162float(__float2bfloat16_rn(kr));
+      wkr[tok * D + t] = kr;
+    }
+    if (t == 0) {
+      wsc[4 * tok + 0] = GATE == GDN_GATE_SCALAR ? expf(P.g[bh]) : 1.f;
+      wsc[4 * tok + 1] = P.beta[bh];
+      wsc[4 * tok + 2] = kq;
+    }
+    __syncthreads();
+  }
+  if (GATE == GDN_GATE_PER_K && t < D) Acol[t] = 1.f;
+  const float A = stage_replay<D, GATE>(P, slot, hv, p, wv, Acol, Dw, Kr);
+  float4 A4[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m)
+    A4[m] = GATE == GDN_GATE_PER_K ? reinterpret_cast<const float4 *>(Acol)[8 * m + cg]
+                                   : make_float4(A, A, A, A);
+
+  const float4 *S = reinterpret_cast<const float4 *>(P.state + ((int64_t)slot * P.HV + hv) * D * D);
+  for (int it = 0; it < ROWS_PER_WARP / 4; ++it) {
+    const int r = warp * ROWS_PER_WARP + it * 4 + rg;
+    // row r of the state before the window
+    float4 s[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const float4 c = S[r * (D / 4) + 8 * m + cg];
+      s[m] = make_float4(A4[m].x * c.x, A4[m].y * c.y, A4[m].z * c.z, A4[m].w * c.w);
+    }
+    for (int j = 0; j < p; ++j) {
+      const float dw = Dw[j * D + r];
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const float4 kr = reinterpret_cast<const float4 *>(Kr + j * D)[8 * m + cg];
+        s[m].x = fmaf(dw, kr.x, s[m].x);
+        s[m].y = fmaf(dw, kr.y, s[m].y);
+        s[m].z = fmaf(dw, kr.z, s[m].z);
+        s[m].w = fmaf(dw, kr.w, s[m].w);
+      }
+    }
+    // the window, token by token
+    for (int tok = 0; tok < T; ++tok) {
+      const float alpha = wsc[4 * tok], beta = wsc[4 * tok + 1], kq = wsc[4 * tok + 2];
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const int c4 = 8 * m + cg;
+        const float4 q4 = reinterpret_cast<const float4 *>(wq + tok * D)[c4];
+        float4 k4 = reinterpret_cast<const float4 *>(wk + tok * D)[c4];
+        if (GATE == GDN_GATE_PER_K) {
+          const float4 a4 = reinterpret_cast<const float4 *>(wa + tok * D)[c4];
+          k4 = make_float4(a4.x * k4.x, a4.y * k4.y, a4.z * k4.z, a4.w * k4.w);
+        }
+        sq = dot4(s[m], q4, sq);
+        sk = dot4(s[m], k4, sk);
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      }
+      if (GATE == GDN_GATE_SCALAR) {
+        sq *= alpha;
+        sk *= alpha;
+      }
+      const float d = beta * (wv_[tok * D + r] - sk);
+      const int64_t orow = ((int64_t)b * T + tok) * P.HV + hv;
+      if (cg == 0) {
+        store_from_f32(P.out, orow * D + r, P.out_dtype, fmaf(d, kq, sq));
+        store_from_f32(P.ring_d, (((int64_t)slot * P.HV + hv) * P.L + p + tok) * D + r, P.ring_dtype, d);
+      }
+      // carry row r to the next token with (d, k) as cached
+      float dr = d;
+      if (P.ring_dtype == GDN_F16) dr = __half2float(__float2half_rn(dr));
+      else if (P.ring_dtype == GDN_BF16) dr = __bfloat162float(__float2bfloat16_rn(dr));
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const int c4 = 8 * m + cg;
+        const float4 kr = reinterpret_cast<const float4 *>(wkr + tok * D)[c4];
+        if (GATE == GDN_GATE_SCALAR) {
+          s[m] = make_float4(fmaf(dr, kr.x, alpha * s[m].x), fmaf(dr, kr.y, alpha * s[m].y),
+                             fmaf(dr, kr.z, alpha * s[m].z), fmaf(dr, kr.w, alpha * s[m].w));
+        } else {
+          const float4 a4 = reinterpret_cast<const float4 *>(wa + tok * D)[c4];
+          s[m] = make_float4(fmaf(dr, kr.x, s[m].x * a4.x), fmaf(dr, kr.y, s[m].y * a4.y),
+                             fmaf(dr, kr.z, s[m].z * a4.z), fmaf(dr, kr.w, s[m].w * a4.w));
+        }
+      }
+    }
+  }
+  // k (one writer per key head) and g of every window token
+  const int hk = hv / P.G;
+  for (int tok = 0; tok < T; ++tok) {
+    const int64_t bh = ((int64_t)b * T + tok) * P.HV + hv;
+    const int64_t pos = p + tok;
+    if (GATE == GDN_GATE_SCALAR) {
+      if (t == 0) P.ring_g[((int64_t)slot * P.HV + hv) * P.L + pos] = P.g[bh];
+    } else if (t < D) {
+      P.ring_g[(((int64_t)slot * P.HV + hv) * P.L + pos) * D + t] = P.g[bh * D + t];
+    }
+    if (hv % P.G == 0 && t < D)
+      store_from_f32(P.ring_k, (((int64_t)slot * P.HK + hk) * P.L + pos) * D + t, P.ring_dtype,
+                     wk[tok * D + t]);
+  }
+}
+
+// Commit after verification ([P3] "rollback is a cursor move"): the cursor
+// moves over the accepted tokens only; a slot whose next window would not fit
+// (p + a + T > L - 1) is listed in flush_slots (else -1) for a fold.
+__global__ void spec_commit_kernel(const int32_t *idx, const int32_t *accepted, int B, int T, int N, int L,
+                                   int32_t *write_pos, int32_t *flush_slots, uint32_t *status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  flush_slots[b] = -1;
+  const int slot = idx[b];
+  if (slot < 0) return;
+  if (slot >= N) {
+    set_status(status, GDN_DEV_BAD_SLOT);
+    return;
+  }
+  const int p = write_pos[slot], a = accepted[b];
+  if (p < 0 || p + T > L - 1) {
+    set_status(status, GDN_DEV_BAD_WRITE_POS);
+    return;
+  }
+  if (a < 0 || a > T) {
+    set_status(status, GDN_DEV_BAD_ACCEPTED);
+    return;
+  }
+  write_pos[slot] = p + a;
+  if (p + a + T > L - 1) flush_slots[b] = slot;
+}
+
 __global__ void advance_kernel(const int32_t *idx, int B, const uint8_t *ff, int N, int L,
                                int32_t *write_pos, uint32_t *status) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -329,6 +521,30 @@ cudaError_t launch_fold(const DecodeParams &P, int D, int gate, int n, cudaStrea
   if (D == 128)
     return gate == GDN_GATE_SCALAR ? launch_fold_t<128, 0>(P, n, s) : launch_fold_t<128, 1>(P, n, s);
   return gate == GDN_GATE_SCALAR ? launch_fold_t<64, 0>(P, n, s) : launch_fold_t<64, 1>(P, n, s);
+}
+
+template <int D, int GATE>
+static cudaError_t launch_spec_t(const DecodeParams &P, cudaStream_t s) {
+  const size_t smem = (5 * (size_t)P.T * D + 4 * (size_t)P.T + 4 * (size_t)D + 8 + 64 +
+                       2 * (size_t)(P.L - 1) * D) * sizeof(float);
+  auto kern = spec_verify_kernel<D, GATE>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)P.B * P.HV, kThreads, smem, s>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_spec_verify(const DecodeParams &P, int D, int gate, cudaStream_t s) {
+  if (D == 128) return gate == GDN_GATE_SCALAR ? launch_spec_t<128, 0>(P, s) : launch_spec_t<128, 1>(P, s);
+  return gate == GDN_GATE_SCALAR ? launch_spec_t<64, 0>(P, s) : launch_spec_t<64, 1>(P, s);
+}
+
+cudaError_t launch_spec_commit(const int32_t *idx, const int32_t *accepted, int B, int T, int N, int L,
+                               int32_t *write_pos, int32_t *flush_slots, uint32_t *status, cudaStream_t s) {
+  spec_commit_kernel<<<(B + 255) / 256, 256, 0, s>>>(idx, accepted, B, T, N, L, write_pos, flush_slots, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_advance(const int32_t *idx, int B, const uint8_t *ff, int N, int L,

@@ -25,6 +25,11 @@ cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUte
 
 cudaError_t launch_fold(const DecodeParams &P, int D, int gate, int n, cudaStream_t s);
 
+// Speculative verify window (P.T tokens per row) and the commit that follows.
+cudaError_t launch_spec_verify(const DecodeParams &P, int D, int gate, cudaStream_t s);
+cudaError_t launch_spec_commit(const int32_t *idx, const int32_t *accepted, int B, int T, int N, int L,
+                               int32_t *write_pos, int32_t *flush_slots, uint32_t *status, cudaStream_t s);
+
 cudaError_t launch_advance(const int32_t *idx, int B, const uint8_t *ff, int N, int L,
                            int32_t *write_pos, uint32_t *status, cudaStream_t s);
 

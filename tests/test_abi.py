@@ -124,3 +124,34 @@ def test_workspace_size_constant_matches_the_header():
     text = open(os.path.join(ROOT, "include", "gdnreplay.h")).read()
     m = re.search(r"#define GDN_DECODE_ADVANCE_WORKSPACE_BYTES (\d+)", text)
     assert m and int(m.group(1)) == Bd.DECODE_ADVANCE_WORKSPACE_BYTES
+
+
+def _spec_step(batch=4, window=3, row=2 * 16 * 128 + 32 * 128):
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: every case below fails a host check
+    return Bd._SpecStep(fake, Bd.BF16, row, fake, fake, fake, batch, window, 1.0, 0, fake, Bd.F32)
+
+
+def test_spec_verify_and_commit_check_their_arguments(lib):
+    d = _desc()
+    cache = Bd._Cache(0x1000, 0x1000, 0x1000, 0x1000)
+    v = lib.gdn_replayssm_spec_verify
+    # window 0, window = ring_len, short row, negative batch, no write_pos: rejected before any launch
+    for step, wp in ((_spec_step(window=0), 0x1000), (_spec_step(window=16), 0x1000),
+                     (_spec_step(row=100), 0x1000), (_spec_step(batch=-1), 0x1000), (_spec_step(), None)):
+        assert v(ctypes.byref(d), ctypes.byref(cache), wp, ctypes.byref(step), None, None) == 1, \
+            lib.gdn_last_error().decode()
+    assert v(ctypes.byref(_desc(ring_len=64)), ctypes.byref(cache), 0x1000, ctypes.byref(_spec_step(window=33)),
+             None, None) == 2
+    assert v(ctypes.byref(d), ctypes.byref(cache), 0x1000, ctypes.byref(_spec_step(batch=0)), None, None) == 0
+    c = lib.gdn_replayssm_spec_commit
+    assert c(None, None, 0, 3, 8, 16, None, None, None, None) == 0           # empty
+    assert c(0x1000, 0x1000, 4, 3, 8, 16, 0x1000, None, None, None) == 1     # no flush_slots
+    assert c(0x1000, 0x1000, 4, 16, 8, 16, 0x1000, 0x1000, None, None) == 1  # window does not fit the ring
+    assert c(0x1000, 0x1000, 4, 3, 8, 1, 0x1000, 0x1000, None, None) == 1    # ring of one entry
+
+
+def test_status_bits_match_the_header():
+    text = open(os.path.join(ROOT, "include", "gdnreplay.h")).read()
+    bits = {n: int(v) for n, v in re.findall(r"#define GDN_(DEV_\w+)\s+(\d+)u", text)}
+    for n in ("DEV_BAD_SLOT", "DEV_BAD_WRITE_POS", "DEV_TIMEOUT", "DEV_INTERNAL", "DEV_BAD_ACCEPTED"):
+        assert bits[n] == getattr(Bd, n), n
