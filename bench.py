@@ -12,6 +12,8 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|referenc
        [--workload headline|qwen3next_layer|kda_layer|stack30|sweep:B:L:f16|f32] [--recon tensor|ffma]
        [--kernel-only]   (timed decode loop only: for profiling and sweeps)
        [--sweep [--sweep-batches 1,8,...] [--sweep-lens 1,4,...]]  (one JSON line per point)
+       [--spec [--spec-batches 64,256] [--spec-windows 2,4,8] [--spec-accept 0.7]]
+                         (speculative verify window + commit + fold, one JSON line per point)
 Under torchrun each rank runs an independent replica on its own GPU (the
 path has no exchange step); rank 0 prints one JSON line.
 """
@@ -64,6 +66,23 @@ def packed_head_step_bytes(K, V, G, ib, ob, kda=False):
     """Packed decode: the state is read and written every step."""
     g_entry = 4 * K if kda else 4
     return 8 * V * K + 2 * K * ib / G + V * ib + g_entry + 4 + V * ob
+
+
+def spec_head_bytes(K, V, G, p, T, rb, ib, ob, kda=False):
+    """Bytes one (row, value head) must move in a verify window of T tokens at
+    cursor p: the checkpoint read, the p committed ring entries read, the T
+    window entries written, T tokens of inputs and of output."""
+    g_entry = 4 * K if kda else 4
+    ring_entry = V * rb + K * rb / G + g_entry
+    return (4 * V * K + (p + T) * ring_entry + T * (2 * K * ib / G + V * ib + g_entry + 4)
+            + T * V * ob)
+
+
+def fold_head_bytes(K, V, G, p, rb, kda=False):
+    """Bytes of folding p ring entries of one (slot, value head) into its
+    checkpoint: the checkpoint read and written, the entries read."""
+    g_entry = 4 * K if kda else 4
+    return 8 * V * K + p * (V * rb + K * rb / G + g_entry)
 
 
 def launch_bytes(w, p_rows, flush_rows, ob, n_pad, cursors=True):
@@ -432,6 +451,133 @@ def run_sweep(args):
     return 0
 
 
+def acceptance_pool(rng, n, rows, T, rate):
+    """Accepted counts per row for n windows: drafts are accepted one by one
+    with probability `rate` until the first rejection (a in [0, T])."""
+    import numpy as np
+    acc = np.zeros((n, rows), dtype=np.int32)
+    alive = np.ones((n, rows), dtype=bool)
+    for _ in range(T):
+        alive &= rng.random((n, rows)) < rate
+        acc += alive
+    return acc
+
+
+def measure_spec(B, T, K, warmup, dev, rate=0.7, L=16, recon=None):
+    """One layer of speculative decoding at the benchmark's layer shape
+    (HV=32, HK=16, K=V=128, fp16 ring, bf16 inputs and output), B rows: each
+    timed window is gdn_replayssm_spec_verify of T tokens per row, the commit of
+    a seeded acceptance draw, and the fold + cursor reset of the slots the
+    commit lists.  Kernel-only (inputs resident).  Also times the verify launch
+    alone and T single-token decode + advance steps for comparison."""
+    import numpy as np
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import inputs as I
+
+    recon = Bd.RECON_TENSOR if recon is None else recon
+    w = I.Workload(f"spec window: N={max(B, 512)} B={B} T={T} HV=32 HK=16 K=V=128 L={L} fp16 ring bf16 qkv",
+                   N=max(B, 512), B=B, HV=32, HK=16, K=128, L=L, ring_dtype=Bd.F16, qkv_dtype=Bd.BF16, seed=5)
+    gen = I.generator(w.seed, dev)
+    wp = torch.randint(0, L - T, (w.N,), generator=gen, device=dev, dtype=torch.int32)
+    c = I.cache(gen, w, wp, dev)
+    cache = Bd.Cache(c.state, c.ring_d, c.ring_k, c.ring_g)
+    idx = I.indices(gen, w.B, w.N, 0, dev)
+    desc = Bd.layer_desc(w.N, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, ring_dtype=w.ring_dtype)
+    pool = [I.step_inputs(gen, w, dev, rows=B * T) for _ in range(4)]
+    out = torch.empty((B * T, w.HV, w.V), dtype=torch.bfloat16, device=dev)
+    steps_in = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out) for b in pool]
+    acc_h = acceptance_pool(np.random.default_rng(w.seed), 16, B, T, rate)
+    acc_dev = [torch.from_numpy(a).to(dev) for a in acc_h]
+    fs = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    idx_h = idx.cpu().numpy()
+    wp_h = wp.cpu().numpy().copy()
+    G = w.HV // w.HK
+
+    def window(i):
+        Bd.gdn_replayssm_spec_verify(desc, cache, wp, T, steps_in[i % 4], recon, status, stream)
+        Bd.gdn_replayssm_spec_commit(idx, acc_dev[i % 16], T, w.N, L, wp, fs, status, stream)
+        Bd.gdn_replayssm_flush(desc, cache, wp, fs, status, stream)
+        Bd.gdn_replayssm_reset_slots(wp, fs, status, stream)
+
+    def host_window(i):
+        """The window's algorithmic bytes; moves the host copy of the cursors."""
+        p = wp_h[idx_h]
+        nb = w.HV * sum(spec_head_bytes(w.K, w.V, G, int(x), T, 2, 2, 2) for x in p)
+        a = acc_h[i % 16]
+        nb += 16 * B  # commit: cursor read + write, accepted read, fold-list write
+        q = p + a
+        fold = q + T > L - 1
+        nb += w.HV * sum(fold_head_bytes(w.K, w.V, G, int(x), 2) for x in q[fold]) + 4 * int(fold.sum())
+        wp_h[idx_h] = np.where(fold, 0, q)
+        return nb, int(a.sum()), int(fold.sum())
+
+    for i in range(warmup):
+        window(i)
+        host_window(i)
+    total = accepted = folds = 0
+    for i in range(warmup, warmup + K):
+        nb, na, nf = host_window(i)
+        total += nb
+        accepted += na
+        folds += nf
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record(stream)
+    for i in range(warmup, warmup + K):
+        window(i)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    assert np.array_equal(wp.cpu().numpy(), wp_h), "device cursors diverged from the commit rule"
+    win_s = ev[0].elapsed_time(ev[1]) / 1e3 / K
+    # the verify launch alone, at the cursors the loop left (verify moves none)
+    vb = w.HV * sum(spec_head_bytes(w.K, w.V, G, int(x), T, 2, 2, 2) for x in wp_h[idx_h])
+    nv = max(K // 2, 16)
+    ev[2].record(stream)
+    for i in range(nv):
+        Bd.gdn_replayssm_spec_verify(desc, cache, wp, T, steps_in[i % 4], recon, status, stream)
+    ev[3].record(stream)
+    torch.cuda.synchronize()
+    ver_s = ev[2].elapsed_time(ev[3]) / 1e3 / nv
+    peak, _ = measured_hbm_peak()
+    dec = measure_replay(I.sweep_point(B, L, Bd.F16), max(K, 2 * L), 2 * L, Bd.RECON_TENSOR, dev)
+    return {"workload": w.name, "B": B, "T": T, "L": L, "acceptance_rate_per_draft": rate, "windows": K,
+            "ms_per_window": win_s * 1e3, "mean_accepted": accepted / K / B, "folds_per_window": folds / K,
+            "verified_tokens_per_s": B * T / win_s, "accepted_tokens_per_s": accepted / K / win_s,
+            "algorithmic_bytes_per_window": total / K, "window_hbm_gbs_algorithmic": total / K / win_s / 1e9,
+            "verify_ms_per_launch": ver_s * 1e3, "verify_hbm_gbs_algorithmic": vb / ver_s / 1e9,
+            "verify_frac": vb / ver_s / 1e9 / peak, "verify_frac_of_8tbs": vb / ver_s / 1e9 / 8000.0,
+            "decode_ms_per_step": dec["ms_per_launch"],
+            "window_vs_T_decode_steps": T * dec["ms_per_launch"] / (win_s * 1e3)}
+
+
+def run_spec(args):
+    """Speculative-window sweep: one JSON line per (batch, window)."""
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import build as cuda_build
+
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cuda_build.build()
+    Bd.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    for B in [int(x) for x in args.spec_batches.split(",")]:
+        for T in [int(x) for x in args.spec_windows.split(",")]:
+            recon = Bd.RECON_FFMA if args.recon == "ffma" else Bd.RECON_TENSOR
+            r = measure_spec(B, T, max(args.steps, 32), args.warmup, dev, rate=args.spec_accept, recon=recon)
+            r["recon"] = args.recon
+            print(json.dumps(r), flush=True)
+            torch.cuda.empty_cache()
+    return 0
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -637,6 +783,12 @@ def main():
                     help="batch x ring length x ring dtype sweep of one layer (one JSON line per point)")
     ap.add_argument("--sweep-batches", default="1,8,64,128,256,512")
     ap.add_argument("--sweep-lens", default="1,4,8,16,32")
+    ap.add_argument("--spec", action="store_true",
+                    help="speculative verify window sweep (one JSON line per batch x window)")
+    ap.add_argument("--spec-batches", default="64,256")
+    ap.add_argument("--spec-windows", default="2,4,8")
+    ap.add_argument("--spec-accept", type=float, default=0.7,
+                    help="probability that each draft token is accepted (until the first rejection)")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--ref-budget", type=float, default=60.0,
@@ -648,6 +800,8 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.spec:
+        return run_spec(args)
     return run_ours(args)
 
 

@@ -240,10 +240,13 @@ typedef struct {
  * position p + t (k once per key head).  The checkpoint and write_pos are not
  * changed: after the target model has accepted a tokens, call
  * gdn_replayssm_spec_commit.  A row whose window does not fit sets
- * GDN_DEV_BAD_WRITE_POS and is treated as padding (zeros).  Replay on the CUDA
- * cores in fp32. */
+ * GDN_DEV_BAD_WRITE_POS and is treated as padding (zeros).
+ * recon = GDN_RECON_TENSOR: the checkpoint products S0 [q_t, k_t] run on the
+ * tensor cores (tf32) for K = V = 128 and window <= 16, the ring and window
+ * terms in fp32 on the CUDA cores; other shapes, or GDN_RECON_FFMA, use the
+ * CUDA-core kernel (all fp32). */
 GDN_API gdn_status_t gdn_replayssm_spec_verify(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
-                                       const int32_t *write_pos, const gdn_spec_step_t *step,
+                                       const int32_t *write_pos, const gdn_spec_step_t *step, int32_t recon,
                                        uint32_t *dev_status, gdn_stream_t stream);
 
 /* Commit after a verify window, once per forward ([P3] "rollback is a cursor

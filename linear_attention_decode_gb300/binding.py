@@ -104,7 +104,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_replayssm_decode_advance.argtypes = [dp, cp, vp, vp, sp, i32, vp, vp, u32p, vp]
         lib.gdn_replayssm_decode_advance_noalloc.argtypes = [dp, cp, vp, vp, sp, i32, vp, u32p, vp]
         lib.gdn_replayssm_advance.argtypes = [vp, i32, vp, i32, i32, vp, u32p, vp]
-        lib.gdn_replayssm_spec_verify.argtypes = [dp, cp, vp, ctypes.POINTER(_SpecStep), u32p, vp]
+        lib.gdn_replayssm_spec_verify.argtypes = [dp, cp, vp, ctypes.POINTER(_SpecStep), i32, u32p, vp]
         lib.gdn_replayssm_spec_commit.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, u32p, vp]
         lib.gdn_replayssm_flush.argtypes = [dp, cp, vp, vp, i32, u32p, vp]
         lib.gdn_replayssm_reset_slots.argtypes = [vp, i32, vp, i32, u32p, vp]
@@ -253,7 +253,8 @@ def gdn_replayssm_decode_advance_noalloc(desc: LayerDesc, cache: Cache, write_po
 
 
 def gdn_replayssm_spec_verify(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor, window: int,
-                              step: Step, dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+                              step: Step, recon: int = RECON_TENSOR, dev_status: Optional[torch.Tensor] = None,
+                              stream=None) -> None:
     """Speculative verify window: `step` holds B*T token rows (token t of row b
     at row b*T + t) and ssm_state_indices [B]; out is [B*T, HV, V]."""
     T = int(window)
@@ -275,7 +276,7 @@ def gdn_replayssm_spec_verify(desc: LayerDesc, cache: Cache, write_pos: torch.Te
     c = _pack_cache(desc, cache)
     _check(load_library().gdn_replayssm_spec_verify(
         ctypes.byref(desc), ctypes.byref(c), _dev(write_pos, "write_pos", (desc.num_slots,), torch.int32),
-        ctypes.byref(s), _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_spec_verify")
+        ctypes.byref(s), int(recon), _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_spec_verify")
 
 
 def gdn_replayssm_spec_commit(ssm_state_indices: torch.Tensor, accepted: torch.Tensor, window: int,

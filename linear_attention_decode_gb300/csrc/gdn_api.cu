@@ -213,13 +213,14 @@ gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, const gd
 }
 
 gdn_status_t gdn_replayssm_spec_verify(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
-                                       const int32_t *write_pos, const gdn_spec_step_t *step,
+                                       const int32_t *write_pos, const gdn_spec_step_t *step, int32_t recon,
                                        uint32_t *dev_status, gdn_stream_t stream) {
   gdn_status_t st = check_desc(desc);
   if (st != GDN_OK) return st;
   if ((st = check_cache(desc, cache)) != GDN_OK) return st;
   if (!step) return fail(GDN_ERR_INVALID_ARG, "step is NULL");
   if (!write_pos) return fail(GDN_ERR_INVALID_ARG, "write_pos is NULL");
+  if (recon != GDN_RECON_TENSOR && recon != GDN_RECON_FFMA) return fail(GDN_ERR_INVALID_ARG, "unknown recon");
   if (step->batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch must be >= 0");
   if (step->window < 1 || step->window > desc->ring_len - 1)
     return fail(GDN_ERR_INVALID_ARG, "window must be in [1, ring_len - 1]");
@@ -252,7 +253,14 @@ gdn_status_t gdn_replayssm_spec_verify(const gdn_layer_desc_t *desc, const gdn_l
   P.ring_g = cache->ring_g;
   P.write_pos = write_pos;
   P.status = dev_status;
-  cudaError_t e = gdn::launch_spec_verify(P, desc->k_dim, desc->gate, (cudaStream_t)stream);
+  cudaError_t e = cudaErrorNotSupported;
+  if (recon == GDN_RECON_TENSOR) {
+    const char *why = nullptr;
+    e = gdn::launch_spec_tc(P, desc->k_dim, desc->gate, (cudaStream_t)stream, &why);
+    if (e != cudaSuccess && e != cudaErrorNotSupported)
+      return cuda_fail(e, why ? why : "gdn_replayssm_spec_verify tensor-core launch");
+  }
+  if (e == cudaErrorNotSupported) e = gdn::launch_spec_verify(P, desc->k_dim, desc->gate, (cudaStream_t)stream);
   return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_replayssm_spec_verify launch");
 }
 

@@ -25,8 +25,17 @@ cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUte
 
 cudaError_t launch_fold(const DecodeParams &P, int D, int gate, int n, cudaStream_t s);
 
-// Speculative verify window (P.T tokens per row) and the commit that follows.
+// Tensor map of the checkpoint as [N*HV*V rows, K fp32 columns] with boxes of
+// [V rows x 32 columns], 128-byte swizzled.  Writes a reason into *why on failure.
+cudaError_t make_state_tmap(const DecodeParams &P, int D, CUtensorMap *map, const char **why);
+
+// Speculative verify window (P.T tokens per row) on the CUDA cores, and the
+// commit that follows.
 cudaError_t launch_spec_verify(const DecodeParams &P, int D, int gate, cudaStream_t s);
+// The same window with the checkpoint contraction on the tensor cores.  Returns
+// cudaErrorNotSupported, with nothing launched, for configurations it does not
+// cover (the caller then uses the CUDA-core kernel).
+cudaError_t launch_spec_tc(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why);
 cudaError_t launch_spec_commit(const int32_t *idx, const int32_t *accepted, int B, int T, int N, int L,
                                int32_t *write_pos, int32_t *flush_slots, uint32_t *status, cudaStream_t s);
 

@@ -315,9 +315,7 @@ static cudaError_t launch_kind(const DecodeParams &P, const CUtensorMap &map, si
   return launch_t<D, GATE, 2, GDN_F32>(P, map, smem, s);
 }
 
-cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why,
-                             bool *fused) {
-  *fused = false;
+cudaError_t make_state_tmap(const DecodeParams &P, int D, CUtensorMap *map, const char **why) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) {
     *why = "cuTensorMapEncodeTiled is not available from the driver";
@@ -325,18 +323,26 @@ cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_
   }
   // The checkpoint as a 2-D tensor [N*HV*V rows, K fp32 columns]; one box is
   // [V rows x 32 columns] = 128-byte rows, 128-byte swizzle.
-  CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)P.N * P.HV * D};
   const cuuint64_t strides[1] = {(cuuint64_t)D * 4};
   const cuuint32_t box[2] = {32, (cuuint32_t)D};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, P.state, dims, strides, box, estr,
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, P.state, dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     *why = "cuTensorMapEncodeTiled rejected the checkpoint tensor";
     return cudaErrorInvalidValue;
   }
+  return cudaSuccess;
+}
+
+cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why,
+                             bool *fused) {
+  *fused = false;
+  CUtensorMap map;
+  const cudaError_t em = make_state_tmap(P, D, &map, why);
+  if (em != cudaSuccess) return em;
   const cudaError_t e = launch_tcp_decode(P, D, gate, map, s);
   if (e != cudaErrorNotSupported) {
     *fused = e == cudaSuccess && P.sync != nullptr;

@@ -138,11 +138,12 @@ def test_spec_verify_and_commit_check_their_arguments(lib):
     # window 0, window = ring_len, short row, negative batch, no write_pos: rejected before any launch
     for step, wp in ((_spec_step(window=0), 0x1000), (_spec_step(window=16), 0x1000),
                      (_spec_step(row=100), 0x1000), (_spec_step(batch=-1), 0x1000), (_spec_step(), None)):
-        assert v(ctypes.byref(d), ctypes.byref(cache), wp, ctypes.byref(step), None, None) == 1, \
+        assert v(ctypes.byref(d), ctypes.byref(cache), wp, ctypes.byref(step), 0, None, None) == 1, \
             lib.gdn_last_error().decode()
+    assert v(ctypes.byref(d), ctypes.byref(cache), 0x1000, ctypes.byref(_spec_step()), 7, None, None) == 1
     assert v(ctypes.byref(_desc(ring_len=64)), ctypes.byref(cache), 0x1000, ctypes.byref(_spec_step(window=33)),
-             None, None) == 2
-    assert v(ctypes.byref(d), ctypes.byref(cache), 0x1000, ctypes.byref(_spec_step(batch=0)), None, None) == 0
+             0, None, None) == 2
+    assert v(ctypes.byref(d), ctypes.byref(cache), 0x1000, ctypes.byref(_spec_step(batch=0)), 0, None, None) == 0
     c = lib.gdn_replayssm_spec_commit
     assert c(None, None, 0, 3, 8, 16, None, None, None, None) == 0           # empty
     assert c(0x1000, 0x1000, 4, 3, 8, 16, 0x1000, None, None, None) == 1     # no flush_slots

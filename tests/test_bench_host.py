@@ -79,3 +79,22 @@ def test_reference_arm_other_ranks_exit_without_work():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--steps", "2", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_spec_window_bytes():
+    """A window of T tokens reads the checkpoint once (not T times): at the
+    benchmark's head shape (K=V=128, G=2, fp16 ring, bf16 inputs and output)."""
+    ring_entry = 128 * 2 + 128 * 2 / 2 + 4
+    inputs = 2 * 128 * 2 / 2 + 128 * 2 + 4 + 4
+    assert bench.spec_head_bytes(128, 128, 2, 5, 4, 2, 2, 2) == 65536 + 9 * ring_entry + 4 * inputs + 4 * 256
+    assert bench.fold_head_bytes(128, 128, 2, 7, 2) == 131072 + 7 * ring_entry
+    kda_entry = 128 * 2 + 128 * 2 + 512
+    assert bench.fold_head_bytes(128, 128, 1, 3, 2, kda=True) == 131072 + 3 * kda_entry
+
+
+def test_acceptance_pool_is_a_prefix_count():
+    import numpy as np
+    acc = bench.acceptance_pool(np.random.default_rng(0), 64, 32, 4, 0.7)
+    assert acc.min() >= 0 and acc.max() <= 4
+    assert 0 < (acc == 0).mean() < 1 and (acc == 4).any()
+    assert abs(acc.mean() - sum(0.7 ** i for i in range(1, 5))) < 0.15

@@ -19,7 +19,7 @@ from linear_attention_decode_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
 
-FF = Bd.RECON_FFMA
+FF, TC = Bd.RECON_FFMA, Bd.RECON_TENSOR
 
 CASES = {
     # fp32 ring: the CUDA-core bound; GQA 2:1, padding rows, several windows per fold
@@ -67,10 +67,11 @@ def _compare_window(dev: Bd.Cache, ora: O.Cache, w: I.Workload, idx, wp_before, 
     assert rel_err(rd[~nan], ora.ring_d[~nan]) <= ring_tolerance(w, tol), f"{tag}: ring d tensor"
 
 
+@pytest.mark.parametrize("recon", [TC, FF], ids=["tensor", "ffma"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_spec_windows_match_the_oracle(gdnlib, name):
+def test_spec_windows_match_the_oracle(gdnlib, name, recon):
     w, T = CASES[name]
-    tol = tolerance(w, FF)
+    tol = tolerance(w, recon)
     gen = I.generator(w.seed, "cpu")
     wp = _cursors(gen, w, T)
     c = I.cache(gen, w, wp, "cpu")
@@ -94,7 +95,7 @@ def test_spec_windows_match_the_oracle(gdnlib, name):
         out = torch.full((rows * T, w.HV, w.V), float("nan"), device="cuda")
         Bd.gdn_replayssm_spec_verify(desc, dev, wp_dev, T,
                                      Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx_dev, out),
-                                     status)
+                                     recon, status)
         wp_before = wp_ora.copy()
         o_ref, st = O.spec_verify(G, ora, wp_ora, idx_h, T, si.mixed_qkv, si.g, si.beta)
         torch.cuda.synchronize()
@@ -165,7 +166,7 @@ def test_tensor_core_decode_reads_what_the_windows_cached(gdnlib):
         out = torch.empty((rows * T, w.HV, w.V), device="cuda")
         Bd.gdn_replayssm_spec_verify(desc, dev, wp_dev, T,
                                      Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx_dev, out),
-                                     status)
+                                     TC, status)
         O.spec_verify(G, ora, wp_ora, idx_h, T, si.mixed_qkv, si.g, si.beta)
         acc = acc_rng.integers(0, T + 1, size=rows).astype(np.int32)
         Bd.gdn_replayssm_spec_commit(idx_dev, torch.from_numpy(acc).cuda(), T, w.N, w.L, wp_dev, flush_dev,
@@ -210,14 +211,15 @@ def test_spec_bad_rows_report_and_touch_nothing(gdnlib):
     dev = Bd.Cache(c.state.cuda(), c.ring_d.cuda(), c.ring_k.cuda(), c.ring_g.cuda())
     ora = O.Cache.from_arrays(c.state, c.ring_d, c.ring_k, c.ring_g)
     desc, G = desc_of(w), oracle_geom(w)
-    for rows_idx, want in (([1], Bd.DEV_BAD_WRITE_POS), ([9], Bd.DEV_BAD_SLOT)):
+    for (rows_idx, want), recon in [(c, r) for c in (([1], Bd.DEV_BAD_WRITE_POS), ([9], Bd.DEV_BAD_SLOT))
+                                    for r in (TC, FF)]:
         idx = torch.tensor(rows_idx, dtype=torch.int32)
         si = I.step_inputs(gen, w, "cpu", rows=T)
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         out = torch.full((T, w.HV, w.V), float("nan"), device="cuda")
         Bd.gdn_replayssm_spec_verify(desc, dev, wp.cuda(), T,
                                      Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx.cuda(), out),
-                                     status)
+                                     recon, status)
         o_ref, st = O.spec_verify(G, ora, wp.numpy().copy(), idx.numpy(), T, si.mixed_qkv, si.g, si.beta)
         torch.cuda.synchronize()
         assert int(status.item()) == want == st
@@ -261,7 +263,8 @@ def test_spec_headline_sizes_sampled(gdnlib):
     mini = O.Cache.from_arrays(dev.state[sl], dev.ring_d[sl], dev.ring_k[sl], dev.ring_g[sl])
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.full((rows * T, w.HV, w.V), float("nan"), dtype=torch.bfloat16, device="cuda")
-    Bd.gdn_replayssm_spec_verify(desc_of(w), dev, wp, T, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out), status)
+    Bd.gdn_replayssm_spec_verify(desc_of(w), dev, wp, T, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out), TC,
+                                 status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     tok = torch.as_tensor((chosen[:, None] * T + np.arange(T)[None, :]).reshape(-1), device="cuda")
