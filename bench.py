@@ -9,7 +9,7 @@ uniformly over [0, L) so flush and append rows mix in every launch.  Every step
 reads 512 MiB of checkpoint (4x the 129 MB L2), so no L2 flush is needed.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       [--workload headline|qwen3next_layer|kda_layer|stack30|sweep:B:L:f16|f32] [--recon tensor|ffma]
+       [--workload headline|qwen3next_layer|kda_layer|stack30|sweep:B:L:f16|f32] [--recon tensor|ffma|output]
        [--kernel-only]   (timed decode loop only: for profiling and sweeps)
        [--sweep [--sweep-batches 1,8,...] [--sweep-lens 1,4,...]]  (one JSON line per point)
        [--spec [--spec-batches 64,256] [--spec-windows 2,4,8] [--spec-accept 0.7]]
@@ -570,6 +570,8 @@ def run_spec(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     for B in [int(x) for x in args.spec_batches.split(",")]:
         for T in [int(x) for x in args.spec_windows.split(",")]:
+            if args.recon == "output":
+                raise SystemExit("--spec verifies with --recon tensor or ffma")
             recon = Bd.RECON_FFMA if args.recon == "ffma" else Bd.RECON_TENSOR
             r = measure_spec(B, T, max(args.steps, 32), args.warmup, dev, rate=args.spec_accept, recon=recon)
             r["recon"] = args.recon
@@ -605,7 +607,7 @@ def run_ours(args):
         if ws > 1:
             dist.destroy_process_group()
         return 0
-    recon = Bd.RECON_FFMA if args.recon == "ffma" else Bd.RECON_TENSOR
+    recon = {"ffma": Bd.RECON_FFMA, "output": Bd.RECON_OUTPUT}.get(args.recon, Bd.RECON_TENSOR)
     rb = 4 if w.ring_dtype == Bd.F32 else 2
     gen = I.generator(w.seed + rank, dev)
     wp = I.write_pos(gen, w, dev)
@@ -777,7 +779,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=32)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="headline")
-    ap.add_argument("--recon", choices=["tensor", "ffma"], default="tensor")
+    ap.add_argument("--recon", choices=["tensor", "ffma", "output"], default="tensor")
     ap.add_argument("--kernel-only", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="batch x ring length x ring dtype sweep of one layer (one JSON line per point)")

@@ -75,8 +75,13 @@ typedef enum { GDN_GATE_SCALAR = 0, GDN_GATE_PER_K = 1 } gdn_gate_t;
  * TENSOR: the L-deep sum is one small GEMM on the tensor cores (tcgen05, fp32
  *         accumulation) — [P1] Design 2.  Operands: f16, bf16 or tf32 for an
  *         fp16, bf16 or fp32 ring.
- * FFMA:   every term in fp32 on the CUDA cores (slower, tighter error bound). */
-typedef enum { GDN_RECON_TENSOR = 0, GDN_RECON_FFMA = 1 } gdn_recon_t;
+ * FFMA:   every term in fp32 on the CUDA cores (slower, tighter error bound).
+ * OUTPUT: a non-flush row never forms S: its readout is factored through the
+ *         ring, S x = A (S0 x) + sum_j w_j d_j (k_j . x) (KDA: S0 (A o x) +
+ *         sum_j d_j ((w_j o k_j) . x)), fp32 on the CUDA cores — the
+ *         "output-only" reconstruction of [P1] Design 1 and [P2] 3.2; flush rows
+ *         rebuild S as FFMA does.  Same results as FFMA up to rounding order. */
+typedef enum { GDN_RECON_TENSOR = 0, GDN_RECON_FFMA = 1, GDN_RECON_OUTPUT = 2 } gdn_recon_t;
 
 /* dev_status bits */
 #define GDN_DEV_BAD_SLOT      1u /* ssm_state_indices[b] >= num_slots               */
@@ -148,7 +153,7 @@ GDN_API gdn_status_t gdn_packed_decode(const gdn_layer_desc_t *desc, float *stat
  * of the forward.  force_flush ([B] uint8, nonzero = flush) may be NULL.
  * flushed_out ([B] uint8, may be NULL) receives 1 for rows that flushed.
  * Padding rows (s < 0) get out = 0, flushed_out = 0 and touch nothing.
- * Rows must map to distinct slots.  recon is a gdn_recon_t. */
+ * Rows must map to distinct slots.  recon is a gdn_recon_t (all three built). */
 GDN_API gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
                                   const int32_t *write_pos, const uint8_t *force_flush,
                                   const gdn_step_t *step, int32_t recon, uint8_t *flushed_out,

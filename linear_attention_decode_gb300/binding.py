@@ -20,7 +20,7 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdnreplay.so")
 
 from .constants import (BF16, DEV_BAD_ACCEPTED, DEV_BAD_SLOT, DEV_BAD_WRITE_POS, DEV_INTERNAL, DEV_TIMEOUT,  # noqa: F401
-                        F16, F32, GATE_PER_K, GATE_SCALAR, GDN_DTYPE, RECON_FFMA, RECON_TENSOR,
+                        F16, F32, GATE_PER_K, GATE_SCALAR, GDN_DTYPE, RECON_FFMA, RECON_OUTPUT, RECON_TENSOR,
                         TORCH_DTYPE)
 
 

@@ -143,8 +143,8 @@ gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gdn_layer_
   if ((st = check_step(desc, step)) != GDN_OK) return st;
   if ((st = check_cache(desc, cache)) != GDN_OK) return st;
   if (!write_pos) return fail(GDN_ERR_INVALID_ARG, "write_pos is NULL");
-  if (recon != GDN_RECON_TENSOR && recon != GDN_RECON_FFMA)
-    return fail(GDN_ERR_INVALID_ARG, "recon must be GDN_RECON_TENSOR or GDN_RECON_FFMA");
+  if (recon != GDN_RECON_TENSOR && recon != GDN_RECON_FFMA && recon != GDN_RECON_OUTPUT)
+    return fail(GDN_ERR_INVALID_ARG, "recon must be GDN_RECON_TENSOR, GDN_RECON_FFMA or GDN_RECON_OUTPUT");
   if (step->batch == 0) return GDN_OK;
   gdn::DecodeParams P = base_params(desc);
   fill_step(P, step);
@@ -159,6 +159,8 @@ gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gdn_layer_
   cudaError_t e;
   if (recon == GDN_RECON_FFMA) {
     e = gdn::launch_ffma_decode(P, desc->k_dim, desc->gate, true, (cudaStream_t)stream);
+  } else if (recon == GDN_RECON_OUTPUT) {
+    e = gdn::launch_output_only_decode(P, desc->k_dim, desc->gate, (cudaStream_t)stream);
   } else {
     const char *why = nullptr;
     bool fused = false;
@@ -179,8 +181,8 @@ gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, const gd
   if (!write_pos) return fail(GDN_ERR_INVALID_ARG, "write_pos is NULL");
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
     return fail(GDN_ERR_INVALID_ARG, "workspace must be a 4-byte aligned device pointer");
-  if (recon != GDN_RECON_TENSOR && recon != GDN_RECON_FFMA)
-    return fail(GDN_ERR_INVALID_ARG, "recon must be GDN_RECON_TENSOR or GDN_RECON_FFMA");
+  if (recon != GDN_RECON_TENSOR && recon != GDN_RECON_FFMA && recon != GDN_RECON_OUTPUT)
+    return fail(GDN_ERR_INVALID_ARG, "recon must be GDN_RECON_TENSOR, GDN_RECON_FFMA or GDN_RECON_OUTPUT");
   if (step->batch == 0) return GDN_OK;
   gdn::DecodeParams P = base_params(desc);
   fill_step(P, step);
@@ -196,6 +198,8 @@ gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, const gd
   bool fused = false;
   if (recon == GDN_RECON_FFMA) {
     e = gdn::launch_ffma_decode(P, desc->k_dim, desc->gate, true, (cudaStream_t)stream);
+  } else if (recon == GDN_RECON_OUTPUT) {
+    e = gdn::launch_output_only_decode(P, desc->k_dim, desc->gate, (cudaStream_t)stream);
   } else {
     P.sync = workspace;
     P.write_pos_w = write_pos;

@@ -17,7 +17,23 @@ constexpr int kThreads = 128;
 // Stages the replay operands of (slot, hv) in shared memory ([P1] Design 1, 7):
 //   GDN: Dw[j][r] = w_j d_j[r], Kr[j][c] = k_j[c], returns A;
 //   KDA: Dw[j][r] = d_j[r],     Kr[j][c] = w_j[c] k_j[c], Acol[c] = A[c].
-// Only entries j < p are read.  Ends with a CTA barrier.
+// Only entries j < p are read; the ring rows are fetched kStageBatch entries
+// at a time so their loads are in flight together.  Ends with a CTA barrier.
+constexpr int kStageBatch = 8;
+
+// In-place suffix decays of one channel: on entry x[j * stride] = g_j, on exit
+// x[j * stride] = w_j = exp(sum_{j<i<p} g_i); returns A = exp(sum_{i<p} g_i).
+// The sums run from the newest entry backwards, as replay_decays does.
+__device__ __forceinline__ float decays_in_place(float *x, int stride, int p) {
+  float s = 0.f;
+  for (int j = p - 1; j >= 0; --j) {
+    const float gj = x[j * stride];
+    x[j * stride] = expf(s);
+    s += gj;
+  }
+  return expf(s);
+}
+
 template <int D, int GATE>
 __device__ float stage_replay(const DecodeParams &P, int slot, int hv, int p, float *wv,
                               float *Acol, float *Dw, float *Kr) {
@@ -27,21 +43,47 @@ __device__ float stage_replay(const DecodeParams &P, int slot, int hv, int p, fl
   const int64_t kbase = ((int64_t)slot * P.HK + hk) * P.L * D;
   float A = 1.f;
   if (GATE == GDN_GATE_SCALAR) {
-    if (t == 0) wv[63] = replay_decays(P.ring_g + ((int64_t)slot * P.HV + hv) * P.L, 1, p, wv, 1);
+    if (t < p) wv[t] = P.ring_g[((int64_t)slot * P.HV + hv) * P.L + t];
+    __syncthreads();
+    if (t == 0) wv[63] = decays_in_place(wv, 1, p);
     __syncthreads();
     A = wv[63];
-    if (t < D)
-      for (int j = 0; j < p; ++j) {
-        Dw[j * D + t] = wv[j] * load_as_f32(P.ring_d, dbase + (int64_t)j * D + t, P.ring_dtype);
-        Kr[j * D + t] = load_as_f32(P.ring_k, kbase + (int64_t)j * D + t, P.ring_dtype);
+  } else if (t < D) {
+    const float *g = P.ring_g + ((int64_t)slot * P.HV + hv) * P.L * D + t;
+    for (int j0 = 0; j0 < p; j0 += kStageBatch) {
+      float gv[kStageBatch];
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) gv[u] = j0 + u < p ? g[(int64_t)(j0 + u) * D] : 0.f;
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u)
+        if (j0 + u < p) Kr[(j0 + u) * D + t] = gv[u];
+    }
+    Acol[t] = decays_in_place(Kr + t, D, p);  // w_j[c] parked in Kr
+  }
+  if (t < D) {
+    for (int j0 = 0; j0 < p; j0 += kStageBatch) {
+      float dv[kStageBatch], kv[kStageBatch];
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        dv[u] = 0.f;
+        kv[u] = 0.f;
+        if (j0 + u < p) {
+          dv[u] = load_as_f32(P.ring_d, dbase + (int64_t)(j0 + u) * D + t, P.ring_dtype);
+          kv[u] = load_as_f32(P.ring_k, kbase + (int64_t)(j0 + u) * D + t, P.ring_dtype);
+        }
       }
-  } else {
-    if (t < D) {
-      const float *g = P.ring_g + ((int64_t)slot * P.HV + hv) * P.L * D + t;
-      Acol[t] = replay_decays(g, D, p, Kr + t, D);  // w_j[c] parked in Kr
-      for (int j = 0; j < p; ++j) {
-        Dw[j * D + t] = load_as_f32(P.ring_d, dbase + (int64_t)j * D + t, P.ring_dtype);
-        Kr[j * D + t] *= load_as_f32(P.ring_k, kbase + (int64_t)j * D + t, P.ring_dtype);
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int j = j0 + u;
+        if (j < p) {
+          if (GATE == GDN_GATE_SCALAR) {
+            Dw[j * D + t] = wv[j] * dv[u];
+            Kr[j * D + t] = kv[u];
+          } else {
+            Dw[j * D + t] = dv[u];
+            Kr[j * D + t] *= kv[u];
+          }
+        }
       }
     }
   }
@@ -51,7 +93,12 @@ __device__ float stage_replay(const DecodeParams &P, int slot, int hv, int p, fl
 
 // REPLAY = false: packed decode (read S, write S every step).
 // REPLAY = true:  ReplaySSM decode with the replay sum on the CUDA cores.
-template <int D, int GATE, bool REPLAY>
+// OUT_ONLY (with REPLAY): a non-flush row never forms the replayed state; its
+// readout is factored through the ring ([P1] Design 1 "output-only"; [P2] 3.2):
+//   GDN: S x = A (S0 x) + sum_j (w_j d_j) (k_j . x),
+//   KDA: S x = S0 (A o x) + sum_j d_j ((w_j o k_j) . x),   x = q, k (KDA: a o q, a o k),
+// O(V K + p (V + K)) per head instead of O(p V K).  Flush rows rebuild S as above.
+template <int D, int GATE, bool REPLAY, bool OUT_ONLY = false>
 __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParams P) {
   constexpr int M = D / 32;             // float4 chunks per lane per row
   constexpr int ROWS_PER_WARP = D / 4;  // 4 warps
@@ -63,6 +110,7 @@ __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParam
   float *q = reinterpret_cast<float *>(smem_f4);
   float *k = q + D, *v = k + D, *a = v + D, *Acol = a + D, *red = Acol + D, *wv = red + 8;
   float *Dw = wv + 64, *Kr = Dw + (P.L - 1) * D;
+  float *zq = Kr + (P.L - 1) * D, *zk = zq + 64;  // OUT_ONLY: k_j . x for the staged entries
 
   RowInfo ri;
   if (REPLAY) {
@@ -80,6 +128,15 @@ __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParam
   const int slot = ri.slot, p = ri.p;
   const int64_t bh = (int64_t)b * P.HV + hv;
 
+  // the checkpoint's first rows are requested before the inputs and the ring
+  float4 *S = reinterpret_cast<float4 *>(P.state + ((int64_t)slot * P.HV + hv) * D * D);
+  float4 cur[M], nxt[M];
+  {
+    const int r0 = warp * ROWS_PER_WARP + rg;
+#pragma unroll
+    for (int m = 0; m < M; ++m) cur[m] = S[r0 * (D / 4) + 8 * m + cg];
+  }
+
   const float kq = load_qkv<D>(P, b, hv, q, k, v, red);
   const float beta = P.beta[bh];
   float alpha = 1.f, A = 1.f;
@@ -92,6 +149,28 @@ __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParam
   if (REPLAY) {
     A = stage_replay<D, GATE>(P, slot, hv, p, wv, Acol, Dw, Kr);
   } else {
+    __syncthreads();
+  }
+  const bool out_only = OUT_ONLY && !ri.flush;
+  if (out_only) {  // zq[j] = Kr[j] . x_q, zk[j] = Kr[j] . x_k, one warp per entry
+    for (int j = warp; j < p; j += 4) {
+      float zqa = 0.f, zka = 0.f;
+      for (int c = lane; c < D; c += 32) {
+        const float kr = Kr[j * D + c];
+        const float ac = GATE == GDN_GATE_PER_K ? a[c] : 1.f;
+        zqa = fmaf(kr, ac * q[c], zqa);
+        zka = fmaf(kr, ac * k[c], zka);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        zqa += __shfl_xor_sync(0xffffffffu, zqa, o);
+        zka += __shfl_xor_sync(0xffffffffu, zka, o);
+      }
+      if (lane == 0) {
+        zq[j] = zqa;
+        zk[j] = zka;
+      }
+    }
     __syncthreads();
   }
 
@@ -111,13 +190,6 @@ __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParam
     }
   }
 
-  float4 *S = reinterpret_cast<float4 *>(P.state + ((int64_t)slot * P.HV + hv) * D * D);
-  float4 cur[M], nxt[M];
-  {
-    const int r0 = warp * ROWS_PER_WARP + rg;
-#pragma unroll
-    for (int m = 0; m < M; ++m) cur[m] = S[r0 * (D / 4) + 8 * m + cg];
-  }
 #pragma unroll 1
   for (int it = 0; it < NIT; ++it) {
     const int r = warp * ROWS_PER_WARP + it * 4 + rg;
@@ -125,8 +197,31 @@ __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParam
 #pragma unroll
       for (int m = 0; m < M; ++m) nxt[m] = S[(r + 4) * (D / 4) + 8 * m + cg];
     }
-    // Replayed row r of the pre-token state.
+    float sq = 0.f, sk = 0.f;
     float4 s[M];
+    if (out_only) {
+      // S0 row r against the decayed readout vectors, plus this lane's share
+      // (j = cg mod 8) of the ring terms; the row's shuffle sums the rest.
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const float4 c = GATE == GDN_GATE_PER_K
+                             ? make_float4(A4[m].x * cur[m].x, A4[m].y * cur[m].y, A4[m].z * cur[m].z,
+                                           A4[m].w * cur[m].w)
+                             : cur[m];
+        sq = dot4(c, qe[m], sq);
+        sk = dot4(c, ke[m], sk);
+      }
+      if (GATE == GDN_GATE_SCALAR) {
+        sq *= A;
+        sk *= A;
+      }
+      for (int j = cg; j < p; j += 8) {
+        const float dw = Dw[j * D + r];
+        sq = fmaf(dw, zq[j], sq);
+        sk = fmaf(dw, zk[j], sk);
+      }
+    } else {
+    // Replayed row r of the pre-token state.
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       if (GATE == GDN_GATE_SCALAR) {
@@ -150,11 +245,11 @@ __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParam
         }
       }
     }
-    float sq = 0.f, sk = 0.f;
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       sq = dot4(s[m], qe[m], sq);
       sk = dot4(s[m], ke[m], sk);
+    }
     }
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) {
@@ -477,15 +572,15 @@ __global__ void reset_kernel(int32_t *write_pos, int N, const int32_t *slots, in
 // Host launchers.
 // ---------------------------------------------------------------------------
 
-static size_t ffma_smem_bytes(int D, int L, bool replay) {
-  size_t floats = 5 * (size_t)D + 8 + 64 + (replay ? 2 * (size_t)(L - 1) * D : 0);
+static size_t ffma_smem_bytes(int D, int L, bool replay, bool out_only = false) {
+  size_t floats = 5 * (size_t)D + 8 + 64 + (replay ? 2 * (size_t)(L - 1) * D : 0) + (out_only ? 128 : 0);
   return floats * sizeof(float);
 }
 
-template <int D, int GATE, bool REPLAY>
+template <int D, int GATE, bool REPLAY, bool OUT_ONLY = false>
 static cudaError_t launch_decode_t(const DecodeParams &P, cudaStream_t s) {
-  const size_t smem = ffma_smem_bytes(D, P.L, REPLAY);
-  auto kern = ffma_decode_kernel<D, GATE, REPLAY>;
+  const size_t smem = ffma_smem_bytes(D, P.L, REPLAY, OUT_ONLY);
+  auto kern = ffma_decode_kernel<D, GATE, REPLAY, OUT_ONLY>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -503,6 +598,12 @@ cudaError_t launch_ffma_decode(const DecodeParams &P, int D, int gate, bool repl
   if (gate == GDN_GATE_SCALAR)
     return replay ? launch_decode_t<64, 0, true>(P, s) : launch_decode_t<64, 0, false>(P, s);
   return replay ? launch_decode_t<64, 1, true>(P, s) : launch_decode_t<64, 1, false>(P, s);
+}
+
+cudaError_t launch_output_only_decode(const DecodeParams &P, int D, int gate, cudaStream_t s) {
+  if (D == 128)
+    return gate == GDN_GATE_SCALAR ? launch_decode_t<128, 0, true, true>(P, s) : launch_decode_t<128, 1, true, true>(P, s);
+  return gate == GDN_GATE_SCALAR ? launch_decode_t<64, 0, true, true>(P, s) : launch_decode_t<64, 1, true, true>(P, s);
 }
 
 template <int D, int GATE>

@@ -11,6 +11,10 @@ namespace gdn {
 // Packed decode (replay = false) or ReplaySSM decode with FFMA replay (replay = true).
 cudaError_t launch_ffma_decode(const DecodeParams &P, int D, int gate, bool replay, cudaStream_t s);
 
+// ReplaySSM decode whose non-flush rows read the output out through the ring
+// without forming the replayed state (CUDA cores); flush rows as the FFMA replay.
+cudaError_t launch_output_only_decode(const DecodeParams &P, int D, int gate, cudaStream_t s);
+
 // ReplaySSM decode with the replay sum on the tensor cores (tcgen05) and the
 // checkpoint streamed by TMA.  Writes a reason into *why on a host-side failure.
 // With P.sync set, *fused tells whether the launched kernel also advanced the

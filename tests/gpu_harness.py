@@ -23,7 +23,7 @@ TOL_TC = 2e-3
 
 
 def tolerance(w: I.Workload, recon: int) -> float:
-    if recon == Bd.RECON_FFMA and w.ring_dtype == Bd.F32:
+    if recon in (Bd.RECON_FFMA, Bd.RECON_OUTPUT) and w.ring_dtype == Bd.F32:
         return TOL_FFMA_F32
     if w.ring_dtype == Bd.BF16:
         # Both sides round nearly equal corrections d to bf16 on their own; a

@@ -35,6 +35,9 @@ CASES = {
     # CUDA-core replay: decode and advance are two launches inside the call
     "ffma": (I.Workload("ffma", N=16, B=5, n_pad=2, HV=8, HK=4, K=128, L=16, ring_dtype=Bd.F32,
                         qkv_dtype=Bd.BF16, steps=18, staggered=True, seed=25), FF, False),
+    # output-only readout: also two launches
+    "output_only": (I.Workload("output", N=16, B=5, n_pad=2, HV=8, HK=4, K=128, L=16, ring_dtype=Bd.F16,
+                               qkv_dtype=Bd.BF16, steps=18, staggered=True, seed=28), Bd.RECON_OUTPUT, True),
     "ring_len_1": (I.Workload("L=1", N=16, B=5, n_pad=2, HV=8, HK=4, K=128, L=1, ring_dtype=Bd.F16,
                               qkv_dtype=Bd.BF16, steps=3, seed=26), TC, False),
 }

@@ -15,7 +15,7 @@ from linear_attention_decode_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
 
-TC, FF = Bd.RECON_TENSOR, Bd.RECON_FFMA
+TC, FF, OUT = Bd.RECON_TENSOR, Bd.RECON_FFMA, Bd.RECON_OUTPUT
 
 # Several CTAs per launch, a ragged batch with padding rows, mixed flush and
 # append rows (staggered cursors) and GQA 2:1, at the pages' head size.
@@ -30,25 +30,25 @@ def _lib(gdnlib):
     yield
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 def test_tiny_fp32(recon):
     rep = run_parity(I.TINY, recon)
     assert sum(s.flushes for s in rep.steps) == 8 * I.TINY.B  # 32 steps, L = 4
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 @pytest.mark.parametrize("ring", [Bd.F16, Bd.BF16, Bd.F32], ids=["f16", "bf16", "f32"])
 def test_ragged_staggered(recon, ring):
     rep = run_parity(I.with_(RAGGED, ring_dtype=ring), recon)
     assert sum(s.flushes for s in rep.steps) > 0 and sum(s.appends for s in rep.steps) > 0
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 def test_kda(recon):
     run_parity(KDA_SMALL, recon)
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 @pytest.mark.parametrize("gate,L", [(Bd.GATE_SCALAR, 8), (Bd.GATE_PER_K, 8), (Bd.GATE_PER_K, 24)],
                          ids=["gdn_L8", "kda_L8", "kda_L24"])
 def test_head_dim_64(recon, gate, L):
@@ -57,7 +57,7 @@ def test_head_dim_64(recon, gate, L):
     run_parity(w, recon)
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 @pytest.mark.parametrize("ring", [Bd.F16, Bd.F32], ids=["f16", "f32"])
 @pytest.mark.parametrize("gate", [Bd.GATE_SCALAR, Bd.GATE_PER_K], ids=["gdn", "kda"])
 def test_longest_ring(recon, ring, gate):
@@ -70,14 +70,14 @@ def test_longest_ring(recon, ring, gate):
     assert sum(s.flushes for s in rep.steps) == 2
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 def test_forced_flush_mid_ring(recon):
     sched = lambda t, rows: (np.arange(rows) % 3 == t % 3).astype(np.uint8) if t % 5 == 2 else np.zeros(rows, np.uint8)
     rep = run_parity(I.with_(RAGGED, steps=20), recon, force=sched)
     assert sum(s.flushes for s in rep.steps) > 0
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 def test_three_layer_stack_shared_cursor(recon):
     run_parity(I.with_(RAGGED, steps=18), recon, layers=3)
 
@@ -87,12 +87,12 @@ def test_bf16_output():
     run_parity(I.with_(RAGGED, steps=10), TC, out_dtype=torch.bfloat16, tol=TOL_TC + 2.0 ** -8)
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 def test_in_kernel_l2norm_and_scale(recon):
     run_parity(I.with_(RAGGED, steps=6), recon, q_scale=0.37, qk_l2norm=True)
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 def test_beta0_g0_leaves_checkpoint_bit_identical(recon):
     """beta = 0 and g = 0 at every step: d = 0 and alpha = 1, so after a full
     ring cycle the flushed checkpoint equals S0 bit for bit."""
@@ -123,7 +123,7 @@ def test_beta0_g0_leaves_checkpoint_bit_identical(recon):
     assert torch.equal(layer.dev.state.cpu().view(torch.int32), S0.view(torch.int32))
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 def test_erased_history_closed_form(recon):
     """g = -1e4 makes alpha underflow to 0: out = beta v (k^T q) whatever the history."""
     w = I.with_(RAGGED, steps=1)
@@ -212,7 +212,7 @@ def test_packed_decode_vs_oracle(gate):
         assert rel_err(dev.cpu().numpy(), ora) <= 1e-5
 
 
-@pytest.mark.parametrize("recon", [FF, TC], ids=["ffma", "tensor"])
+@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
 def test_bad_rows_set_status_and_touch_nothing(recon):
     w = I.with_(RAGGED, steps=1)
     gen = I.generator(w.seed, "cpu")
@@ -252,7 +252,7 @@ def test_empty_and_all_padding_batches():
         idx = torch.full((rows,), -1, dtype=torch.int32, device="cuda")
         si = I.step_inputs(gen, w, "cuda", rows=rows)
         out = torch.full((rows, w.HV, w.V), float("nan"), device="cuda")
-        for recon in (FF, TC):
+        for recon in (FF, TC, OUT):
             Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wp.cuda(), None,
                                     Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out), recon)
         Bd.gdn_packed_decode(desc_of(w), layer.dev.state, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out))
@@ -306,6 +306,11 @@ def test_host_side_rejects_bad_arguments():
 def test_full_size_sampled(w):
     """The launch configuration the benchmark times, checked on sampled rows."""
     run_sampled(w, TC, steps=3)
+
+
+def test_full_size_sampled_output_only():
+    """The output-only readout at the benchmark's layer size, sampled rows."""
+    run_sampled(I.HEADLINE, OUT, steps=3)
 
 
 def test_drift_after_four_rings():
