@@ -73,6 +73,12 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
                                        dp, dp, dp, ctypes.c_double, ctypes.c_int, dp, up]
     lib.oracle_spec_commit.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ip, ip,
                                        ip, ip, up]
+    fp = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_step_f32.argtypes = [ctypes.c_int, ctypes.c_int, fp, fp, fp, fp, ctypes.c_float, fp,
+                                    ctypes.c_float, fp, fp]
+    lib.oracle_lossless_verify.argtypes = [gp, dp, ctypes.c_int, ctypes.c_int, ip, dp, dp, dp,
+                                           ctypes.c_double, ctypes.c_int, dp, dp, dp, dp, up]
+    lib.oracle_lossless_commit.argtypes = [gp, fp, ctypes.c_int, ctypes.c_int, ip, ip, ip, fp, fp, fp, up]
     return lib
 
 
@@ -261,3 +267,63 @@ def spec_commit(N: int, L: int, T: int, indices, accepted, write_pos: np.ndarray
     _lib().oracle_spec_commit(N, L, int(T), idx.shape[0], _i(idx), _i(acc), _i(write_pos), _i(fs),
                               ctypes.byref(st))
     return fs, st.value
+
+
+def _f(a: np.ndarray):
+    assert a.dtype == np.float32 and a.flags.c_contiguous, "binary32 oracle arrays are C-contiguous float32"
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def f32(a) -> np.ndarray:
+    """Exact (or RNE) conversion of any numeric array to C-contiguous float32."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().to("cpu", torch.float32).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def step_f32(h: np.ndarray, q, k, v, g: float, beta: float, gk=None):
+    """One binary32 step of the sequential recurrence (decayed state formed once,
+    update as one fma); h ([V][K] float32) updated in place. Returns (y, u)."""
+    V, K = h.shape
+    q, k, v = f32(q), f32(k), f32(v)
+    gkk = None if gk is None else f32(gk)
+    y, u = np.zeros(V, dtype=np.float32), np.zeros(V, dtype=np.float32)
+    _lib().oracle_step_f32(K, V, _f(h), _f(q), _f(k), _f(v), float(g), None if gkk is None else _f(gkk),
+                           float(beta), _f(y), _f(u))
+    return y, u
+
+
+def lossless_verify(G: Geom, state: np.ndarray, indices, T: int, mixed_qkv, g, beta,
+                    q_scale: float = 1.0, qk_l2norm: int = 0):
+    """Verify of T tokens per row without a state update. Returns
+    (o [B*T, HV, V], tup_u [B, T, HV, V], tup_k [B, T, HK, K], tup_g [B, T, HV(, K)], status);
+    tuples are fp32 values held in float64."""
+    idx = np.ascontiguousarray(np.asarray(indices, dtype=np.int32))
+    qkv, gg, bb = f64(mixed_qkv), f64(g), f64(beta)
+    B = idx.shape[0]
+    o = np.zeros((B * T, G.HV, G.V))
+    tu = np.zeros((B, T, G.HV, G.V))
+    tk = np.zeros((B, T, G.HK, G.K))
+    tg = np.zeros((B, T, G.HV, G.K) if G.gate == GATE_PER_K else (B, T, G.HV))
+    st = ctypes.c_uint(0)
+    _lib().oracle_lossless_verify(ctypes.byref(G), _d(state), B, int(T), _i(idx), _d(qkv), _d(gg), _d(bb),
+                                  float(q_scale), int(qk_l2norm), _d(o), _d(tu), _d(tk), _d(tg),
+                                  ctypes.byref(st))
+    return o, tu, tk, tg, st.value
+
+
+def lossless_commit(G: Geom, state: np.ndarray, T: int, src, accepted, tup_u, tup_k, tup_g, dst=None) -> int:
+    """Exact-order (binary32) replay of each row's accepted tuples into state
+    (float32 [N, HV, V, K], updated in place). Returns status."""
+    s_ = np.ascontiguousarray(np.asarray(src, dtype=np.int32))
+    a_ = np.ascontiguousarray(np.asarray(accepted, dtype=np.int32))
+    d_ = None if dst is None else np.ascontiguousarray(np.asarray(dst, dtype=np.int32))
+    u, k, g = f32(tup_u), f32(tup_k), f32(tup_g)
+    st = ctypes.c_uint(0)
+    _lib().oracle_lossless_commit(ctypes.byref(G), _f(state), s_.shape[0], int(T), _i(s_),
+                                  None if d_ is None else _i(d_), _i(a_), _f(u), _f(k), _f(g), ctypes.byref(st))
+    return st.value

@@ -436,3 +436,132 @@ int oracle_spec_commit(int N, int L, int T, int B, const int *indices, const int
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Lossless speculative verify and its exact-order commit (sglang pull        */
+/* request #42388: "The idea"; Modifications, "Verify kernel" and "Commit").  */
+/* Verify updates no state and keeps, per draft token, the fp32 tuple         */
+/* (u, k, g) instead of a state snapshot; the commit rebuilds the accepted    */
+/* state from the checkpoint by replaying the tuples with the sequential      */
+/* kernel's own rounding, so the committed state is bit-identical to it.      */
+/* ------------------------------------------------------------------------- */
+
+/* One fp32 step of the sequential recurrence with the rounding the pages give
+ * its verify kernel: the decayed state D = fl32(h * a) is formed once and used
+ * twice, by the delta reduction and by the update,
+ *   Sk_r = sum_c D[r][c] k[c]  (fp32, c ascending),   u_r = fl32(beta * fl32(v_r - Sk_r)),
+ *   h[r][c] = fma(k[c], u_r, D[r][c]),                 y_r = sum_c h[r][c] q[c]  (fp32),
+ * with a = expf(g) for every channel (GDN, gk == NULL) or a_c = expf(gk[c]) (KDA).
+ * h is [V][K] in IEEE binary32. */
+void oracle_step_f32(int K, int V, float *h, const float *q, const float *k, const float *v,
+                     float g, const float *gk, float beta, float *y, float *u)
+{
+    float alpha = expf(g);
+    for (int r = 0; r < V; r++) {
+        float *hr = h + (size_t)r * K;
+        for (int c = 0; c < K; c++) hr[c] = hr[c] * (gk ? expf(gk[c]) : alpha);  /* D */
+        float sk = 0.0f;
+        for (int c = 0; c < K; c++) sk = sk + hr[c] * k[c];
+        float diff = v[r] - sk;
+        u[r] = beta * diff;
+        for (int c = 0; c < K; c++) hr[c] = fmaf(k[c], u[r], hr[c]);
+        float yr = 0.0f;
+        for (int c = 0; c < K; c++) yr = yr + hr[c] * q[c];
+        y[r] = yr;
+    }
+}
+
+/* Verify of B rows x T tokens that writes no state: row b with slot
+ * s = indices[b] runs O1 (oracle_gdn_step / oracle_kda_step) from the
+ * checkpoint state[s] over its T tokens (token t at input row b*T + t); token
+ * t's output goes to o row b*T + t and its correction u, key k (after the
+ * optional norm) and log-gate g, rounded to fp32 (the tuples are always fp32),
+ * to
+ *   tup_u [B][T][HV][V],  tup_k [B][T][HK][K],  tup_g [B][T][HV] (KDA [B][T][HV][K]).
+ * The checkpoint is unchanged.  Padding rows (slot < 0) and slots >= N (which
+ * set ORACLE_BAD_SLOT) get zero outputs and leave the tuples alone. */
+int oracle_lossless_verify(const oracle_geom *G, const double *state, int B, int T, const int *indices,
+                           const double *mixed_qkv, const double *g, const double *beta,
+                           double q_scale, int qk_l2norm, double *o, double *tup_u, double *tup_k,
+                           double *tup_g, unsigned *status)
+{
+    int K = G->K, V = G->V, HV = G->HV, HK = G->HK;
+    int kda = G->gate == ORACLE_GATE_PER_K;
+    size_t gsz = kda ? (size_t)HV * K : (size_t)HV;
+    double *q = malloc(sizeof(double) * K), *k = malloc(sizeof(double) * K);
+    double *v = malloc(sizeof(double) * V), *u = malloc(sizeof(double) * V);
+    double *S = malloc(sizeof(double) * (size_t)V * K);
+    for (int b = 0; b < B; b++) {
+        int slot = indices[b];
+        if (slot >= G->N) *status |= ORACLE_BAD_SLOT;
+        for (int hv = 0; hv < HV; hv++) {
+            if (slot < 0 || slot >= G->N) {
+                for (int t = 0; t < T; t++)
+                    for (int r = 0; r < V; r++) o[(((size_t)b * T + t) * HV + hv) * V + r] = 0.0;
+                continue;
+            }
+            int hk = hv / (HV / HK);
+            memcpy(S, state + ((size_t)slot * HV + hv) * V * K, sizeof(double) * (size_t)V * K);
+            for (int t = 0; t < T; t++) {
+                size_t row = (size_t)b * T + t;
+                unpack_head(G, mixed_qkv + row * row_len(G), hv, q, k, v);
+                prepare_qk(K, q, k, q_scale, qk_l2norm);
+                double bt = beta[row * HV + hv];
+                double *ob = o + (row * HV + hv) * V;
+                const double *gt = g + row * gsz + (kda ? (size_t)hv * K : (size_t)hv);
+                if (kda) oracle_kda_step(K, V, S, q, k, v, gt, bt, ob, u);
+                else oracle_gdn_step(K, V, S, q, k, v, gt[0], bt, ob, u);
+                for (int r = 0; r < V; r++) tup_u[(row * HV + hv) * V + r] = oracle_round(u[r], ORACLE_F32);
+                for (int c = 0; c < K; c++) tup_k[(row * HK + hk) * K + c] = oracle_round(k[c], ORACLE_F32);
+                if (kda)
+                    for (int c = 0; c < K; c++) tup_g[(row * HV + hv) * K + c] = oracle_round(gt[c], ORACLE_F32);
+                else
+                    tup_g[row * HV + hv] = oracle_round(gt[0], ORACLE_F32);
+            }
+        }
+    }
+    free(q); free(k); free(v); free(u); free(S);
+    return 0;
+}
+
+/* Exact-order commit: for row b with source slot s = src[b] and a = accepted[b]
+ * tokens (0 <= a <= T), every value head replays, in IEEE binary32,
+ *   h[r][c] <- fma(k_t[c], u_t[r], fl32(h[r][c] * a_t)),   t = 0 .. a-1,
+ * from h = state[s], with a_t = expf(g_t) (KDA: a_t[c] = expf(g_t[c])): the
+ * decayed state is one rounded multiply and the rank-1 update one fused
+ * multiply-add, as in the sequential step.  The result is stored at slot
+ * dst[b] (dst == NULL: back at s).  Tuples as oracle_lossless_verify lays them
+ * out, in fp32.  Rows with s < 0, a < 0 or dst[b] < 0 are skipped; a slot >= N
+ * sets ORACLE_BAD_SLOT and a > T sets ORACLE_BAD_ACCEPTED (row skipped). */
+int oracle_lossless_commit(const oracle_geom *G, float *state, int B, int T, const int *src,
+                           const int *dst, const int *accepted, const float *tup_u, const float *tup_k,
+                           const float *tup_g, unsigned *status)
+{
+    int K = G->K, V = G->V, HV = G->HV, HK = G->HK;
+    int kda = G->gate == ORACLE_GATE_PER_K;
+    float *h = malloc(sizeof(float) * (size_t)V * K);
+    for (int b = 0; b < B; b++) {
+        int s = src[b], d = dst ? dst[b] : s, a = accepted[b];
+        if (s < 0 || d < 0 || a < 0) continue;
+        if (s >= G->N || d >= G->N) { *status |= ORACLE_BAD_SLOT; continue; }
+        if (a > T) { *status |= ORACLE_BAD_ACCEPTED; continue; }
+        for (int hv = 0; hv < HV; hv++) {
+            int hk = hv / (HV / HK);
+            memcpy(h, state + ((size_t)s * HV + hv) * V * K, sizeof(float) * (size_t)V * K);
+            for (int t = 0; t < a; t++) {
+                size_t row = (size_t)b * T + t;
+                const float *ut = tup_u + (row * HV + hv) * V;
+                const float *kt = tup_k + (row * HK + hk) * K;
+                for (int r = 0; r < V; r++)
+                    for (int c = 0; c < K; c++) {
+                        float at = kda ? expf(tup_g[(row * HV + hv) * K + c]) : expf(tup_g[row * HV + hv]);
+                        float decayed = h[(size_t)r * K + c] * at;
+                        h[(size_t)r * K + c] = fmaf(kt[c], ut[r], decayed);
+                    }
+            }
+            memcpy(state + ((size_t)d * HV + hv) * V * K, h, sizeof(float) * (size_t)V * K);
+        }
+    }
+    free(h);
+    return 0;
+}

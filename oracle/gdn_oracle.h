@@ -71,6 +71,22 @@ int oracle_spec_verify(const oracle_geom *G, double *state, double *ring_d, doub
 int oracle_spec_commit(int N, int L, int T, int B, const int *indices, const int *accepted,
                        int *write_pos, int *flush_slots, unsigned *status);
 
+/* Lossless verify (no state update, fp32 (u, k, g) tuples per draft token) and
+ * the exact-order commit that replays the accepted tuples in binary32.  The
+ * commit's state is float [N][HV][V][K]; tuples:
+ *   tup_u [B][T][HV][V], tup_k [B][T][HK][K], tup_g [B][T][HV] ([B][T][HV][K] for KDA). */
+void oracle_step_f32(int K, int V, float *h, const float *q, const float *k, const float *v,
+                     float g, const float *gk, float beta, float *y, float *u);
+
+int oracle_lossless_verify(const oracle_geom *G, const double *state, int B, int T, const int *indices,
+                           const double *mixed_qkv, const double *g, const double *beta,
+                           double q_scale, int qk_l2norm, double *o, double *tup_u, double *tup_k,
+                           double *tup_g, unsigned *status);
+
+int oracle_lossless_commit(const oracle_geom *G, float *state, int B, int T, const int *src,
+                           const int *dst, const int *accepted, const float *tup_u, const float *tup_k,
+                           const float *tup_g, unsigned *status);
+
 #ifdef __cplusplus
 }
 #endif

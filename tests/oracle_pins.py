@@ -567,4 +567,164 @@ def pin_spec_bad_rows():
     assert st == O.BAD_ACCEPTED and list(fs) == [-1, -1, -1] and list(wp) == [0, 3, 0]
 
 
+# ---------------------------------------------------------------------------
+# Lossless verify and its exact-order commit (sglang #42388: "The idea";
+# Modifications, "Verify kernel" and "Commit"; the tests it lists).  The commit
+# replays fp32 (u, k, g) tuples with one rounded multiply (the decayed state)
+# and one fma (the update) per element, so its state must equal, bit for bit,
+# the state a binary32 sequential step with that rounding reaches.
+# ---------------------------------------------------------------------------
+
+def _f32_sequence(gate, seed, T, HV, HK, K, V, h0):
+    """Runs oracle_step_f32 T times per value head from h0 [HV][V][K] (float32).
+    Returns the states after every token [T + 1][HV][V][K], outputs, and the
+    tuples (u [T][HV][V], k [T][HK][K], g [T][HV](, K)) in float32."""
+    seq = _Seq(seed, T, HV, HK, K, V, gate)
+    h = h0.copy()
+    states, ys = [h.copy()], np.zeros((T, HV, V), dtype=np.float32)
+    tu = np.zeros((T, HV, V), dtype=np.float32)
+    tk = seq.k.astype(np.float32)
+    tg = seq.g.astype(np.float32)
+    for t in range(T):
+        for hv in range(HV):
+            hk = hv // (HV // HK)
+            gk = tg[t, hv] if gate else None
+            y, u = O.step_f32(h[hv], seq.q[t][hk], tk[t, hk], seq.v[t][hv],
+                              0.0 if gate else tg[t, hv], seq.beta[t][hv], gk=gk)
+            ys[t, hv], tu[t, hv] = y, u
+        states.append(h.copy())
+    return seq, states, ys, tu, tk, tg
+
+
+def _bits_equal(a, b):
+    return np.array_equal(np.asarray(a, dtype=np.float32).view(np.uint32),
+                          np.asarray(b, dtype=np.float32).view(np.uint32))
+
+
+def _lossless_commit_bit_identical(gate):
+    HV, HK, K, V, T, N = 4, 2, K5, V3, 6, 3
+    G = O.geom(N, HV, HK, K, V, gate=gate)
+    r = _rng(500 + gate)
+    pool = (r.standard_normal((N, HV, V, K)) * 0.3).astype(np.float32)
+    slots = [2, 0]
+    runs = [_f32_sequence(gate, 510 + 10 * gate + i, T, HV, HK, K, V, pool[s]) for i, s in enumerate(slots)]
+    tup_u = np.stack([run[3] for run in runs])
+    tup_k = np.stack([run[4] for run in runs])
+    tup_g = np.stack([run[5] for run in runs])
+    # the binary32 step follows the recurrence (O1, double) to fp32 accuracy
+    for (seq, states, ys, _, _, _), s in zip(runs, slots):
+        S = [pool[s, hv].astype(np.float64) for hv in range(HV)]
+        for t in range(T):
+            for hv in range(HV):
+                hk = hv // (HV // HK)
+                fn = O.kda_step if gate else O.gdn_step
+                y, _ = fn(S[hv], seq.q[t][hk], seq.k[t][hk], seq.v[t][hv], seq.g[t][hv], seq.beta[t][hv])
+                _close(ys[t, hv], y, 2e-6, "binary32 step output vs the recurrence")
+                _close(states[t + 1][hv], S[hv], 2e-6, "binary32 step state vs the recurrence")
+    for a0 in range(T + 1):
+        a1 = T - a0
+        st = pool.copy()
+        assert O.lossless_commit(G, st, T, slots, [a0, a1], tup_u, tup_k, tup_g) == 0
+        assert _bits_equal(st[2], runs[0][1][a0]), f"{a0} accepted: committed state is not bit-identical"
+        assert _bits_equal(st[0], runs[1][1][a1]), f"{a1} accepted: committed state is not bit-identical"
+        assert _bits_equal(st[1], pool[1]), "a slot no row names was touched"
+
+
+def pin_lossless_commit_is_bit_identical_gdn():
+    _lossless_commit_bit_identical(O.GATE_SCALAR)
+
+
+def pin_lossless_commit_is_bit_identical_kda():
+    _lossless_commit_bit_identical(O.GATE_PER_K)
+
+
+def _lossless_verify_is_sequential(gate):
+    HV, HK, K, V, T, N = 4, 2, K5, V3, 5, 4
+    G = O.geom(N, HV, HK, K, V, gate=gate, state_dtype=O.F64)
+    r = _rng(520 + gate)
+    state = r.standard_normal((N, HV, V, K)) * 0.3
+    before = state.copy()
+    idx = [3, -1, 1]
+    seqs = [_Seq(530 + 10 * gate + b, T, HV, HK, K, V, gate) for b in range(len(idx))]
+    rows = np.concatenate([np.concatenate([sq.row(t) for t in range(T)]) for sq in seqs])
+    g = np.concatenate([sq.g for sq in seqs])
+    beta = np.concatenate([sq.beta for sq in seqs])
+    o, tu, tk, tg, st = O.lossless_verify(G, state, idx, T, rows, g, beta)
+    assert st == 0 and np.array_equal(state, before), "verify changed the checkpoint"
+    for b, (slot, sq) in enumerate(zip(idx, seqs)):
+        if slot < 0:
+            assert np.all(o[b * T:(b + 1) * T] == 0.0) and np.all(tu[b] == 0.0), "padding row"
+            continue
+        ref = state.copy()  # T packed decodes (which do write the state) on a copy
+        for t in range(T):
+            ob, st2 = O.packed_decode(G, ref, [slot], sq.row(t), sq.g[t][None], sq.beta[t][None])
+            _close(o[b * T + t], ob[0], 1e-13, f"row {b} token {t} output vs packed decode")
+        _, us, _ = _run_sequential(state[slot], sq, T, gate)
+        assert np.array_equal(tu[b], O.round_to(us, O.F32)), "u tuples are not the recurrence's corrections"
+        assert np.array_equal(tk[b], O.round_to(sq.k, O.F32)), "k tuples are not the keys"
+        assert np.array_equal(tg[b], O.round_to(sq.g, O.F32)), "g tuples are not the log-gates"
+        # committing all T tuples (binary32) lands on the recurrence's state
+        f = state.astype(np.float32)
+        assert O.lossless_commit(G, f, T, [slot], [T], tu[b:b + 1], tk[b:b + 1], tg[b:b + 1]) == 0
+        _close(f[slot], ref[slot], 2e-6, "commit of the verify's tuples vs the packed decodes' state")
+    o, tu, tk, tg, st = O.lossless_verify(G, state, [N + 2], T, rows[:T], g[:T], beta[:T])
+    assert st == O.BAD_SLOT and np.all(o == 0.0)
+
+
+def pin_lossless_verify_is_sequential_gdn():
+    _lossless_verify_is_sequential(O.GATE_SCALAR)
+
+
+def pin_lossless_verify_is_sequential_kda():
+    _lossless_verify_is_sequential(O.GATE_PER_K)
+
+
+def pin_lossless_commit_special_cases():
+    """No accepted token or a zero update leaves the state's bits alone; an
+    erased history (exp underflows to 0) leaves exactly fl32(k u); bad rows are
+    reported and touch nothing; negative entries are skipped."""
+    HV, HK, K, V, T, N = 2, 1, 4, 3, 3, 3
+    G = O.geom(N, HV, HK, K, V)
+    r = _rng(540)
+    pool = r.standard_normal((N, HV, V, K)).astype(np.float32)
+    tu = r.standard_normal((1, T, HV, V)).astype(np.float32)
+    tk = r.standard_normal((1, T, HK, K)).astype(np.float32)
+    tg = (-r.random((1, T, HV))).astype(np.float32)
+    st = pool.copy()
+    assert O.lossless_commit(G, st, T, [1], [0], tu, tk, tg) == 0 and _bits_equal(st, pool)
+    st = pool.copy()
+    assert O.lossless_commit(G, st, T, [1], [T], np.zeros_like(tu), tk, np.zeros_like(tg)) == 0
+    assert _bits_equal(st, pool), "g = 0, u = 0 must leave the state's bits unchanged"
+    st = pool.copy()
+    assert O.lossless_commit(G, st, T, [1], [1], tu, tk, np.full_like(tg, -1e4)) == 0
+    want = tu[0, 0, :, :, None] * tk[0, 0, 0][None, None, :]  # float32 products, rounded once
+    assert _bits_equal(st[1], want), "an erased history must leave fl32(k u)"
+    for src, acc, dst, code in (([N], [1], None, O.BAD_SLOT), ([0], [T + 1], None, O.BAD_ACCEPTED),
+                                ([0], [1], [N + 1], O.BAD_SLOT), ([-1], [1], None, 0), ([0], [-1], None, 0),
+                                ([0], [1], [-1], 0)):
+        st = pool.copy()
+        assert O.lossless_commit(G, st, T, src, acc, tu, tk, tg, dst=dst) == code, (src, acc, dst)
+        assert _bits_equal(st, pool), (src, acc, dst)
+
+
+def pin_lossless_track_commit_before_in_place():
+    """#42388 Commit, "Order matters": the prefix-cache track state (m tokens,
+    written to another slot) must be replayed before the in-place replay of the
+    accepted state, because both start from the pre-verify state."""
+    HV, HK, K, V, T, N = 2, 1, K5, V3, 5, 4
+    G = O.geom(N, HV, HK, K, V)
+    r = _rng(550)
+    pool = (r.standard_normal((N, HV, V, K)) * 0.3).astype(np.float32)
+    _, states, _, tu, tk, tg = _f32_sequence(0, 551, T, HV, HK, K, V, pool[0])
+    m, a, track = 2, 4, 3
+    st = pool.copy()
+    assert O.lossless_commit(G, st, T, [0], [m], tu[None], tk[None], tg[None], dst=[track]) == 0
+    assert O.lossless_commit(G, st, T, [0], [a], tu[None], tk[None], tg[None]) == 0
+    assert _bits_equal(st[track], states[m]) and _bits_equal(st[0], states[a])
+    st = pool.copy()  # the wrong order: the track replay starts from the advanced state
+    assert O.lossless_commit(G, st, T, [0], [a], tu[None], tk[None], tg[None]) == 0
+    assert O.lossless_commit(G, st, T, [0], [m], tu[None], tk[None], tg[None], dst=[track]) == 0
+    assert not _bits_equal(st[track], states[m])
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -77,6 +77,24 @@ MUTATIONS = [
     ("spec_fold_rule_one_late",
      "if (p + a + T > L - 1) flush_slots[b] = slot;",
      "if (p + a + T > L) flush_slots[b] = slot;"),
+    ("commit_update_not_fused",
+     "h[(size_t)r * K + c] = fmaf(kt[c], ut[r], decayed);",
+     "h[(size_t)r * K + c] = kt[c] * ut[r] + decayed;"),
+    ("commit_other_contraction",
+     "h[(size_t)r * K + c] = fmaf(kt[c], ut[r], decayed);",
+     "h[(size_t)r * K + c] = fmaf(h[(size_t)r * K + c], at, kt[c] * ut[r]);"),
+    ("commit_one_token_too_many",
+     "for (int t = 0; t < a; t++) {\n                size_t row = (size_t)b * T + t;\n                const float *ut",
+     "for (int t = 0; t <= a && t < T; t++) {\n                size_t row = (size_t)b * T + t;\n                const float *ut"),
+    ("commit_gate_of_next_token",
+     ": expf(tup_g[row * HV + hv]);",
+     ": expf(tup_g[(row + (t + 1 < a)) * HV + hv]);"),
+    ("commit_writes_source_slot",
+     "memcpy(state + ((size_t)d * HV + hv) * V * K, h, sizeof(float) * (size_t)V * K);",
+     "memcpy(state + ((size_t)s * HV + hv) * V * K, h, sizeof(float) * (size_t)V * K);"),
+    ("verify_u_tuple_of_other_head",
+     "for (int r = 0; r < V; r++) tup_u[(row * HV + hv) * V + r] = oracle_round(u[r], ORACLE_F32);",
+     "for (int r = 0; r < V; r++) tup_u[(row * HV + (hv ^ 1)) * V + r] = oracle_round(u[r], ORACLE_F32);"),
     ("spec_capacity_one_more",
      "if (ok && (p < 0 || p + T > G->L - 1)) { *status |= ORACLE_BAD_WRITE_POS; ok = 0; }",
      "if (ok && (p < 0 || p + T > G->L)) { *status |= ORACLE_BAD_WRITE_POS; ok = 0; }"),
