@@ -14,6 +14,8 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|referenc
        [--sweep [--sweep-batches 1,8,...] [--sweep-lens 1,4,...]]  (one JSON line per point)
        [--spec [--spec-batches 64,256] [--spec-windows 2,4,8] [--spec-accept 0.7]]
                          (speculative verify window + commit + fold, one JSON line per point)
+       [--lossless [--spec-batches ...] [--spec-windows ...]]
+                         (lossless verify + exact-order commit, one JSON line per point)
 Under torchrun each rank runs an independent replica on its own GPU (the
 path has no exchange step); rank 0 prints one JSON line.
 """
@@ -83,6 +85,24 @@ def fold_head_bytes(K, V, G, p, rb, kda=False):
     checkpoint: the checkpoint read and written, the entries read."""
     g_entry = 4 * K if kda else 4
     return 8 * V * K + p * (V * rb + K * rb / G + g_entry)
+
+
+def lossless_verify_head_bytes(K, V, G, T, ib, ob, kda=False):
+    """Bytes one (row, value head) must move in a lossless verify of T tokens:
+    the state read once, T tokens of inputs and of output, T fp32 tuples
+    written (u per value head, k once per key head, g)."""
+    g_entry = 4 * K if kda else 4
+    return (4 * V * K + T * (2 * K * ib / G + V * ib + g_entry + 4 + V * ob)
+            + T * (4 * V + 4 * K / G + g_entry))
+
+
+def lossless_commit_head_bytes(K, V, G, a, kda=False):
+    """Exact-order commit of a tuples into one (slot, value head) in place: the
+    state read and written and the a tuples read; nothing when a = 0."""
+    if a <= 0:
+        return 0.0
+    g_entry = 4 * K if kda else 4
+    return 8 * V * K + a * (4 * V + 4 * K / G + g_entry)
 
 
 def launch_bytes(w, p_rows, flush_rows, ob, n_pad, cursors=True):
@@ -580,6 +600,104 @@ def run_spec(args):
     return 0
 
 
+def measure_lossless(B, T, K, warmup, dev, rate=0.7):
+    """Lossless verify + exact-order commit of one GDN layer (HV=32, HK=16,
+    K=V=128, fp32 state, bf16 inputs and output), B rows of T tokens: each timed
+    window is gdn_lossless_verify and gdn_lossless_commit of a seeded acceptance
+    draw, in place.  Four disjoint slot sets rotate so no window finds its
+    states in L2.  Kernel-only (inputs resident); also times each launch alone
+    and one packed decode step."""
+    import numpy as np
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import inputs as I
+
+    N = 4 * B
+    w = I.Workload(f"lossless window: N={N} B={B} T={T} HV=32 HK=16 K=V=128 fp32 state bf16 qkv",
+                   N=N, B=B, HV=32, HK=16, K=128, L=1, ring_dtype=Bd.F32, qkv_dtype=Bd.BF16, seed=6)
+    gen = I.generator(w.seed, dev)
+    state = I.state(gen, w.N, w.HV, w.V, w.K, dev)
+    perm = torch.randperm(N, generator=gen, device=dev).to(torch.int32)
+    idx_sets = [perm[i * B:(i + 1) * B].contiguous() for i in range(4)]
+    desc = Bd.layer_desc(w.N, w.HV, w.HK, w.K, w.V, 1)
+    pool = [I.step_inputs(gen, w, dev, rows=B * T) for _ in range(4)]
+    out = torch.empty((B * T, w.HV, w.V), dtype=torch.bfloat16, device=dev)
+    su, sk, sg = Bd.tuple_shapes(desc, B, T)
+    tu, tk, tg = (torch.empty(su, device=dev), torch.empty(sk, device=dev), torch.empty(sg, device=dev))
+    acc_h = acceptance_pool(np.random.default_rng(w.seed), 16, B, T, rate)
+    acc_dev = [torch.from_numpy(a).to(dev) for a in acc_h]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    G = w.HV // w.HK
+
+    def verify(i):
+        b = pool[i % 4]
+        Bd.gdn_lossless_verify(desc, state, T, Bd.Step(b.mixed_qkv, b.g, b.beta, idx_sets[i % 4], out),
+                               tu, tk, tg, status, stream)
+
+    def commit(i):
+        Bd.gdn_lossless_commit(desc, state, idx_sets[i % 4], acc_dev[i % 16], T, tu, tk, tg, None, status, stream)
+
+    vbytes = B * w.HV * lossless_verify_head_bytes(w.K, w.V, G, T, 2, 2)
+    cbytes = [w.HV * sum(lossless_commit_head_bytes(w.K, w.V, G, int(a)) for a in acc_h[j]) + 8 * B
+              for j in range(16)]
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    for i in range(warmup):
+        verify(i)
+        commit(i)
+    win_s = timed(lambda i: (verify(i), commit(i)), K)
+    ver_s = timed(verify, K)
+    com_s = timed(commit, K)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    com_bytes = float(np.mean([cbytes[i % 16] for i in range(K)]))
+    pk = Bd.Step(pool[0].mixed_qkv[:B], pool[0].g[:B], pool[0].beta[:B], idx_sets[0],
+                 torch.empty((B, w.HV, w.V), dtype=torch.bfloat16, device=dev))
+    pk_s = timed(lambda i: Bd.gdn_packed_decode(desc, state, pk, None, stream), max(K // 4, 16))
+    peak, _ = measured_hbm_peak()
+    snap = B * w.HV * (4 * w.V * w.K * (1 + T))  # a snapshot verify: state read + T snapshots written
+    return {"workload": w.name, "B": B, "T": T, "acceptance_rate_per_draft": rate, "windows": K,
+            "mean_accepted": float(acc_h.mean()), "ms_per_window": win_s * 1e3,
+            "verified_tokens_per_s": B * T / win_s,
+            "verify_ms_per_launch": ver_s * 1e3, "verify_algorithmic_bytes": vbytes,
+            "verify_hbm_gbs_algorithmic": vbytes / ver_s / 1e9, "verify_frac": vbytes / ver_s / 1e9 / peak,
+            "commit_ms_per_launch": com_s * 1e3, "commit_algorithmic_bytes": com_bytes,
+            "commit_hbm_gbs_algorithmic": com_bytes / com_s / 1e9, "commit_frac": com_bytes / com_s / 1e9 / peak,
+            "snapshot_verify_bytes_over_lossless": snap / vbytes,
+            "packed_decode_ms_per_step": pk_s * 1e3}
+
+
+def run_lossless(args):
+    """Lossless verify + commit sweep: one JSON line per (batch, window)."""
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import build as cuda_build
+
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cuda_build.build()
+    Bd.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    for B in [int(x) for x in args.spec_batches.split(",")]:
+        for T in [int(x) for x in args.spec_windows.split(",")]:
+            r = measure_lossless(B, T, max(args.steps, 32), args.warmup, dev, rate=args.spec_accept)
+            print(json.dumps(r), flush=True)
+            torch.cuda.empty_cache()
+    return 0
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -787,6 +905,8 @@ def main():
     ap.add_argument("--sweep-lens", default="1,4,8,16,32")
     ap.add_argument("--spec", action="store_true",
                     help="speculative verify window sweep (one JSON line per batch x window)")
+    ap.add_argument("--lossless", action="store_true",
+                    help="lossless verify + exact-order commit sweep (one JSON line per batch x window)")
     ap.add_argument("--spec-batches", default="64,256")
     ap.add_argument("--spec-windows", default="2,4,8")
     ap.add_argument("--spec-accept", type=float, default=0.7,
@@ -804,6 +924,8 @@ def main():
         return run_sweep(args)
     if args.spec:
         return run_spec(args)
+    if args.lossless:
+        return run_lossless(args)
     return run_ours(args)
 
 

@@ -25,6 +25,10 @@
  *       (replay identity), 2.2 (cache layout table), 3.1 (packed mixed_qkv,
  *       ssm_state_indices, negative padding rows), 3.2 (non-flush step), 3.3
  *       (flush step), 5.2 (KDA gate cache [N, HV, L, K]).
+ *  [P3] vLLM pull request #49887 "ReplaySSM: cache SSM inputs for faster Gated
+ *       DeltaNet speculative decode": Core concept, Design notes.
+ *  [P5] sglang pull request #42388 (lossless verify): The idea; Modifications
+ *       (Verify kernel, Commit).
  *
  * Layouts (row-major, innermost last; N slots, HV value heads, HK key heads
  * with HV % HK == 0, K key dim, V value dim, L ring length, B batch rows):
@@ -264,6 +268,45 @@ GDN_API gdn_status_t gdn_replayssm_spec_commit(const int32_t *ssm_state_indices,
                                        int32_t batch, int32_t window, int32_t num_slots,
                                        int32_t ring_len, int32_t *write_pos, int32_t *flush_slots,
                                        uint32_t *dev_status, gdn_stream_t stream);
+
+/* Lossless speculative verify ([P5] The idea; Modifications, Verify kernel):
+ * the sequential verify that updates no state and, in place of a state
+ * snapshot per draft token, keeps each token's (u, k, g) in fp32 tuple buffers.
+ * Row b with slot s = ssm_state_indices[b] decodes its T = window tokens (input
+ * and output rows b*T + t, layouts as in gdn_spec_step_t) with the recurrence of
+ * gdn_packed_decode, starting from state[s]: token t's output is bit-identical
+ * to the output of the t-th of T successive gdn_packed_decode calls on the same
+ * inputs.  Tuples (device, fp32, caller-owned):
+ *   tup_u [B, T, HV, V]          u = beta (v - S~ k), the correction
+ *   tup_k [B, T, HK, K]          the key as the update uses it (after the optional norm)
+ *   tup_g [B, T, HV] (KDA [B, T, HV, K])  the log-gate
+ * state is only read.  Padding rows (s < 0) get zero outputs and leave their
+ * tuples alone; s >= num_slots sets GDN_DEV_BAD_SLOT and is treated the same.
+ * The ring fields of desc are not used.  1 <= window <= 32. */
+GDN_API gdn_status_t gdn_lossless_verify(const gdn_layer_desc_t *desc, const float *state,
+                                         const gdn_spec_step_t *step, float *tup_u, float *tup_k,
+                                         float *tup_g, uint32_t *dev_status, gdn_stream_t stream);
+
+/* Exact-order commit after gdn_lossless_verify ([P5] The idea; Modifications,
+ * Commit): for row b with source slot s = ssm_state_indices[b] and
+ * a = accepted[b] (0 <= a <= window), every value head replays
+ *   h <- fma(k_t, u_t, fl(h * exp(g_t))),   t = 0 .. a-1   (KDA: exp per key channel)
+ * from h = state[s] in fp32, with the decayed state one rounded multiply and the
+ * rank-1 update one fused multiply-add per element — the rounding of
+ * gdn_packed_decode's update — and stores h at slot dst = dst_indices[b]
+ * (dst_indices NULL: back at s).  The stored state is bit-identical to the one
+ * a successive gdn_packed_decode calls leave.  A second target (a prefix-cache
+ * track state at another slot) must be committed before the in-place commit of
+ * the same source, in an earlier call: both replay from the pre-verify state.
+ * Rows with a negative s, dst or a are skipped; s or dst >= num_slots
+ * (GDN_DEV_BAD_SLOT) and a > window (GDN_DEV_BAD_ACCEPTED) are reported and
+ * skipped.  Within one call the rows' destinations must be distinct and differ
+ * from the other rows' sources.  Tuples as gdn_lossless_verify wrote them. */
+GDN_API gdn_status_t gdn_lossless_commit(const gdn_layer_desc_t *desc, float *state,
+                                         const int32_t *ssm_state_indices, const int32_t *dst_indices,
+                                         const int32_t *accepted, int32_t batch, int32_t window,
+                                         const float *tup_u, const float *tup_k, const float *tup_g,
+                                         uint32_t *dev_status, gdn_stream_t stream);
 
 /* Static text for a status code (host). */
 GDN_API const char *gdn_status_str(gdn_status_t status);

@@ -108,9 +108,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_replayssm_spec_commit.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, u32p, vp]
         lib.gdn_replayssm_flush.argtypes = [dp, cp, vp, vp, i32, u32p, vp]
         lib.gdn_replayssm_reset_slots.argtypes = [vp, i32, vp, i32, u32p, vp]
+        lib.gdn_lossless_verify.argtypes = [dp, vp, ctypes.POINTER(_SpecStep), vp, vp, vp, u32p, vp]
+        lib.gdn_lossless_commit.argtypes = [dp, vp, vp, vp, vp, i32, i32, vp, vp, vp, u32p, vp]
         for f in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_decode_advance",
                   "gdn_replayssm_decode_advance_noalloc", "gdn_replayssm_advance", "gdn_replayssm_flush",
-                  "gdn_replayssm_reset_slots", "gdn_replayssm_spec_verify", "gdn_replayssm_spec_commit"):
+                  "gdn_replayssm_reset_slots", "gdn_replayssm_spec_verify", "gdn_replayssm_spec_commit",
+                  "gdn_lossless_verify", "gdn_lossless_commit"):
             getattr(lib, f).restype = ctypes.c_int
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
@@ -250,6 +253,65 @@ def gdn_replayssm_decode_advance_noalloc(desc: LayerDesc, cache: Cache, write_po
         ctypes.byref(s), int(recon),
         _dev(flushed_out, "flushed_out", (B,), torch.uint8, optional=True),
         _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_decode_advance_noalloc")
+
+
+def _pack_spec_step(desc: LayerDesc, T: int, step: Step) -> _SpecStep:
+    B = step.ssm_state_indices.shape[0]
+    HV, HK, K, V = desc.num_v_heads, desc.num_k_heads, desc.k_dim, desc.v_dim
+    q = step.mixed_qkv
+    if not q.is_cuda or q.dim() != 2 or q.shape[0] != B * T or q.stride(1) != 1:
+        raise GdnError("mixed_qkv must be a CUDA [B*T, row] tensor with unit inner stride")
+    if q.shape[1] < 2 * HK * K + HV * V:
+        raise GdnError("mixed_qkv rows are shorter than 2*HK*K + HV*V")
+    if q.dtype not in GDN_DTYPE or step.out.dtype not in GDN_DTYPE:
+        raise GdnError("mixed_qkv and out must be fp32, bf16 or fp16")
+    gshape = (B * T, HV, K) if desc.gate == GATE_PER_K else (B * T, HV)
+    return _SpecStep(q.data_ptr() if B else None, GDN_DTYPE[q.dtype], q.stride(0) if B * T > 1 else q.shape[1],
+                     _dev(step.g, "g", gshape, torch.float32), _dev(step.beta, "beta", (B * T, HV), torch.float32),
+                     _dev(step.ssm_state_indices, "ssm_state_indices", (B,), torch.int32), B, T,
+                     float(step.q_scale), int(bool(step.qk_l2norm)),
+                     _dev(step.out, "out", (B * T, HV, V)), GDN_DTYPE[step.out.dtype])
+
+
+def tuple_shapes(desc: LayerDesc, batch: int, window: int):
+    """Shapes of the lossless verify's fp32 tuple buffers (u, k, g)."""
+    B, T, HV, HK, K, V = batch, window, desc.num_v_heads, desc.num_k_heads, desc.k_dim, desc.v_dim
+    return ((B, T, HV, V), (B, T, HK, K), (B, T, HV, K) if desc.gate == GATE_PER_K else (B, T, HV))
+
+
+def gdn_lossless_verify(desc: LayerDesc, state: torch.Tensor, window: int, step: Step, tup_u: torch.Tensor,
+                        tup_k: torch.Tensor, tup_g: torch.Tensor, dev_status: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    """Lossless verify: `step` holds B*T token rows (token t of row b at row
+    b*T + t); out is [B*T, HV, V]; the fp32 tuples have tuple_shapes(desc, B, T)."""
+    T = int(window)
+    B = step.ssm_state_indices.shape[0]
+    su, sk, sg = tuple_shapes(desc, B, T)
+    s = _pack_spec_step(desc, T, step)
+    _check(load_library().gdn_lossless_verify(
+        ctypes.byref(desc), _dev(state, "state", (desc.num_slots, desc.num_v_heads, desc.v_dim, desc.k_dim),
+                                 torch.float32),
+        ctypes.byref(s), _dev(tup_u, "tup_u", su, torch.float32), _dev(tup_k, "tup_k", sk, torch.float32),
+        _dev(tup_g, "tup_g", sg, torch.float32), _status_ptr(dev_status), _stream(stream)), "gdn_lossless_verify")
+
+
+def gdn_lossless_commit(desc: LayerDesc, state: torch.Tensor, ssm_state_indices: torch.Tensor,
+                        accepted: torch.Tensor, window: int, tup_u: torch.Tensor, tup_k: torch.Tensor,
+                        tup_g: torch.Tensor, dst_indices: Optional[torch.Tensor] = None,
+                        dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Exact-order commit of each row's accepted tuples into state (in place,
+    or into dst_indices[b] when given)."""
+    T = int(window)
+    B = ssm_state_indices.shape[0]
+    su, sk, sg = tuple_shapes(desc, B, T)
+    _check(load_library().gdn_lossless_commit(
+        ctypes.byref(desc), _dev(state, "state", (desc.num_slots, desc.num_v_heads, desc.v_dim, desc.k_dim),
+                                 torch.float32),
+        _dev(ssm_state_indices, "ssm_state_indices", (B,), torch.int32),
+        _dev(dst_indices, "dst_indices", (B,), torch.int32, optional=True),
+        _dev(accepted, "accepted", (B,), torch.int32), B, T,
+        _dev(tup_u, "tup_u", su, torch.float32), _dev(tup_k, "tup_k", sk, torch.float32),
+        _dev(tup_g, "tup_g", sg, torch.float32), _status_ptr(dev_status), _stream(stream)), "gdn_lossless_commit")
 
 
 def gdn_replayssm_spec_verify(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor, window: int,

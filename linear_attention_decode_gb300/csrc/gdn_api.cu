@@ -283,6 +283,73 @@ gdn_status_t gdn_replayssm_spec_commit(const int32_t *ssm_state_indices, const i
   return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_replayssm_spec_commit launch");
 }
 
+gdn_status_t gdn_lossless_verify(const gdn_layer_desc_t *desc, const float *state, const gdn_spec_step_t *step,
+                                 float *tup_u, float *tup_k, float *tup_g, uint32_t *dev_status,
+                                 gdn_stream_t stream) {
+  gdn_status_t st = check_desc(desc);
+  if (st != GDN_OK) return st;
+  if (!step) return fail(GDN_ERR_INVALID_ARG, "step is NULL");
+  if (step->batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch must be >= 0");
+  if (step->window < 1) return fail(GDN_ERR_INVALID_ARG, "window must be >= 1");
+  if (step->window > 32) return fail(GDN_ERR_UNSUPPORTED, "built for window <= 32");
+  if (step->batch == 0) return GDN_OK;
+  if (!state) return fail(GDN_ERR_INVALID_ARG, "state is NULL");
+  if (!aligned16(state)) return fail(GDN_ERR_INVALID_ARG, "state must be 16-byte aligned");
+  if (!tup_u || !tup_k || !tup_g) return fail(GDN_ERR_INVALID_ARG, "tuple buffers must be set");
+  if (!step->mixed_qkv || !step->g || !step->beta || !step->ssm_state_indices || !step->out)
+    return fail(GDN_ERR_INVALID_ARG, "step has a NULL input or output pointer");
+  if (!dtype_ok(step->qkv_dtype) || !dtype_ok(step->out_dtype))
+    return fail(GDN_ERR_INVALID_ARG, "unknown qkv or out dtype");
+  const int64_t row = 2 * (int64_t)desc->num_k_heads * desc->k_dim + (int64_t)desc->num_v_heads * desc->v_dim;
+  if (step->qkv_row_stride < row) return fail(GDN_ERR_INVALID_ARG, "qkv_row_stride is shorter than 2*HK*K + HV*V");
+  if ((int64_t)step->batch * step->window * desc->num_v_heads >= (int64_t)1 << 31)
+    return fail(GDN_ERR_UNSUPPORTED, "batch * window * num_v_heads must be < 2^31");
+  gdn::DecodeParams P = base_params(desc);
+  P.qkv = step->mixed_qkv;
+  P.qkv_dtype = step->qkv_dtype;
+  P.qkv_stride = step->qkv_row_stride;
+  P.g = step->g;
+  P.beta = step->beta;
+  P.idx = step->ssm_state_indices;
+  P.B = step->batch;
+  P.T = step->window;
+  P.q_scale = step->q_scale;
+  P.qk_l2norm = step->qk_l2norm;
+  P.out = step->out;
+  P.out_dtype = step->out_dtype;
+  P.state = const_cast<float *>(state);  // read only
+  P.status = dev_status;
+  cudaError_t e = gdn::launch_lossless_verify(P, desc->k_dim, desc->gate, tup_u, tup_k, tup_g, (cudaStream_t)stream);
+  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_lossless_verify launch");
+}
+
+gdn_status_t gdn_lossless_commit(const gdn_layer_desc_t *desc, float *state, const int32_t *ssm_state_indices,
+                                 const int32_t *dst_indices, const int32_t *accepted, int32_t batch,
+                                 int32_t window, const float *tup_u, const float *tup_k, const float *tup_g,
+                                 uint32_t *dev_status, gdn_stream_t stream) {
+  gdn_status_t st = check_desc(desc);
+  if (st != GDN_OK) return st;
+  if (batch < 0) return fail(GDN_ERR_INVALID_ARG, "batch must be >= 0");
+  if (window < 1) return fail(GDN_ERR_INVALID_ARG, "window must be >= 1");
+  if (window > 32) return fail(GDN_ERR_UNSUPPORTED, "built for window <= 32");
+  if (batch == 0) return GDN_OK;
+  if (!state) return fail(GDN_ERR_INVALID_ARG, "state is NULL");
+  if (!aligned16(state)) return fail(GDN_ERR_INVALID_ARG, "state must be 16-byte aligned");
+  if (!ssm_state_indices || !accepted || !tup_u || !tup_k || !tup_g)
+    return fail(GDN_ERR_INVALID_ARG, "ssm_state_indices, accepted and the tuple buffers must be set");
+  if ((int64_t)batch * window * desc->num_v_heads >= (int64_t)1 << 31)
+    return fail(GDN_ERR_UNSUPPORTED, "batch * window * num_v_heads must be < 2^31");
+  gdn::DecodeParams P = base_params(desc);
+  P.state = state;
+  P.idx = ssm_state_indices;
+  P.B = batch;
+  P.T = window;
+  P.status = dev_status;
+  cudaError_t e = gdn::launch_lossless_commit(P, desc->k_dim, desc->gate, dst_indices, accepted, tup_u, tup_k,
+                                              tup_g, (cudaStream_t)stream);
+  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_lossless_commit launch");
+}
+
 gdn_status_t gdn_replayssm_advance(const int32_t *ssm_state_indices, int32_t batch,
                                    const uint8_t *force_flush, int32_t num_slots, int32_t ring_len,
                                    int32_t *write_pos, uint32_t *dev_status, gdn_stream_t stream) {

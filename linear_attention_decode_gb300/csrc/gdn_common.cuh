@@ -161,32 +161,53 @@ __device__ __forceinline__ float2 block_sum2(float x, float y, float *red) {
   return r;
 }
 
+// Row b's raw inputs for thread t = key / value channel t (zeros for t >= D):
+// q and k of key head hv / G, v of value head hv ([P2] 3.1 packed input).
+struct QkvRaw {
+  float q, k, v;
+};
+
+template <int D>
+__device__ __forceinline__ QkvRaw load_qkv_raw(const DecodeParams &P, int b, int hv) {
+  const int t = threadIdx.x;
+  const int hk = hv / P.G;
+  const int64_t base = (int64_t)b * P.qkv_stride;
+  QkvRaw x{0.f, 0.f, 0.f};
+  if (t < D)
+    load3_as_f32(P.qkv, base + (int64_t)hk * D + t, base + (int64_t)P.HK * D + (int64_t)hk * D + t,
+                 base + 2 * (int64_t)P.HK * D + (int64_t)hv * D + t, P.qkv_dtype, x.q, x.k, x.v);
+  return x;
+}
+
+// Applies the optional L2 norm and q_scale to one token's raw inputs, publishes
+// q, k, v to shared memory and returns k^T q (a CTA-wide sum; ends with a CTA
+// barrier).  Every rounding is pinned, so kernels that share it agree bit for bit.
+template <int D>
+__device__ __forceinline__ float finish_qkv(const DecodeParams &P, QkvRaw x, float *q, float *k, float *v,
+                                            float *red) {
+  const int t = threadIdx.x;
+  float qt = x.q, kt = x.k;
+  if (t < D) v[t] = x.v;
+  if (P.qk_l2norm) {
+    float2 n = block_sum2(__fmul_rn(qt, qt), __fmul_rn(kt, kt), red);
+    qt = __fdiv_rn(qt, __fsqrt_rn(__fadd_rn(n.x, 1e-6f)));
+    kt = __fdiv_rn(kt, __fsqrt_rn(__fadd_rn(n.y, 1e-6f)));
+  }
+  qt = __fmul_rn(qt, P.q_scale);
+  if (t < D) {
+    q[t] = qt;
+    k[t] = kt;
+  }
+  float2 kq = block_sum2(__fmul_rn(kt, qt), 0.f, red);  // also publishes q, k, v
+  return kq.x;
+}
+
 // Loads q, k (key head hv / G) and v (value head hv) of row b as fp32, applies
 // the optional L2 norm and q_scale, and returns k^T q ([P2] 3.1 packed input).
 template <int D>
 __device__ float load_qkv(const DecodeParams &P, int b, int hv, float *q, float *k, float *v,
                           float *red) {
-  const int t = threadIdx.x;
-  const int hk = hv / P.G;
-  const int64_t base = (int64_t)b * P.qkv_stride;
-  float qt = 0.f, kt = 0.f;
-  if (t < D) {
-    qt = load_as_f32(P.qkv, base + (int64_t)hk * D + t, P.qkv_dtype);
-    kt = load_as_f32(P.qkv, base + (int64_t)P.HK * D + (int64_t)hk * D + t, P.qkv_dtype);
-    v[t] = load_as_f32(P.qkv, base + 2 * (int64_t)P.HK * D + (int64_t)hv * D + t, P.qkv_dtype);
-  }
-  if (P.qk_l2norm) {
-    float2 n = block_sum2(qt * qt, kt * kt, red);
-    qt = qt / sqrtf(n.x + 1e-6f);
-    kt = kt / sqrtf(n.y + 1e-6f);
-  }
-  qt *= P.q_scale;
-  if (t < D) {
-    q[t] = qt;
-    k[t] = kt;
-  }
-  float2 kq = block_sum2(kt * qt, 0.f, red);  // also publishes q, k, v
-  return kq.x;
+  return finish_qkv<D>(P, load_qkv_raw<D>(P, b, hv), q, k, v, red);
 }
 
 // ---------------------------------------------------------------------------

@@ -91,6 +91,46 @@ __device__ float stage_replay(const DecodeParams &P, int slot, int hv, int p, fl
   return A;
 }
 
+// The per-token arithmetic of one state row, shared by the packed decode and
+// the lossless verify and commit so that they agree bit for bit: every rounding
+// is pinned (mul.rn / sub.rn / fma.rn; nothing the compiler may contract).
+//
+// token_out: once the row's 8 lanes hold partial sums of S x (x = q, k; KDA
+// a o q, a o k), sums them (xor 1, 2, 4) and forms
+//   GDN: sq, sk <- alpha sq, alpha sk;   d = beta (v_r - sk);   o = sq + d (k^T q).
+template <int GATE>
+__device__ __forceinline__ float token_out(float sq, float sk, float alpha, float beta, float vr, float kq,
+                                           float &d) {
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+  }
+  if (GATE == GDN_GATE_SCALAR) {
+    sq = __fmul_rn(sq, alpha);
+    sk = __fmul_rn(sk, alpha);
+  }
+  d = __fmul_rn(beta, __fsub_rn(vr, sk));
+  return __fmaf_rn(d, kq, sq);
+}
+
+// token_update: four columns of the row after the token,
+//   GDN: s <- fma(d, k, fl(alpha s));   KDA: s <- fma(d, k, fl(s a))
+// (the decayed state is one rounded multiply, the rank-1 update one fma).
+template <int GATE>
+__device__ __forceinline__ float4 token_update(const float4 &s, const float4 &k, const float4 &a, float alpha,
+                                               float d) {
+  if (GATE == GDN_GATE_SCALAR)
+    return make_float4(__fmaf_rn(d, k.x, __fmul_rn(alpha, s.x)), __fmaf_rn(d, k.y, __fmul_rn(alpha, s.y)),
+                       __fmaf_rn(d, k.z, __fmul_rn(alpha, s.z)), __fmaf_rn(d, k.w, __fmul_rn(alpha, s.w)));
+  return make_float4(__fmaf_rn(d, k.x, __fmul_rn(s.x, a.x)), __fmaf_rn(d, k.y, __fmul_rn(s.y, a.y)),
+                     __fmaf_rn(d, k.z, __fmul_rn(s.z, a.z)), __fmaf_rn(d, k.w, __fmul_rn(s.w, a.w)));
+}
+
+__device__ __forceinline__ float4 mul4(const float4 &a, const float4 &b) {
+  return make_float4(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y), __fmul_rn(a.z, b.z), __fmul_rn(a.w, b.w));
+}
+
 // REPLAY = false: packed decode (read S, write S every step).
 // REPLAY = true:  ReplaySSM decode with the replay sum on the CUDA cores.
 // OUT_ONLY (with REPLAY): a non-flush row never forms the replayed state; its
@@ -182,11 +222,12 @@ __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParam
     kraw[m] = reinterpret_cast<const float4 *>(k)[c4];
     qe[m] = reinterpret_cast<const float4 *>(q)[c4];
     ke[m] = kraw[m];
+    a4[m] = A4[m] = make_float4(1.f, 1.f, 1.f, 1.f);
     if (GATE == GDN_GATE_PER_K) {
       a4[m] = reinterpret_cast<const float4 *>(a)[c4];
       A4[m] = reinterpret_cast<const float4 *>(Acol)[c4];
-      qe[m] = make_float4(a4[m].x * qe[m].x, a4[m].y * qe[m].y, a4[m].z * qe[m].z, a4[m].w * qe[m].w);
-      ke[m] = make_float4(a4[m].x * ke[m].x, a4[m].y * ke[m].y, a4[m].z * ke[m].z, a4[m].w * ke[m].w);
+      qe[m] = mul4(a4[m], qe[m]);
+      ke[m] = mul4(a4[m], ke[m]);
     }
   }
 
@@ -251,31 +292,12 @@ __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParam
       sk = dot4(s[m], ke[m], sk);
     }
     }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
-    }
-    if (GATE == GDN_GATE_SCALAR) {
-      sq *= alpha;
-      sk *= alpha;
-    }
-    const float d = beta * (v[r] - sk);
-    const float o = fmaf(d, kq, sq);
+    float d;
+    const float o = token_out<GATE>(sq, sk, alpha, beta, v[r], kq, d);
     if (cg == 0) store_from_f32(P.out, bh * D + r, P.out_dtype, o);
     if (ri.flush) {
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        float4 n;
-        if (GATE == GDN_GATE_SCALAR) {
-          n = make_float4(fmaf(d, kraw[m].x, alpha * s[m].x), fmaf(d, kraw[m].y, alpha * s[m].y),
-                          fmaf(d, kraw[m].z, alpha * s[m].z), fmaf(d, kraw[m].w, alpha * s[m].w));
-        } else {
-          n = make_float4(fmaf(d, kraw[m].x, s[m].x * a4[m].x), fmaf(d, kraw[m].y, s[m].y * a4[m].y),
-                          fmaf(d, kraw[m].z, s[m].z * a4[m].z), fmaf(d, kraw[m].w, s[m].w * a4[m].w));
-        }
-        S[r * (D / 4) + 8 * m + cg] = n;
-      }
+      for (int m = 0; m < M; ++m) S[r * (D / 4) + 8 * m + cg] = token_update<GATE>(s[m], kraw[m], a4[m], alpha, d);
     } else if (cg == 0) {
       store_from_f32(P.ring_d, (((int64_t)slot * P.HV + hv) * P.L + p) * D + r, P.ring_dtype, d);
     }
@@ -509,6 +531,226 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const DecodeParam
   }
 }
 
+// Lossless speculative verify ([P5] The idea; Modifications, Verify kernel):
+// row b's T tokens (input rows b*T + t) run the packed decode's recurrence from
+// the checkpoint, token after token, with the packed decode's lane layout and
+// its pinned arithmetic (finish_qkv, token_out, token_update), so token t's
+// output and correction are bit-identical to those of the t-th of T successive
+// gdn_packed_decode calls.  No state is written: each token's correction u,
+// key k and log-gate g go to fp32 tuple buffers instead
+//   tup_u [B, T, HV, V],  tup_k [B, T, HK, K] (one writer per key head),
+//   tup_g [B, T, HV] (KDA [B, T, HV, K]).
+// State rows evolve independently, so each is carried through the window in
+// registers; the window's inputs sit in shared memory.
+template <int D, int GATE>
+__global__ void __launch_bounds__(kThreads) lossless_verify_kernel(const DecodeParams P, float *tup_u,
+                                                                   float *tup_k, float *tup_g) {
+  constexpr int M = D / 32;
+  constexpr int ROWS_PER_WARP = D / 4;
+  constexpr int NIT = ROWS_PER_WARP / 4;
+  const int b = blockIdx.x / P.HV, hv = blockIdx.x % P.HV;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int rg = lane >> 3, cg = lane & 7;
+  const int T = P.T;
+  extern __shared__ float4 smem_f4[];
+  // per token [T][D]: readout vectors x_q, x_k (KDA a o q, a o k), key, gate a (KDA), v;
+  // scalars [T][4]: alpha, beta, k.q; then one token's q, k, v and the reduction scratch
+  float *wq = reinterpret_cast<float *>(smem_f4);
+  float *wke = wq + T * D, *wk = wke + T * D, *wa = wk + T * D, *wv = wa + T * D, *wsc = wv + T * D;
+  float *q = wsc + 4 * T, *k = q + D, *v = k + D, *red = v + D;
+
+  const int slot = P.idx[b];
+  if (slot >= P.N && hv == 0 && t == 0) set_status(P.status, GDN_DEV_BAD_SLOT);
+  if (slot < 0 || slot >= P.N) {  // padding row: zeros for every token, tuples untouched
+    for (int tok = 0; tok < T; ++tok)
+      if (t < D) store_from_f32(P.out, (((int64_t)b * T + tok) * P.HV + hv) * D + t, P.out_dtype, 0.f);
+    return;
+  }
+  const int hk = hv / P.G;
+
+  // the checkpoint's first rows are requested before the window's inputs
+  const float4 *S = reinterpret_cast<const float4 *>(P.state + ((int64_t)slot * P.HV + hv) * D * D);
+  float4 cur[M], nxt[M];
+  {
+    const int r0 = warp * ROWS_PER_WARP + rg;
+#pragma unroll
+    for (int m = 0; m < M; ++m) cur[m] = S[r0 * (D / 4) + 8 * m + cg];
+  }
+
+  // window inputs: kStageBatch tokens' loads in flight at once, then each
+  // token finished as the packed decode finishes its single token
+  for (int tok0 = 0; tok0 < T; tok0 += kStageBatch) {
+    QkvRaw raw[kStageBatch];
+    float graw[kStageBatch], braw[kStageBatch];
+#pragma unroll
+    for (int u = 0; u < kStageBatch; ++u) {
+      raw[u] = QkvRaw{0.f, 0.f, 0.f};
+      graw[u] = braw[u] = 0.f;
+      const int tok = tok0 + u;
+      if (tok < T) {
+        const int64_t bh = ((int64_t)b * T + tok) * P.HV + hv;
+        raw[u] = load_qkv_raw<D>(P, b * T + tok, hv);
+        graw[u] = GATE == GDN_GATE_PER_K ? (t < D ? P.g[bh * D + t] : 0.f) : P.g[bh];
+        braw[u] = P.beta[bh];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kStageBatch; ++u) {
+      const int tok = tok0 + u;
+      if (tok < T) {
+        const int64_t row = (int64_t)b * T + tok;
+        const float kq = finish_qkv<D>(P, raw[u], q, k, v, red);
+        if (t < D) {
+          const float a = GATE == GDN_GATE_PER_K ? expf(graw[u]) : 1.f;
+          wq[tok * D + t] = GATE == GDN_GATE_PER_K ? __fmul_rn(a, q[t]) : q[t];
+          wke[tok * D + t] = GATE == GDN_GATE_PER_K ? __fmul_rn(a, k[t]) : k[t];
+          wk[tok * D + t] = k[t];
+          wa[tok * D + t] = a;
+          wv[tok * D + t] = v[t];
+          if (hv % P.G == 0) tup_k[(row * P.HK + hk) * D + t] = k[t];
+          if (GATE == GDN_GATE_PER_K) tup_g[(row * P.HV + hv) * D + t] = graw[u];
+        }
+        if (t == 0) {
+          wsc[4 * tok + 0] = GATE == GDN_GATE_SCALAR ? expf(graw[u]) : 1.f;
+          wsc[4 * tok + 1] = braw[u];
+          wsc[4 * tok + 2] = kq;
+          if (GATE == GDN_GATE_SCALAR) tup_g[row * P.HV + hv] = graw[u];
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+#pragma unroll 1
+  for (int it = 0; it < NIT; ++it) {
+    const int r = warp * ROWS_PER_WARP + it * 4 + rg;
+    if (it + 1 < NIT) {
+#pragma unroll
+      for (int m = 0; m < M; ++m) nxt[m] = S[(r + 4) * (D / 4) + 8 * m + cg];
+    }
+    for (int tok = 0; tok < T; ++tok) {
+      const float alpha = wsc[4 * tok], beta = wsc[4 * tok + 1], kq = wsc[4 * tok + 2];
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const int c4 = 8 * m + cg;
+        sq = dot4(cur[m], reinterpret_cast<const float4 *>(wq + tok * D)[c4], sq);
+        sk = dot4(cur[m], reinterpret_cast<const float4 *>(wke + tok * D)[c4], sk);
+      }
+      float d;
+      const float o = token_out<GATE>(sq, sk, alpha, beta, wv[tok * D + r], kq, d);
+      const int64_t orow = ((int64_t)b * T + tok) * P.HV + hv;
+      if (cg == 0) {
+        store_from_f32(P.out, orow * D + r, P.out_dtype, o);
+        tup_u[orow * D + r] = d;
+      }
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const int c4 = 8 * m + cg;
+        const float4 kr = reinterpret_cast<const float4 *>(wk + tok * D)[c4];
+        const float4 a4 = reinterpret_cast<const float4 *>(wa + tok * D)[c4];
+        cur[m] = token_update<GATE>(cur[m], kr, a4, alpha, d);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) cur[m] = nxt[m];
+  }
+}
+
+// Exact-order commit ([P5] Modifications, Commit): row b's first a =
+// accepted[b] tuples are replayed from state[src], src = ssm_state_indices[b],
+// with the packed decode's own update (token_update: fl(alpha s), then one fma
+// per element), and the result is stored at state[dst], dst = dst_idx[b] (src
+// when dst_idx is null).  The state is therefore bit-identical to the one a
+// successive gdn_packed_decode calls leave.  Rows with a negative src, dst or
+// a are skipped; src or dst >= N and a > T are reported and skipped.
+template <int D, int GATE>
+__global__ void __launch_bounds__(kThreads) lossless_commit_kernel(const DecodeParams P, const int32_t *dst_idx,
+                                                                   const int32_t *accepted, const float *tup_u,
+                                                                   const float *tup_k, const float *tup_g) {
+  constexpr int M = D / 32;
+  constexpr int ROWS_PER_WARP = D / 4;
+  const int b = blockIdx.x / P.HV, hv = blockIdx.x % P.HV;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int rg = lane >> 3, cg = lane & 7;
+  const int T = P.T;
+  extern __shared__ float4 smem_f4[];
+  float *wk = reinterpret_cast<float *>(smem_f4);  // [T][D] keys
+  float *wu = wk + T * D, *wa = wu + T * D;        // [T][D] corrections, [T][D] KDA gates
+  float *walpha = wa + T * D;                      // [T] GDN decays
+
+  const int src = P.idx[b], dst = dst_idx ? dst_idx[b] : src, a = accepted[b];
+  if (src < 0 || dst < 0 || a < 0) return;
+  if (src >= P.N || dst >= P.N) {
+    if (hv == 0 && t == 0) set_status(P.status, GDN_DEV_BAD_SLOT);
+    return;
+  }
+  if (a > T) {
+    if (hv == 0 && t == 0) set_status(P.status, GDN_DEV_BAD_ACCEPTED);
+    return;
+  }
+  if (a == 0 && dst == src) return;  // nothing to replay, nothing moves
+  const int hk = hv / P.G;
+  const float4 *S = reinterpret_cast<const float4 *>(P.state + ((int64_t)src * P.HV + hv) * D * D);
+  float4 *Sd = reinterpret_cast<float4 *>(P.state + ((int64_t)dst * P.HV + hv) * D * D);
+  float4 cur[M];
+  {
+    const int r0 = warp * ROWS_PER_WARP + rg;
+#pragma unroll
+    for (int m = 0; m < M; ++m) cur[m] = S[r0 * (D / 4) + 8 * m + cg];
+  }
+  // the accepted tuples, kStageBatch tokens' loads in flight at once
+  if (t < D) {
+    for (int tok0 = 0; tok0 < a; tok0 += kStageBatch) {
+      float ku[kStageBatch], uu[kStageBatch], gg[kStageBatch];
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        ku[u] = uu[u] = gg[u] = 0.f;
+        const int64_t row = (int64_t)b * T + tok0 + u;
+        if (tok0 + u < a) {
+          ku[u] = tup_k[(row * P.HK + hk) * D + t];
+          uu[u] = tup_u[(row * P.HV + hv) * D + t];
+          gg[u] = GATE == GDN_GATE_PER_K ? tup_g[(row * P.HV + hv) * D + t] : tup_g[row * P.HV + hv];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int tok = tok0 + u;
+        if (tok < a) {
+          wk[tok * D + t] = ku[u];
+          wu[tok * D + t] = uu[u];
+          wa[tok * D + t] = GATE == GDN_GATE_PER_K ? expf(gg[u]) : 1.f;
+          if (GATE == GDN_GATE_SCALAR && t == 0) walpha[tok] = expf(gg[u]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int it = 0; it < ROWS_PER_WARP / 4; ++it) {
+    const int r = warp * ROWS_PER_WARP + it * 4 + rg;
+    float4 nxt[M];
+    if (it + 1 < ROWS_PER_WARP / 4) {
+#pragma unroll
+      for (int m = 0; m < M; ++m) nxt[m] = S[(r + 4) * (D / 4) + 8 * m + cg];
+    }
+    for (int tok = 0; tok < a; ++tok) {
+      const float d = wu[tok * D + r];
+      const float alpha = GATE == GDN_GATE_SCALAR ? walpha[tok] : 1.f;
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const int c4 = 8 * m + cg;
+        cur[m] = token_update<GATE>(cur[m], reinterpret_cast<const float4 *>(wk + tok * D)[c4],
+                                    reinterpret_cast<const float4 *>(wa + tok * D)[c4], alpha, d);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      Sd[r * (D / 4) + 8 * m + cg] = cur[m];
+      cur[m] = nxt[m];
+    }
+  }
+}
+
 // Commit after verification ([P3] "rollback is a cursor move"): the cursor
 // moves over the accepted tokens only; a slot whose next window would not fit
 // (p + a + T > L - 1) is listed in flush_slots (else -1) for a fold.
@@ -640,6 +882,51 @@ static cudaError_t launch_spec_t(const DecodeParams &P, cudaStream_t s) {
 cudaError_t launch_spec_verify(const DecodeParams &P, int D, int gate, cudaStream_t s) {
   if (D == 128) return gate == GDN_GATE_SCALAR ? launch_spec_t<128, 0>(P, s) : launch_spec_t<128, 1>(P, s);
   return gate == GDN_GATE_SCALAR ? launch_spec_t<64, 0>(P, s) : launch_spec_t<64, 1>(P, s);
+}
+
+template <int D, int GATE>
+static cudaError_t launch_lossless_verify_t(const DecodeParams &P, float *tu, float *tk, float *tg,
+                                            cudaStream_t s) {
+  const size_t smem = (5 * (size_t)P.T * D + 4 * (size_t)P.T + 3 * (size_t)D + 8) * sizeof(float);
+  auto kern = lossless_verify_kernel<D, GATE>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)P.B * P.HV, kThreads, smem, s>>>(P, tu, tk, tg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lossless_verify(const DecodeParams &P, int D, int gate, float *tup_u, float *tup_k,
+                                   float *tup_g, cudaStream_t s) {
+  if (D == 128)
+    return gate == GDN_GATE_SCALAR ? launch_lossless_verify_t<128, 0>(P, tup_u, tup_k, tup_g, s)
+                                   : launch_lossless_verify_t<128, 1>(P, tup_u, tup_k, tup_g, s);
+  return gate == GDN_GATE_SCALAR ? launch_lossless_verify_t<64, 0>(P, tup_u, tup_k, tup_g, s)
+                                 : launch_lossless_verify_t<64, 1>(P, tup_u, tup_k, tup_g, s);
+}
+
+template <int D, int GATE>
+static cudaError_t launch_lossless_commit_t(const DecodeParams &P, const int32_t *dst, const int32_t *acc,
+                                            const float *tu, const float *tk, const float *tg, cudaStream_t s) {
+  const size_t smem = (3 * (size_t)P.T * D + (size_t)P.T) * sizeof(float);
+  auto kern = lossless_commit_kernel<D, GATE>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)P.B * P.HV, kThreads, smem, s>>>(P, dst, acc, tu, tk, tg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lossless_commit(const DecodeParams &P, int D, int gate, const int32_t *dst_idx,
+                                   const int32_t *accepted, const float *tup_u, const float *tup_k,
+                                   const float *tup_g, cudaStream_t s) {
+  if (D == 128)
+    return gate == GDN_GATE_SCALAR ? launch_lossless_commit_t<128, 0>(P, dst_idx, accepted, tup_u, tup_k, tup_g, s)
+                                   : launch_lossless_commit_t<128, 1>(P, dst_idx, accepted, tup_u, tup_k, tup_g, s);
+  return gate == GDN_GATE_SCALAR ? launch_lossless_commit_t<64, 0>(P, dst_idx, accepted, tup_u, tup_k, tup_g, s)
+                                 : launch_lossless_commit_t<64, 1>(P, dst_idx, accepted, tup_u, tup_k, tup_g, s);
 }
 
 cudaError_t launch_spec_commit(const int32_t *idx, const int32_t *accepted, int B, int T, int N, int L,

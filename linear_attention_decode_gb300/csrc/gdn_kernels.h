@@ -43,6 +43,14 @@ cudaError_t launch_spec_tc(const DecodeParams &P, int D, int gate, cudaStream_t 
 cudaError_t launch_spec_commit(const int32_t *idx, const int32_t *accepted, int B, int T, int N, int L,
                                int32_t *write_pos, int32_t *flush_slots, uint32_t *status, cudaStream_t s);
 
+// Lossless verify (P.T tokens per row, no state update, fp32 (u, k, g) tuples)
+// and the exact-order commit that replays accepted tuples into the state.
+cudaError_t launch_lossless_verify(const DecodeParams &P, int D, int gate, float *tup_u, float *tup_k,
+                                   float *tup_g, cudaStream_t s);
+cudaError_t launch_lossless_commit(const DecodeParams &P, int D, int gate, const int32_t *dst_idx,
+                                   const int32_t *accepted, const float *tup_u, const float *tup_k,
+                                   const float *tup_g, cudaStream_t s);
+
 cudaError_t launch_advance(const int32_t *idx, int B, const uint8_t *ff, int N, int L,
                            int32_t *write_pos, uint32_t *status, cudaStream_t s);
 

@@ -156,3 +156,27 @@ def test_status_bits_match_the_header():
     bits = {n: int(v) for n, v in re.findall(r"#define GDN_(DEV_\w+)\s+(\d+)u", text)}
     for n in ("DEV_BAD_SLOT", "DEV_BAD_WRITE_POS", "DEV_TIMEOUT", "DEV_INTERNAL", "DEV_BAD_ACCEPTED"):
         assert bits[n] == getattr(Bd, n), n
+
+
+def test_lossless_verify_and_commit_check_their_arguments(lib):
+    d = _desc()
+    v = lib.gdn_lossless_verify
+    # window 0, window 33, short row, negative batch, no state, misaligned state, no tuples:
+    # rejected before any launch
+    cases = ((_spec_step(window=0), 0x1000, 0x1000, 1), (_spec_step(window=33), 0x1000, 0x1000, 2),
+             (_spec_step(row=100), 0x1000, 0x1000, 1), (_spec_step(batch=-1), 0x1000, 0x1000, 1),
+             (_spec_step(), None, 0x1000, 1), (_spec_step(), 0x1004, 0x1000, 1), (_spec_step(), 0x1000, None, 1))
+    for step, state, tup, code in cases:
+        assert v(ctypes.byref(d), state, ctypes.byref(step), tup, 0x1000, 0x1000, None, None) == code, \
+            lib.gdn_last_error().decode()
+    # the lossless path keeps no ring: a window longer than ring_len is fine (checked, not launched: batch 0)
+    assert v(ctypes.byref(_desc(ring_len=1)), 0x1000, ctypes.byref(_spec_step(batch=0, window=8)),
+             0x1000, 0x1000, 0x1000, None, None) == 0
+    c = lib.gdn_lossless_commit
+    assert c(ctypes.byref(d), None, None, None, None, 0, 4, None, None, None, None, None) == 0   # empty
+    assert c(ctypes.byref(d), 0x1000, 0x1000, None, None, 4, 4, 0x1000, 0x1000, 0x1000, None, None) == 1  # no accepted
+    assert c(ctypes.byref(d), 0x1000, 0x1000, None, 0x1000, 4, 0, 0x1000, 0x1000, 0x1000, None, None) == 1  # window 0
+    assert c(ctypes.byref(d), 0x1000, 0x1000, None, 0x1000, 4, 33, 0x1000, 0x1000, 0x1000, None, None) == 2
+    assert c(ctypes.byref(d), 0x1008, 0x1000, None, 0x1000, 4, 4, 0x1000, 0x1000, 0x1000, None, None) == 1  # misaligned
+    assert c(ctypes.byref(_desc(num_k_heads=5)), 0x1000, 0x1000, None, 0x1000, 4, 4, 0x1000, 0x1000, 0x1000,
+             None, None) == 1
