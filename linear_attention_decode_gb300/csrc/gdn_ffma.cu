@@ -117,14 +117,35 @@ __device__ __forceinline__ float token_out(float sq, float sk, float alpha, floa
 // token_update: four columns of the row after the token,
 //   GDN: s <- fma(d, k, fl(alpha s));   KDA: s <- fma(d, k, fl(s a))
 // (the decayed state is one rounded multiply, the rank-1 update one fma).
+// Packed fp32x2 operations round each element exactly as mul.rn / fma.rn do.
 template <int GATE>
 __device__ __forceinline__ float4 token_update(const float4 &s, const float4 &k, const float4 &a, float alpha,
                                                float d) {
-  if (GATE == GDN_GATE_SCALAR)
-    return make_float4(__fmaf_rn(d, k.x, __fmul_rn(alpha, s.x)), __fmaf_rn(d, k.y, __fmul_rn(alpha, s.y)),
-                       __fmaf_rn(d, k.z, __fmul_rn(alpha, s.z)), __fmaf_rn(d, k.w, __fmul_rn(alpha, s.w)));
-  return make_float4(__fmaf_rn(d, k.x, __fmul_rn(s.x, a.x)), __fmaf_rn(d, k.y, __fmul_rn(s.y, a.y)),
-                     __fmaf_rn(d, k.z, __fmul_rn(s.z, a.z)), __fmaf_rn(d, k.w, __fmul_rn(s.w, a.w)));
+  const float2 dd = make_float2(d, d);
+  float2 lo, hi;
+  if (GATE == GDN_GATE_SCALAR) {
+    const float2 aa = make_float2(alpha, alpha);
+    lo = __ffma2_rn(dd, make_float2(k.x, k.y), __fmul2_rn(aa, make_float2(s.x, s.y)));
+    hi = __ffma2_rn(dd, make_float2(k.z, k.w), __fmul2_rn(aa, make_float2(s.z, s.w)));
+  } else {
+    lo = __ffma2_rn(dd, make_float2(k.x, k.y), __fmul2_rn(make_float2(s.x, s.y), make_float2(a.x, a.y)));
+    hi = __ffma2_rn(dd, make_float2(k.z, k.w), __fmul2_rn(make_float2(s.z, s.w), make_float2(a.z, a.w)));
+  }
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// This lane's partial sum of a state row against x over its M float4 column
+// chunks: one fma chain per float4 component (m ascending; two packed fp32x2
+// chains), the four chains added pairwise.  Short chains, pinned order.
+template <int M>
+__device__ __forceinline__ float lane_dot(const float4 (&s)[M], const float4 (&x)[M]) {
+  float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    lo = __ffma2_rn(make_float2(s[m].x, s[m].y), make_float2(x[m].x, x[m].y), lo);
+    hi = __ffma2_rn(make_float2(s[m].z, s[m].w), make_float2(x[m].z, x[m].w), hi);
+  }
+  return __fadd_rn(__fadd_rn(lo.x, lo.y), __fadd_rn(hi.x, hi.y));
 }
 
 __device__ __forceinline__ float4 mul4(const float4 &a, const float4 &b) {
@@ -286,11 +307,8 @@ __global__ void __launch_bounds__(kThreads) ffma_decode_kernel(const DecodeParam
         }
       }
     }
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-      sq = dot4(s[m], qe[m], sq);
-      sk = dot4(s[m], ke[m], sk);
-    }
+    sq = lane_dot<M>(s, qe);
+    sk = lane_dot<M>(s, ke);
     }
     float d;
     const float o = token_out<GATE>(sq, sk, alpha, beta, v[r], kq, d);
@@ -540,14 +558,16 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const DecodeParam
 // key k and log-gate g go to fp32 tuple buffers instead
 //   tup_u [B, T, HV, V],  tup_k [B, T, HK, K] (one writer per key head),
 //   tup_g [B, T, HV] (KDA [B, T, HV, K]).
-// State rows evolve independently, so each is carried through the window in
-// registers; the window's inputs sit in shared memory.
-template <int D, int GATE>
+// State rows evolve independently: a thread keeps RG groups of its rows in
+// registers for the whole window (token loop outside, row loop inside), so each
+// token's readout vectors are read from shared memory once per pass.
+template <int D, int GATE, int RG>
 __global__ void __launch_bounds__(kThreads) lossless_verify_kernel(const DecodeParams P, float *tup_u,
                                                                    float *tup_k, float *tup_g) {
   constexpr int M = D / 32;
   constexpr int ROWS_PER_WARP = D / 4;
   constexpr int NIT = ROWS_PER_WARP / 4;
+  static_assert(NIT % RG == 0, "row groups per pass must divide the row groups of a warp");
   const int b = blockIdx.x / P.HV, hv = blockIdx.x % P.HV;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int rg = lane >> 3, cg = lane & 7;
@@ -567,14 +587,15 @@ __global__ void __launch_bounds__(kThreads) lossless_verify_kernel(const DecodeP
     return;
   }
   const int hk = hv / P.G;
-
-  // the checkpoint's first rows are requested before the window's inputs
   const float4 *S = reinterpret_cast<const float4 *>(P.state + ((int64_t)slot * P.HV + hv) * D * D);
-  float4 cur[M], nxt[M];
-  {
-    const int r0 = warp * ROWS_PER_WARP + rg;
+
+  // the first pass's rows are requested before the window's inputs
+  float4 st[RG][M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) cur[m] = S[r0 * (D / 4) + 8 * m + cg];
+  for (int i = 0; i < RG; ++i) {
+    const int r = warp * ROWS_PER_WARP + i * 4 + rg;
+#pragma unroll
+    for (int m = 0; m < M; ++m) st[i][m] = S[r * (D / 4) + 8 * m + cg];
   }
 
   // window inputs: kStageBatch tokens' loads in flight at once, then each
@@ -622,38 +643,44 @@ __global__ void __launch_bounds__(kThreads) lossless_verify_kernel(const DecodeP
   __syncthreads();
 
 #pragma unroll 1
-  for (int it = 0; it < NIT; ++it) {
-    const int r = warp * ROWS_PER_WARP + it * 4 + rg;
-    if (it + 1 < NIT) {
+  for (int pass = 0; pass < NIT / RG; ++pass) {
+    if (pass > 0) {
 #pragma unroll
-      for (int m = 0; m < M; ++m) nxt[m] = S[(r + 4) * (D / 4) + 8 * m + cg];
+      for (int i = 0; i < RG; ++i) {
+        const int r = warp * ROWS_PER_WARP + (pass * RG + i) * 4 + rg;
+#pragma unroll
+        for (int m = 0; m < M; ++m) st[i][m] = S[r * (D / 4) + 8 * m + cg];
+      }
     }
+#pragma unroll 1
     for (int tok = 0; tok < T; ++tok) {
       const float alpha = wsc[4 * tok], beta = wsc[4 * tok + 1], kq = wsc[4 * tok + 2];
-      float sq = 0.f, sk = 0.f;
+      float4 xq[M], xk[M], kr[M], a4[M];
 #pragma unroll
       for (int m = 0; m < M; ++m) {
         const int c4 = 8 * m + cg;
-        sq = dot4(cur[m], reinterpret_cast<const float4 *>(wq + tok * D)[c4], sq);
-        sk = dot4(cur[m], reinterpret_cast<const float4 *>(wke + tok * D)[c4], sk);
+        xq[m] = reinterpret_cast<const float4 *>(wq + tok * D)[c4];
+        xk[m] = reinterpret_cast<const float4 *>(wke + tok * D)[c4];
+        kr[m] = reinterpret_cast<const float4 *>(wk + tok * D)[c4];
+        a4[m] = GATE == GDN_GATE_PER_K ? reinterpret_cast<const float4 *>(wa + tok * D)[c4]
+                                       : make_float4(1.f, 1.f, 1.f, 1.f);
       }
-      float d;
-      const float o = token_out<GATE>(sq, sk, alpha, beta, wv[tok * D + r], kq, d);
       const int64_t orow = ((int64_t)b * T + tok) * P.HV + hv;
-      if (cg == 0) {
-        store_from_f32(P.out, orow * D + r, P.out_dtype, o);
-        tup_u[orow * D + r] = d;
-      }
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        const int c4 = 8 * m + cg;
-        const float4 kr = reinterpret_cast<const float4 *>(wk + tok * D)[c4];
-        const float4 a4 = reinterpret_cast<const float4 *>(wa + tok * D)[c4];
-        cur[m] = token_update<GATE>(cur[m], kr, a4, alpha, d);
+      for (int i = 0; i < RG; ++i) {
+        const int r = warp * ROWS_PER_WARP + (pass * RG + i) * 4 + rg;
+        const float sq = lane_dot<M>(st[i], xq);
+        const float sk = lane_dot<M>(st[i], xk);
+        float d;
+        const float o = token_out<GATE>(sq, sk, alpha, beta, wv[tok * D + r], kq, d);
+        if (cg == 0) {
+          store_from_f32(P.out, orow * D + r, P.out_dtype, o);
+          tup_u[orow * D + r] = d;
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) st[i][m] = token_update<GATE>(st[i][m], kr[m], a4[m], alpha, d);
       }
     }
-#pragma unroll
-    for (int m = 0; m < M; ++m) cur[m] = nxt[m];
   }
 }
 
@@ -884,11 +911,18 @@ cudaError_t launch_spec_verify(const DecodeParams &P, int D, int gate, cudaStrea
   return gate == GDN_GATE_SCALAR ? launch_spec_t<64, 0>(P, s) : launch_spec_t<64, 1>(P, s);
 }
 
+// Row groups of four rows a verify thread keeps in registers at once (of 8 for K = 128;
+// two measured fastest: more raise the registers per thread and cut occupancy).
+#ifndef GDN_VERIFY_ROW_GROUPS
+#define GDN_VERIFY_ROW_GROUPS 2
+#endif
+constexpr int kVerifyRowGroups = GDN_VERIFY_ROW_GROUPS;
+
 template <int D, int GATE>
 static cudaError_t launch_lossless_verify_t(const DecodeParams &P, float *tu, float *tk, float *tg,
                                             cudaStream_t s) {
   const size_t smem = (5 * (size_t)P.T * D + 4 * (size_t)P.T + 3 * (size_t)D + 8) * sizeof(float);
-  auto kern = lossless_verify_kernel<D, GATE>;
+  auto kern = lossless_verify_kernel<D, GATE, (D == 128 ? kVerifyRowGroups : 4)>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
