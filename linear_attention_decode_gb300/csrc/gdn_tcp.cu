@@ -724,6 +724,25 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (2 groups)
+    // Decode + advance with one row per thread ([P1] Design 3): every CTA has
+    // read its cursors by the end of the dealing, so the last CTA to get past
+    // it may advance them at once.  The first epilogue warp does it while it
+    // waits for its first item, off the launch's tail.
+    if (warp == 9 && P.sync && P.B <= kTcpThreads) {
+      uint32_t last = 0u;
+      if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(P.sync, 1u) == (uint32_t)(G - 1) ? 1u : 0u;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        __threadfence();
+        for (int b = lane; b < P.B; b += 32) {
+          const int q = advq[b];
+          if (q >= 0) P.write_pos_w[q >> 7] = q & 127;
+        }
+        if (lane == 0) *P.sync = 0u;  // every CTA of this launch has counted
+      }
+    }
     // Group eg takes the items with li % 2 == eg and reads TMEM accumulator
     // 2 eg + (li / 2) % 2.
     const int eg = (warp - 9) >> 2;
@@ -890,10 +909,11 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     tmem_dealloc(tmem, 4 * D);
   }
 
-  // Decode + advance ([P1] Design 3): every CTA read the cursors while dealing,
-  // long before it got here; the last CTA to finish advances them and leaves
-  // the counter at zero for the next launch.  No CTA waits for another.
-  if (P.sync) {
+  // Decode + advance with more rows than threads ([P1] Design 3): every CTA
+  // read the cursors while dealing, long before it got here; the last CTA to
+  // finish advances them and leaves the counter at zero for the next launch.
+  // No CTA waits for another.
+  if (P.sync && P.B > kTcpThreads) {
     if (tid == 0) {
       __threadfence();
       misc[7] = atomicAdd(P.sync, 1u) == (uint32_t)(G - 1) ? 1u : 0u;
@@ -901,16 +921,9 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     __syncthreads();
     if (misc[7]) {
       __threadfence();
-      if (P.B <= kTcpThreads) {
-        if (tid < P.B) {
-          const int q = advq[tid];
-          if (q >= 0) P.write_pos_w[q >> 7] = q & 127;
-        }
-      } else {
-        for (int b = tid; b < P.B; b += kTcpThreads) {
-          const RowInfo ri = resolve_row(P, b, false);
-          if (ri.live) P.write_pos_w[ri.slot] = ri.flush ? 0 : ri.p + 1;
-        }
+      for (int b = tid; b < P.B; b += kTcpThreads) {
+        const RowInfo ri = resolve_row(P, b, false);
+        if (ri.live) P.write_pos_w[ri.slot] = ri.flush ? 0 : ri.p + 1;
       }
       if (tid == 0) *P.sync = 0u;
     }
