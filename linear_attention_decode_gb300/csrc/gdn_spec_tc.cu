@@ -451,11 +451,15 @@ __global__ void __launch_bounds__(kThreadsSpec, 1) spec_tc_kernel(const DecodePa
           store_from_f32(P.ring_k, (krow * P.L + p + t) * D + r, P.ring_dtype, k[t]);
       }
 
-      // 3. staged entries landed (the barrier also publishes the GDN gates)
+      // 3. the committed gates are in shared memory (the barrier publishes the
+      // GDN gates; KDA's come with the staged copies).  A GDN group waits for
+      // the staged corrections and keys only where it first reads them (the
+      // committed dot products), so its operand for the contraction, which
+      // needs only the gates, is not held up by those copies.
       bool ok = true;
-      if (p > 0) ok = wait_or_abort(ringbar, ringph, abort_flag);
+      if (GATE == GDN_GATE_PER_K && p > 0) ok = wait_or_abort(ringbar, ringph, abort_flag);
       if (named_bar_or(bar_id, 128, !ok)) break;
-      if (p > 0) {
+      if (GATE == GDN_GATE_PER_K && p > 0) {
         ringph ^= 1u;
         ring_pending = false;
       }
@@ -508,6 +512,12 @@ __global__ void __launch_bounds__(kThreadsSpec, 1) spec_tc_kernel(const DecodePa
           const float s = warp_reduce_scatter<NCOL>(v, lane);
           if (lane < NCOL) part[wq * pstride + (1 + i2) * NCOL + lane] = s;
         }
+      }
+      if (GATE == GDN_GATE_SCALAR && p > 0) {  // the staged corrections and keys
+        ok = wait_or_abort(ringbar, ringph, abort_flag);
+        if (named_bar_or(bar_id, 128, !ok)) break;
+        ringph ^= 1u;
+        ring_pending = false;
       }
       {  // batches T + j: committed entry j, weight w_j = prod_{j<i<p} a_i
         float s = 0.f;
@@ -618,6 +628,12 @@ static cudaError_t launch_spec_tc_t(const DecodeParams &P, const CUtensorMap &ma
   return cudaGetLastError();
 }
 
+// Checkpoint box slots (16 KB each, four per item) when shared memory allows.
+#ifndef GDN_SPEC_BOX_SLOTS
+#define GDN_SPEC_BOX_SLOTS 8
+#endif
+constexpr int kSpecBoxSlots = GDN_SPEC_BOX_SLOTS;
+
 cudaError_t launch_spec_tc(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why) {
   static const int sms = spec_device_attr(cudaDevAttrMultiProcessorCount);
   static const int optin = spec_device_attr(cudaDevAttrMaxSharedMemoryPerBlockOptin);
@@ -630,7 +646,7 @@ cudaError_t launch_spec_tc(const DecodeParams &P, int D, int gate, cudaStream_t 
   const int items = P.B * P.HV;
   const int grid = sms > 0 && sms < items ? sms : items;
   const int cap = (items + grid - 1) / grid;
-  SpecLayout lay = spec_layout(P.T, P.L, ncol, 8, rb, gate, cap);
+  SpecLayout lay = spec_layout(P.T, P.L, ncol, kSpecBoxSlots, rb, gate, cap);
   while (lay.NB > 4 && lay.total > (uint32_t)optin) lay = spec_layout(P.T, P.L, ncol, lay.NB - 1, rb, gate, cap);
   if (lay.total > (uint32_t)optin) return cudaErrorNotSupported;
   CUtensorMap map;
