@@ -601,16 +601,16 @@ __global__ void __launch_bounds__(kThreads) lossless_verify_kernel(const DecodeP
   // window inputs: kStageBatch tokens' loads in flight at once, then each
   // token finished as the packed decode finishes its single token
   for (int tok0 = 0; tok0 < T; tok0 += kStageBatch) {
-    QkvRaw raw[kStageBatch];
+    QkvBits raw[kStageBatch];
     float graw[kStageBatch], braw[kStageBatch];
 #pragma unroll
     for (int u = 0; u < kStageBatch; ++u) {
-      raw[u] = QkvRaw{0.f, 0.f, 0.f};
+      raw[u] = QkvBits{0u, 0u, 0u};
       graw[u] = braw[u] = 0.f;
       const int tok = tok0 + u;
       if (tok < T) {
         const int64_t bh = ((int64_t)b * T + tok) * P.HV + hv;
-        raw[u] = load_qkv_raw<D>(P, b * T + tok, hv);
+        raw[u] = load_qkv_bits<D>(P, b * T + tok, hv);
         graw[u] = GATE == GDN_GATE_PER_K ? (t < D ? P.g[bh * D + t] : 0.f) : P.g[bh];
         braw[u] = P.beta[bh];
       }
@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(kThreads) lossless_verify_kernel(const DecodeP
       const int tok = tok0 + u;
       if (tok < T) {
         const int64_t row = (int64_t)b * T + tok;
-        const float kq = finish_qkv<D>(P, raw[u], q, k, v, red);
+        const float kq = finish_qkv<D>(P, qkv_from_bits(raw[u], P.qkv_dtype), q, k, v, red);
         if (t < D) {
           const float a = GATE == GDN_GATE_PER_K ? expf(graw[u]) : 1.f;
           wq[tok * D + t] = GATE == GDN_GATE_PER_K ? __fmul_rn(a, q[t]) : q[t];

@@ -376,7 +376,10 @@ __global__ void __launch_bounds__(kThreadsSpec, 1) spec_tc_kernel(const DecodePa
       const int64_t hrow = (int64_t)slot * P.HV + hv;
       const int64_t krow = (int64_t)slot * P.HK + hk;
 
-      // 1. the committed entries j < p, staged by bulk copies (one round trip)
+      // 1. the committed entries j < p, staged by bulk copies (one round trip);
+      // a GDN group's committed gates go through registers and reach shared
+      // memory only after the window loads below have been issued
+      float gate_r = 0.f;
       if (p > 0) {
         if (r == 0) {
           const uint32_t bytes = 2u * p * row_bytes + (GATE == GDN_GATE_PER_K ? (uint32_t)p * D * 4u : 0u);
@@ -388,25 +391,34 @@ __global__ void __launch_bounds__(kThreadsSpec, 1) spec_tc_kernel(const DecodePa
           if (GATE == GDN_GATE_PER_K)
             bulk_load(smem_addr(gst), P.ring_g + hrow * P.L * D, (uint32_t)p * D * 4u, ringbar);
         }
-        if (GATE == GDN_GATE_SCALAR && r < p) gst[r] = P.ring_g[hrow * P.L + r];
+        if (GATE == GDN_GATE_SCALAR && r < p) gate_r = P.ring_g[hrow * P.L + r];
         ring_pending = true;
       }
 
-      // 2. window inputs of channel r: every load first, then the stores
+      // 2. window inputs of channel r: every load first (raw bits, so none waits
+      // for the one before), then the conversions and the stores
       float q[TMAX], k[TMAX], a[TMAX], vv[TMAX];
+      {
+        uint32_t bq[TMAX], bk[TMAX], bv[TMAX];
 #pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        q[t] = 0.f;
-        k[t] = 0.f;
-        a[t] = 0.f;  // log-gate; tokens past the window keep exp(0) = 1
-        vv[t] = 0.f;
-        if (t < T) {
-          const int64_t row = (int64_t)b * T + t;
-          const int64_t base = row * P.qkv_stride;
-          load3_as_f32(P.qkv, base + (int64_t)hk * D + r, base + (int64_t)(P.HK + hk) * D + r,
-                       base + (int64_t)2 * P.HK * D + (int64_t)hv * D + r, P.qkv_dtype, q[t], k[t], vv[t]);
-          const int64_t bh = row * P.HV + hv;
-          a[t] = GATE == GDN_GATE_PER_K ? P.g[bh * D + r] : P.g[bh];
+        for (int t = 0; t < TMAX; ++t) {
+          bq[t] = bk[t] = bv[t] = 0u;
+          a[t] = 0.f;  // log-gate; tokens past the window keep exp(0) = 1
+          if (t < T) {
+            const int64_t row = (int64_t)b * T + t;
+            const int64_t base = row * P.qkv_stride;
+            bq[t] = load_bits(P.qkv, base + (int64_t)hk * D + r, P.qkv_dtype);
+            bk[t] = load_bits(P.qkv, base + (int64_t)(P.HK + hk) * D + r, P.qkv_dtype);
+            bv[t] = load_bits(P.qkv, base + (int64_t)2 * P.HK * D + (int64_t)hv * D + r, P.qkv_dtype);
+            const int64_t bh = row * P.HV + hv;
+            a[t] = GATE == GDN_GATE_PER_K ? P.g[bh * D + r] : P.g[bh];
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          q[t] = bits_to_f32(bq[t], P.qkv_dtype);
+          k[t] = bits_to_f32(bk[t], P.qkv_dtype);
+          vv[t] = bits_to_f32(bv[t], P.qkv_dtype);
         }
       }
       const float beta_r = r < T ? P.beta[((int64_t)b * T + r) * P.HV + hv] : 0.f;
@@ -420,6 +432,7 @@ __global__ void __launch_bounds__(kThreadsSpec, 1) spec_tc_kernel(const DecodePa
         }
       }
       if (r < T) Bt[r] = beta_r;
+      if (GATE == GDN_GATE_SCALAR && r < p) gst[r] = gate_r;
       if (P.qk_l2norm) {
         float v[NCOL];
 #pragma unroll
