@@ -7,6 +7,7 @@
 // and a lane owns columns 32*m + 4*column_group + {0..3} (m < K/32), so each
 // 16-byte load of a warp covers four 128-byte runs of four rows and a row's
 // contraction over K needs only a 3-step shuffle among its 8 lanes.
+#include "gdn_bits.cuh"
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 

@@ -34,6 +34,7 @@
 // The MMA is issued only from warp 1, which never reads TMEM.  Every wait is
 // bounded; a CTA that runs out of time records GDN_DEV_TIMEOUT, lets its copies
 // and contractions land, frees its TMEM and returns.
+#include "gdn_bits.cuh"
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 #include "gdn_tc_common.cuh"
