@@ -98,3 +98,20 @@ def test_acceptance_pool_is_a_prefix_count():
     assert acc.min() >= 0 and acc.max() <= 4
     assert 0 < (acc == 0).mean() < 1 and (acc == 4).any()
     assert abs(acc.mean() - sum(0.7 ** i for i in range(1, 5))) < 0.15
+
+
+def test_lossless_bytes():
+    """Lossless verify: the state once, T tokens of inputs and outputs, T fp32
+    tuples (u per value head, k shared by the G heads of a key head, g); the
+    commit: the state in and out plus the accepted tuples, nothing when none
+    is accepted.  Against a snapshot verify (the state read, T states written)
+    the verify moves about (T + 1) / (1 + small) times fewer bytes."""
+    inputs = 2 * 128 * 2 / 2 + 128 * 2 + 4 + 4          # q, k (per key head, G = 2), v, g, beta
+    tuples = 4 * 128 + 4 * 128 / 2 + 4                 # u, k (G = 2), g
+    assert bench.lossless_verify_head_bytes(128, 128, 2, 4, 2, 2) == 65536 + 4 * (inputs + 256) + 4 * tuples
+    assert bench.lossless_commit_head_bytes(128, 128, 2, 3) == 131072 + 3 * tuples
+    assert bench.lossless_commit_head_bytes(128, 128, 2, 0) == 0.0
+    kda_tuples = 4 * 128 + 4 * 128 + 4 * 128           # G = 1, g per channel
+    assert bench.lossless_commit_head_bytes(128, 128, 1, 2, kda=True) == 131072 + 2 * kda_tuples
+    snapshot = 65536 * (1 + 8)
+    assert 7.0 < snapshot / bench.lossless_verify_head_bytes(128, 128, 2, 8, 2, 2) < 8.0
