@@ -53,7 +53,7 @@ def _token_rows(R, T, t):
     return torch.arange(R) * T + t
 
 
-def _packed_sequence(w, S0_dev, idx_dev, si_dev, T, out_dtype, accepted=None):
+def _packed_sequence(w, S0_dev, idx_dev, si_dev, T, out_dtype, accepted=None, q_scale=1.0, l2=False):
     """T successive packed decodes on a copy of the state; returns per-token
     outputs [R*T, HV, V] and the states after each prefix length (if accepted
     is given: the state where row b stopped after accepted[b] tokens)."""
@@ -68,7 +68,7 @@ def _packed_sequence(w, S0_dev, idx_dev, si_dev, T, out_dtype, accepted=None):
             idx_t[accepted.cuda() <= t] = -1  # this row has stopped: its state stays
         o = torch.empty((R, w.HV, w.V), dtype=out_dtype, device="cuda")
         Bd.gdn_packed_decode(d, st, Bd.Step(si_dev.mixed_qkv[rows].contiguous(), si_dev.g[rows].contiguous(),
-                                            si_dev.beta[rows].contiguous(), idx_t, o))
+                                            si_dev.beta[rows].contiguous(), idx_t, o, q_scale, l2))
         outs[rows] = o
     return outs, st
 
@@ -77,14 +77,15 @@ def _dev_inputs(si):
     return I.StepInputs(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda())
 
 
-def _verify(w, S_dev, idx_dev, si_dev, T, out_dtype, status=None):
+def _verify(w, S_dev, idx_dev, si_dev, T, out_dtype, status=None, q_scale=1.0, l2=False):
     R = idx_dev.shape[0]
     su, sk, sg = Bd.tuple_shapes(_desc(w), R, T)
     tu = torch.full(su, float("nan"), device="cuda")
     tk = torch.full(sk, float("nan"), device="cuda")
     tg = torch.full(sg, float("nan"), device="cuda")
     out = torch.full((R * T, w.HV, w.V), float("nan"), dtype=out_dtype, device="cuda")
-    Bd.gdn_lossless_verify(_desc(w), S_dev, T, Bd.Step(si_dev.mixed_qkv, si_dev.g, si_dev.beta, idx_dev, out),
+    Bd.gdn_lossless_verify(_desc(w), S_dev, T, Bd.Step(si_dev.mixed_qkv, si_dev.g, si_dev.beta, idx_dev, out,
+                                                       q_scale, l2),
                            tu, tk, tg, status)
     return out, tu, tk, tg
 
@@ -106,14 +107,22 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("name", list(CASES))
+# cases whose inputs go through the in-kernel L2 norm and q_scale
+NORMED = {"gdn_k128_T4", "kda_k64_T3"}
+
+
+@pytest.mark.parametrize("name", list(CASES) + [n + "_l2norm" for n in sorted(NORMED)])
 def test_verify_and_commit_are_bit_identical_to_packed_decode(gdnlib, name):
-    w, T, out_dtype = CASES[name]
+    normed = name.endswith("_l2norm")
+    w, T, out_dtype = CASES[name[: -len("_l2norm")] if normed else name]
     gen, S0, idx, si = _setup(w, T, w.seed)
+    if normed:  # unnormalised q, k: the kernels normalise and scale them
+        si = I.StepInputs(si.mixed_qkv * 3.0, si.g, si.beta)
+    q_scale, l2 = (0.37, True) if normed else (1.0, False)
     R = idx.shape[0]
     S_dev, idx_dev, si_dev = S0.cuda(), idx.cuda(), _dev_inputs(si)
-    out, tu, tk, tg = _verify(w, S_dev, idx_dev, si_dev, T, out_dtype)
-    ref_out, _ = _packed_sequence(w, S_dev, idx_dev, si_dev, T, out_dtype)
+    out, tu, tk, tg = _verify(w, S_dev, idx_dev, si_dev, T, out_dtype, q_scale=q_scale, l2=l2)
+    ref_out, _ = _packed_sequence(w, S_dev, idx_dev, si_dev, T, out_dtype, q_scale=q_scale, l2=l2)
     torch.cuda.synchronize()
     assert torch.equal(S_dev.cpu(), S0), "verify wrote the state"
     assert _same_bits(out, ref_out), "verify outputs differ from successive packed decodes"
@@ -123,14 +132,15 @@ def test_verify_and_commit_are_bit_identical_to_packed_decode(gdnlib, name):
     acc[idx < 0] = -1
     st = S_dev.clone()
     Bd.gdn_lossless_commit(_desc(w), st, idx_dev, acc.cuda(), T, tu, tk, tg)
-    _, ref_st = _packed_sequence(w, S_dev, idx_dev, si_dev, T, out_dtype, accepted=acc.clamp(min=0))
+    _, ref_st = _packed_sequence(w, S_dev, idx_dev, si_dev, T, out_dtype, accepted=acc.clamp(min=0),
+                                 q_scale=q_scale, l2=l2)
     torch.cuda.synchronize()
     assert _same_bits(st, ref_st), "committed state differs from the packed decodes' state"
 
     # the oracle: outputs and corrections within 1e-5, key and gate tuples exact
     G = O.geom(w.N, w.HV, w.HK, w.K, w.V, gate=w.gate, state_dtype=O.F64)
     o_ref, tu_ref, tk_ref, tg_ref, status = O.lossless_verify(G, O.f64(S0), idx.numpy(), T, si.mixed_qkv,
-                                                              si.g, si.beta)
+                                                              si.g, si.beta, q_scale, int(l2))
     assert status == 0
     live = np.repeat(idx.numpy() >= 0, T)
     o = out.float().cpu().numpy()
@@ -139,7 +149,10 @@ def test_verify_and_commit_are_bit_identical_to_packed_decode(gdnlib, name):
     assert np.all(o[~live] == 0.0), "padding rows must be zero"
     lb = idx.numpy() >= 0
     assert _rel(tu.cpu().numpy()[lb], tu_ref[lb]) <= TOL
-    assert np.array_equal(tk.cpu().numpy()[lb], tk_ref[lb])
+    if normed:  # the normalised keys: fp32 on the GPU, double in the oracle
+        assert _rel(tk.cpu().numpy()[lb], tk_ref[lb]) <= TOL
+    else:  # copies of the inputs
+        assert np.array_equal(tk.cpu().numpy()[lb], tk_ref[lb])
     assert np.array_equal(tg.cpu().numpy()[lb], tg_ref[lb])
     assert torch.all(torch.isnan(tu[torch.from_numpy(~lb).cuda()])), "padding rows' tuples must stay untouched"
 
