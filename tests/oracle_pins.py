@@ -177,6 +177,40 @@ def pin_kda_retrieval():
     _close(y, v, 1e-13, "y")
 
 
+def pin_scalar_head_closed_form():
+    """K = V = 1: the recurrence is the scalar s <- a s + b (v - a s k) k with
+    y = s q (a = exp g); the sequential step and the whole replay state machine
+    (ring of 3, natural flushes, cursor advance) must follow it, for GDN and
+    for KDA (one channel: its gate is the head's gate)."""
+    r = _rng(600)
+    steps = 10
+    q, k, v = r.standard_normal(steps), r.standard_normal(steps), r.standard_normal(steps)
+    g = -np.log1p(np.exp(r.standard_normal(steps)))
+    b = 1 / (1 + np.exp(-r.standard_normal(steps)))
+    s0 = 0.7
+    want, s = [], s0
+    for t in range(steps):
+        a = np.exp(g[t])
+        s = a * s + b[t] * (v[t] - a * s * k[t]) * k[t]
+        want.append(s * q[t])
+    for gate in (O.GATE_SCALAR, O.GATE_PER_K):
+        S = np.array([[s0]])
+        for t in range(steps):
+            fn = O.kda_step if gate else O.gdn_step
+            y, _ = fn(S, [q[t]], [k[t]], [v[t]], [g[t]] if gate else g[t], b[t])
+            _close(y, [want[t]], 1e-14, f"scalar step {t} (gate {gate})")
+        G = O.geom(1, 1, 1, 1, 1, 3, gate=gate, state_dtype=O.F64, ring_dtype=O.F64)
+        gk = (1,) if gate else ()
+        cache = O.Cache(np.full((1, 1, 1, 1), s0), np.full((1, 1, 3, 1), np.nan), np.full((1, 1, 3, 1), np.nan),
+                        np.full((1, 1, 3) + gk, np.nan))
+        wp = np.zeros(1, dtype=np.int32)
+        for t in range(steps):
+            gt = np.array([[[g[t]]]]) if gate else np.array([[g[t]]])
+            o, _, st = O.replay_decode(G, cache, wp, [0], None, np.array([[q[t], k[t], v[t]]]), gt, np.array([[b[t]]]))
+            assert st == 0 and O.replay_advance(1, [0], None, 3, wp) == 0
+            _close(o[0, 0], [want[t]], 1e-13, f"scalar replay step {t} (gate {gate})")
+
+
 # ---------------------------------------------------------------------------
 # The replay state machine (explainer 2.1, 3.1-3.3; #28451 Design 1/3/5/7).
 # ---------------------------------------------------------------------------
