@@ -41,6 +41,43 @@ def tolerance(w: I.Workload, recon: int) -> float:
 STORAGE_ULP = {Bd.BF16: 2.0 ** -7, Bd.F16: 2.0 ** -10, Bd.F32: 2.0 ** -23}
 
 
+# Guard bands: every device tensor a parity run hands the library sits between
+# two 4 KiB bands of a known bit pattern (a NaN pattern for float views), checked
+# bitwise after each step, so a write just outside a tensor cannot go unseen.
+GUARD_BYTES = 4096
+GUARD_WORD = 0x7FA5A5A5
+
+
+class Guarded:
+    """A device copy of a tensor between two guard bands (16-byte aligned body)."""
+
+    def __init__(self, t: torch.Tensor):
+        self.nbytes = t.numel() * t.element_size()
+        total = 2 * GUARD_BYTES + ((self.nbytes + 15) // 16) * 16
+        self.raw = torch.full((total // 4,), GUARD_WORD, dtype=torch.int32, device="cuda")
+        u8 = self.raw.view(torch.uint8)
+        self.body = u8[GUARD_BYTES:GUARD_BYTES + self.nbytes].view(t.dtype).view(t.shape)
+        self.body.copy_(t.to("cuda"))
+        self.bands = torch.cat([u8[:GUARD_BYTES], u8[GUARD_BYTES + self.nbytes:]]).clone()
+
+    def check(self, what: str) -> None:
+        u8 = self.raw.view(torch.uint8)
+        now = torch.cat([u8[:GUARD_BYTES], u8[GUARD_BYTES + self.nbytes:]])
+        assert torch.equal(now, self.bands), f"{what}: a write landed in the guard band around the tensor"
+
+
+def guarded(t: torch.Tensor, keep: list) -> torch.Tensor:
+    """Device tensor with t's contents inside guard bands; its checker goes to keep."""
+    g = Guarded(t)
+    keep.append(g)
+    return g.body
+
+
+def check_guards(keep: list, what: str) -> None:
+    for g in keep:
+        g.check(what)
+
+
 def ring_tolerance(w: I.Workload, tol: float) -> float:
     return tol + STORAGE_ULP[w.ring_dtype]
 
@@ -65,12 +102,14 @@ class Layer:
     dev: Bd.Cache
     ora: O.Cache
     init: I.CacheTensors  # CPU copy of the initial cache (for untouched checks)
+    guards: list = field(default_factory=list)
 
     @staticmethod
     def make(w: I.Workload, gen, wp_cpu: torch.Tensor) -> "Layer":
         c = I.cache(gen, w, wp_cpu, "cpu")
-        dev = Bd.Cache(c.state.cuda(), c.ring_d.cuda(), c.ring_k.cuda(), c.ring_g.cuda())
-        return Layer(w, dev, O.Cache.from_arrays(c.state, c.ring_d, c.ring_k, c.ring_g), c)
+        g: list = []
+        dev = Bd.Cache(guarded(c.state, g), guarded(c.ring_d, g), guarded(c.ring_k, g), guarded(c.ring_g, g))
+        return Layer(w, dev, O.Cache.from_arrays(c.state, c.ring_d, c.ring_k, c.ring_g), c, g)
 
 
 @dataclass
@@ -114,13 +153,14 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
     idx = I.indices(gen, w.B, w.N, w.n_pad, "cpu")
     rows = idx.shape[0]
     live = idx.numpy() >= 0
-    wp_dev = wp.cuda()
+    io_guards: list = []
+    wp_dev = guarded(wp, io_guards)
     wp_ora = wp.numpy().astype(np.int32).copy()
-    idx_dev = idx.cuda()
+    idx_dev = guarded(idx, io_guards)
     desc = desc_of(w)
     G = oracle_geom(w)
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    flushed = torch.empty(rows, dtype=torch.uint8, device="cuda")
+    status = guarded(torch.zeros(1, dtype=torch.int32), io_guards)
+    flushed = guarded(torch.zeros(rows, dtype=torch.uint8), io_guards)
     report = RunReport()
     for t in range(steps):
         ff = None if force is None else force(t, rows)
@@ -131,9 +171,10 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
             si = I.step_inputs(gen, w, "cpu")
             if tweak is not None:
                 tweak(t, si)
-            out = torch.full((rows, w.HV, w.V), float("nan"), dtype=out_dtype, device="cuda")
-            step = Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx_dev, out,
-                           q_scale=q_scale, qk_l2norm=qk_l2norm)
+            step_guards: list = []
+            out = guarded(torch.full((rows, w.HV, w.V), float("nan"), dtype=out_dtype), step_guards)
+            step = Bd.Step(guarded(si.mixed_qkv, step_guards), guarded(si.g, step_guards),
+                           guarded(si.beta, step_guards), idx_dev, out, q_scale=q_scale, qk_l2norm=qk_l2norm)
             Bd.gdn_replayssm_decode(desc, layer.dev, wp_dev, ff_dev, step, recon, flushed, status)
             o_ref, fl_ref, st_ref = O.replay_decode(G, layer.ora, wp_ora, idx.numpy(), ff,
                                                     si.mixed_qkv, si.g, si.beta, q_scale, int(qk_l2norm))
@@ -148,7 +189,10 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
             rep.o_err = max(rep.o_err, rel_err(o[live], ref[live]))
             assert rep.o_err <= tol, f"step {t} layer {li}: out rel err {rep.o_err:.3e} > {tol:.1e}"
             _compare_cache(layer, w, idx.numpy(), wp_before, fl_ref, tol, rep, t, exact_k=not qk_l2norm)
+            check_guards(step_guards + layer.guards, f"step {t} layer {li}")
         Bd.gdn_replayssm_advance(idx_dev, ff_dev, w.N, w.L, wp_dev, status)
+        torch.cuda.synchronize()
+        check_guards(io_guards, f"step {t} cursors")
         O.replay_advance(w.N, idx.numpy(), ff, w.L, wp_ora)
         assert np.array_equal(wp_dev.cpu().numpy(), wp_ora), f"write_pos differs after step {t}"
         report.steps.append(rep)

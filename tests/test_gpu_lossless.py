@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import oracle as O
+from gpu_harness import check_guards, guarded
 from linear_attention_decode_gb300 import binding as Bd
 from linear_attention_decode_gb300 import inputs as I
 
@@ -77,16 +78,21 @@ def _dev_inputs(si):
     return I.StepInputs(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda())
 
 
-def _verify(w, S_dev, idx_dev, si_dev, T, out_dtype, status=None, q_scale=1.0, l2=False):
+def _verify(w, S_dev, idx_dev, si_dev, T, out_dtype, status=None, q_scale=1.0, l2=False, guards=None):
+    """The verify into NaN-filled tuple and output buffers, each between guard
+    bands (checked here after the launch; the bands' owners go to `guards`)."""
     R = idx_dev.shape[0]
     su, sk, sg = Bd.tuple_shapes(_desc(w), R, T)
-    tu = torch.full(su, float("nan"), device="cuda")
-    tk = torch.full(sk, float("nan"), device="cuda")
-    tg = torch.full(sg, float("nan"), device="cuda")
-    out = torch.full((R * T, w.HV, w.V), float("nan"), dtype=out_dtype, device="cuda")
+    g = [] if guards is None else guards
+    tu = guarded(torch.full(su, float("nan")), g)
+    tk = guarded(torch.full(sk, float("nan")), g)
+    tg = guarded(torch.full(sg, float("nan")), g)
+    out = guarded(torch.full((R * T, w.HV, w.V), float("nan"), dtype=out_dtype), g)
     Bd.gdn_lossless_verify(_desc(w), S_dev, T, Bd.Step(si_dev.mixed_qkv, si_dev.g, si_dev.beta, idx_dev, out,
                                                        q_scale, l2),
                            tu, tk, tg, status)
+    torch.cuda.synchronize()
+    check_guards(g, "lossless verify")
     return out, tu, tk, tg
 
 
@@ -130,8 +136,11 @@ def test_verify_and_commit_are_bit_identical_to_packed_decode(gdnlib, name):
     # commit a random accepted prefix per row, in place
     acc = torch.randint(0, T + 1, (R,), generator=gen, dtype=torch.int32)
     acc[idx < 0] = -1
-    st = S_dev.clone()
+    cg: list = []
+    st = guarded(S_dev, cg)
     Bd.gdn_lossless_commit(_desc(w), st, idx_dev, acc.cuda(), T, tu, tk, tg)
+    torch.cuda.synchronize()
+    check_guards(cg, "lossless commit")
     _, ref_st = _packed_sequence(w, S_dev, idx_dev, si_dev, T, out_dtype, accepted=acc.clamp(min=0),
                                  q_scale=q_scale, l2=l2)
     torch.cuda.synchronize()
