@@ -308,6 +308,16 @@ GDN_API gdn_status_t gdn_lossless_commit(const gdn_layer_desc_t *desc, float *st
                                          const float *tup_u, const float *tup_k, const float *tup_g,
                                          uint32_t *dev_status, gdn_stream_t stream);
 
+/* Self-test of the on-chip wait bound (no counterpart in the pages).  The
+ * decode kernels wait on shared-memory barriers through one bounded wait: when
+ * a wait runs out (a copy or a contraction that never completes) the kernel
+ * ORs GDN_DEV_TIMEOUT into dev_status and returns instead of hanging.  This
+ * call launches one block that runs that same wait on a barrier no thread ever
+ * arrives on, with a limit of limit_us microseconds (1 .. 100000), so it
+ * always runs out: *dev_status gets GDN_DEV_TIMEOUT and the context stays
+ * usable.  dev_status is a device uint32 (required). */
+GDN_API gdn_status_t gdn_selftest_wait_timeout(uint32_t *dev_status, uint32_t limit_us, gdn_stream_t stream);
+
 /* Static text for a status code (host). */
 GDN_API const char *gdn_status_str(gdn_status_t status);
 

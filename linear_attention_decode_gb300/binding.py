@@ -110,10 +110,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_replayssm_reset_slots.argtypes = [vp, i32, vp, i32, u32p, vp]
         lib.gdn_lossless_verify.argtypes = [dp, vp, ctypes.POINTER(_SpecStep), vp, vp, vp, u32p, vp]
         lib.gdn_lossless_commit.argtypes = [dp, vp, vp, vp, vp, i32, i32, vp, vp, vp, u32p, vp]
+        lib.gdn_selftest_wait_timeout.argtypes = [u32p, ctypes.c_uint32, vp]
         for f in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_decode_advance",
                   "gdn_replayssm_decode_advance_noalloc", "gdn_replayssm_advance", "gdn_replayssm_flush",
                   "gdn_replayssm_reset_slots", "gdn_replayssm_spec_verify", "gdn_replayssm_spec_commit",
-                  "gdn_lossless_verify", "gdn_lossless_commit"):
+                  "gdn_lossless_verify", "gdn_lossless_commit", "gdn_selftest_wait_timeout"):
             getattr(lib, f).restype = ctypes.c_int
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
@@ -384,6 +385,13 @@ def gdn_replayssm_reset_slots(write_pos: torch.Tensor, slots: torch.Tensor,
         _dev(write_pos, "write_pos", (N,), torch.int32), N,
         _dev(slots, "slots", (n,), torch.int32), n, _status_ptr(dev_status), _stream(stream)),
         "gdn_replayssm_reset_slots")
+
+
+def gdn_selftest_wait_timeout(dev_status: torch.Tensor, limit_us: int = 2000, stream=None) -> None:
+    """One block waits, with the decode kernels' bounded wait, on a barrier
+    nothing completes; dev_status ([1] int32) gets DEV_TIMEOUT."""
+    _check(load_library().gdn_selftest_wait_timeout(_status_ptr(dev_status), int(limit_us), _stream(stream)),
+           "gdn_selftest_wait_timeout")
 
 
 def gdn_status_str(status: int) -> str:

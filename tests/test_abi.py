@@ -180,3 +180,10 @@ def test_lossless_verify_and_commit_check_their_arguments(lib):
     assert c(ctypes.byref(d), 0x1008, 0x1000, None, 0x1000, 4, 4, 0x1000, 0x1000, 0x1000, None, None) == 1  # misaligned
     assert c(ctypes.byref(_desc(num_k_heads=5)), 0x1000, 0x1000, None, 0x1000, 4, 4, 0x1000, 0x1000, 0x1000,
              None, None) == 1
+
+
+def test_wait_selftest_checks_its_arguments(lib):
+    f = lib.gdn_selftest_wait_timeout
+    assert f(None, 10, None) == 1         # no status word
+    assert f(0x1000, 0, None) == 1        # limit below 1 us
+    assert f(0x1000, 100001, None) == 1   # limit above 100 ms
