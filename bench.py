@@ -14,6 +14,7 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|referenc
        [--sweep [--sweep-batches 1,8,...] [--sweep-lens 1,4,...]]  (one JSON line per point)
        [--spec [--spec-batches 64,256] [--spec-windows 2,4,8] [--spec-accept 0.7]]
                          (speculative verify window + commit + fold, one JSON line per point)
+       [--graph [--graph-batches 1,8,64,256]]  (CUDA-graph replay vs one-by-one launches)
        [--lossless [--spec-batches ...] [--spec-windows ...]]
                          (lossless verify + exact-order commit, one JSON line per point)
 Under torchrun each rank runs an independent replica on its own GPU (the
@@ -677,6 +678,77 @@ def measure_lossless(B, T, K, warmup, dev, rate=0.7):
             "packed_decode_ms_per_step": pk_s * 1e3}
 
 
+def measure_graph(B, n, warmup, dev):
+    """One GDN layer's decode + advance at batch B (L=16, fp16 ring): n steps
+    launched one by one, against the same n steps captured once in a CUDA graph
+    and replayed (the library allocates nothing and never synchronises, so its
+    calls capture).  Kernel-only, inputs resident."""
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import inputs as I
+
+    w = I.sweep_point(B, 16, Bd.F16)
+    gen = I.generator(w.seed, dev)
+    wp = I.write_pos(gen, w, dev)
+    c = I.cache(gen, w, wp, dev)
+    cache = Bd.Cache(c.state, c.ring_d, c.ring_k, c.ring_g)
+    idx = I.indices(gen, w.B, w.N, w.n_pad, dev)
+    desc = Bd.layer_desc(w.N, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, ring_dtype=w.ring_dtype)
+    out = torch.empty((idx.shape[0], w.HV, w.V), dtype=torch.bfloat16, device=dev)
+    steps_in = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out) for b in (I.step_inputs(gen, w, dev) for _ in range(4))]
+    ws = Bd.decode_advance_workspace(dev)
+
+    def seq(stream):
+        for i in range(n):
+            Bd.gdn_replayssm_decode_advance(desc, cache, wp, None, steps_in[i % 4], ws, Bd.RECON_TENSOR, None, None,
+                                            stream)
+
+    def timed(fn, stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    cur = torch.cuda.current_stream()
+    for _ in range(max(1, warmup // n + 1)):
+        seq(cur)
+    eager_us = timed(lambda: seq(cur), cur)
+    graph = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(graph, stream=cs):
+            seq(cs)
+    graph.replay()
+    torch.cuda.synchronize()
+    graph_us = timed(graph.replay, cur)
+    return {"workload": w.name, "B": B, "steps_per_graph": n, "eager_us_per_step": eager_us,
+            "graph_us_per_step": graph_us, "graph_head_steps_per_s": B * w.HV / (graph_us * 1e-6),
+            "graph_vs_eager": eager_us / graph_us}
+
+
+def run_graph(args):
+    """CUDA-graph replay against one-by-one launches: one JSON line per batch."""
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import build as cuda_build
+
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cuda_build.build()
+    Bd.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    for B in [int(x) for x in args.graph_batches.split(",")]:
+        print(json.dumps(measure_graph(B, 64, args.warmup, dev)), flush=True)
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_lossless(args):
     """Lossless verify + commit sweep: one JSON line per (batch, window)."""
     import torch
@@ -931,6 +1003,9 @@ def main():
     ap.add_argument("--sweep-lens", default="1,4,8,16,32")
     ap.add_argument("--spec", action="store_true",
                     help="speculative verify window sweep (one JSON line per batch x window)")
+    ap.add_argument("--graph", action="store_true",
+                    help="CUDA-graph replay of 64 decode + advance steps against one-by-one launches")
+    ap.add_argument("--graph-batches", default="1,8,64,256")
     ap.add_argument("--lossless", action="store_true",
                     help="lossless verify + exact-order commit sweep (one JSON line per batch x window)")
     ap.add_argument("--spec-batches", default="64,256")
@@ -952,6 +1027,8 @@ def main():
         return run_spec(args)
     if args.lossless:
         return run_lossless(args)
+    if args.graph:
+        return run_graph(args)
     return run_ours(args)
 
 
