@@ -325,6 +325,45 @@ def pin_l1_is_packed_decode():
     _close(cache.state, state, 1e-13, "checkpoint")
 
 
+def _factored_readout(gate):
+    """The replayed state's readout S x, where S = A S0 + sum_j w_j d_j k_j^T
+    (KDA: S0 Diag(A) + sum_j d_j (w_j o k_j)^T), equals the factored form
+    A (S0 x) + sum_j w_j d_j (k_j . x) (KDA: S0 (A o x) + sum_j d_j ((w_j o k_j) . x))
+    that never forms S ([P1] Design 1 "output-only"; [P2] 3.2): the algebra the
+    output-only readout and the verify window's checkpoint products rely on."""
+    HV, HK, K, V, L, p = 2, 1, K5, V3, 8, 5
+    G = O.geom(1, HV, HK, K, V, L, gate=gate, state_dtype=O.F64, ring_dtype=O.F64)
+    r = _rng(610 + gate)
+    gk = (K,) if gate else ()
+    cache = O.Cache(r.standard_normal((1, HV, V, K)), r.standard_normal((1, HV, L, V)),
+                    r.standard_normal((1, HK, L, K)), -np.abs(r.standard_normal((1, HV, L) + gk)))
+    x = r.standard_normal(K)
+    for hv in range(HV):
+        S = O.replay_state(G, cache, 0, hv, p)
+        S0, g = cache.state[0, hv], cache.ring_g[0, hv]
+        d, k = cache.ring_d[0, hv], cache.ring_k[0, 0]
+        if gate:
+            A = np.exp(g[:p].sum(axis=0))
+            y = S0 @ (A * x)
+            for j in range(p):
+                w = np.exp(g[j + 1:p].sum(axis=0))
+                y = y + d[j] * np.dot(w * k[j], x)
+        else:
+            A = np.exp(g[:p].sum())
+            y = A * (S0 @ x)
+            for j in range(p):
+                y = y + np.exp(g[j + 1:p].sum()) * d[j] * np.dot(k[j], x)
+        _close(S @ x, y, 1e-12, f"factored readout, head {hv}")
+
+
+def pin_factored_readout_gdn():
+    _factored_readout(O.GATE_SCALAR)
+
+
+def pin_factored_readout_kda():
+    _factored_readout(O.GATE_PER_K)
+
+
 def pin_walkthrough_L4():
     """The explainer's L = 4 table (section 3.3): checkpoint before each step,
     valid entries before each step, and the action taken."""
