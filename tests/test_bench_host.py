@@ -115,3 +115,15 @@ def test_lossless_bytes():
     assert bench.lossless_commit_head_bytes(128, 128, 1, 2, kda=True) == 131072 + 2 * kda_tuples
     snapshot = 65536 * (1 + 8)
     assert 7.0 < snapshot / bench.lossless_verify_head_bytes(128, 128, 2, 8, 2, 2) < 8.0
+
+
+def test_lossless_tuple_ratio_matches_the_pages():
+    """sglang #42388 (The idea): keeping (u, k, g) costs HV (V + K + 1) floats per
+    draft step instead of an HV V K snapshot, 63.8x less at K = V = 128.  The
+    tuple bytes of the verify's byte model give that ratio with one key head per
+    value head (G = 1); sharing k across a GQA group (G = 2) makes it larger."""
+    def tuple_bytes(G):  # the verify's bytes for T = 1 minus the state read, inputs and output
+        inputs = 2 * 128 * 2 / G + 128 * 2 + 4 + 4
+        return bench.lossless_verify_head_bytes(128, 128, G, 1, 2, 2) - 65536 - inputs - 128 * 2
+    assert round(4 * 128 * 128 / tuple_bytes(1), 1) == 63.8
+    assert 4 * 128 * 128 / tuple_bytes(2) > 80
