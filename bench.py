@@ -40,8 +40,12 @@ METRIC = "GDN decode head-steps/s & HBM GB/s vs 8 TB/s (HV=32,K=V=128,L=16,B=256
 UNIT = "head-steps/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE = os.path.join(ROOT, "profiles", "gdn_replayssm_decode_tc_B256_L16.md")
-KERNEL_SOURCES = [os.path.join(ROOT, "linear_attention_decode_gb300", "csrc", f)
-                  for f in ("gdn_tcp.cu", "gdn_tc_common.cuh", "gdn_common.cuh")]
+# everything the profiled kernel's code and launch depend on: a change to any
+# of these marks the stored ncu traffic stale
+KERNEL_SOURCES = ([os.path.join(ROOT, "linear_attention_decode_gb300", "csrc", f)
+                   for f in ("gdn_tcp.cu", "gdn_tc_common.cuh", "gdn_common.cuh", "gdn_kernels.h", "gdn_tc.cu",
+                             "gdn_api.cu")]
+                  + [os.path.join(ROOT, "include", "gdnreplay.h")])
 
 
 # ---------------------------------------------------------------------------
@@ -241,7 +245,7 @@ class OracleSample:
     """The CPU oracle as it stands (single thread) on a small pool of the
     workload's shapes: each call decodes `rows` rows x HV heads for one step."""
 
-    def __init__(self, w, pool_rows=16):
+    def __init__(self, w, pool_rows=16, seed_offset=0):
         import numpy as np
 
         import oracle as O
@@ -251,7 +255,7 @@ class OracleSample:
         self.w, self.np, self.O, self.I = w, np, O, I
         self.pool = pool_rows
         self.sw = I.with_(w, N=pool_rows, B=pool_rows, n_pad=0)
-        self.gen = I.generator(w.seed + 100, "cpu")
+        self.gen = I.generator(w.seed + 100 + seed_offset, "cpu")
         wp = I.write_pos(self.gen, self.sw, "cpu")
         c = I.cache(self.gen, self.sw, wp, "cpu")
         self.G = O.geom(pool_rows, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, state_dtype=O.F32,
@@ -275,16 +279,79 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
-def cpu_oracle_timing(w, seconds_target=10.0, rows=16):
-    """cpu_baseline leg: the oracle on a bounded sample (about seconds_target)."""
-    s = OracleSample(w, pool_rows=rows)
-    t_total, steps = 0.0, 0
-    while t_total < seconds_target:
-        t_total += s.step(rows)
-        steps += 1
-    return {"value": rows * w.HV * steps / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{rows} rows x {w.HV} heads x {steps} steps of the workload's shapes "
-                      f"(K=V={w.K}, L={w.L}, fp16 ring, staggered cursors), one thread, {t_total:.1f} s"}
+def host_cpu_info():
+    """The host's thread count (what std::thread::hardware_concurrency reports),
+    the threads this process may use, and the CPU model from /proc/cpuinfo."""
+    info = {"hardware_concurrency": os.cpu_count(), "usable_threads": len(os.sched_getaffinity(0))}
+    model = None
+    try:
+        text = open("/proc/cpuinfo").read()
+        m = re.search(r"^model name\s*:\s*(.+)$", text, re.M)
+        if m:
+            model = m.group(1).strip()
+        else:  # Arm: the implementer and part codes
+            imp = re.search(r"^CPU implementer\s*:\s*(\S+)", text, re.M)
+            part = re.search(r"^CPU part\s*:\s*(\S+)", text, re.M)
+            if imp and part:
+                known = {("0x41", "0xd4f"): "Arm Neoverse-V2"}
+                model = known.get((imp.group(1), part.group(1)),
+                                  f"CPU implementer {imp.group(1)}, part {part.group(1)}")
+    except OSError:
+        pass
+    info["model"] = model or "unknown"
+    return info
+
+
+def cpu_oracle_timing(w, seconds_target=10.0, rows=16, threads=1):
+    """The oracle as it stands on a bounded sample of the workload: `threads`
+    host threads, each decoding its own pool of `rows` slots step after step
+    (the oracle's C code runs with the GIL released, so the threads use
+    separate cores) for about seconds_target of wall time.  Head-steps per
+    second of wall time, Python marshalling included."""
+    samples = [OracleSample(w, pool_rows=rows, seed_offset=i) for i in range(threads)]
+    counts = [0] * threads
+    go = threading.Barrier(threads + 1)
+    stop_at = [0.0]
+
+    def work(i):
+        go.wait()
+        while time.perf_counter() < stop_at[0]:
+            samples[i].step(rows)
+            counts[i] += 1
+
+    pool = [threading.Thread(target=work, args=(i,)) for i in range(threads)]
+    for t in pool:
+        t.start()
+    t0 = time.perf_counter()
+    stop_at[0] = t0 + seconds_target
+    go.wait()
+    for t in pool:
+        t.join()
+    wall = time.perf_counter() - t0
+    steps = sum(counts)
+    ring = {0: "fp32", 1: "bf16", 2: "fp16"}[w.ring_dtype]
+    return {"value": rows * w.HV * steps / wall, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{threads} thread(s) x {rows} rows x {w.HV} heads, {steps} steps in all, of the "
+                      f"workload's shapes (K=V={w.K}, L={w.L}, {ring} ring, staggered cursors), {wall:.1f} s"}
+
+
+def cpu_baseline_report(w, seconds=8.0, rows=16):
+    """cpu_baseline of the bench line: the oracle on the workload over all the
+    host's usable threads, and single-threaded, plus the same pair on the tiny
+    configuration and the one-layer configuration (shorter samples)."""
+    from linear_attention_decode_gb300 import inputs as I
+    host = host_cpu_info()
+    n = host["usable_threads"]
+    main = cpu_oracle_timing(w, seconds, rows, threads=n)
+    main["single_thread"] = cpu_oracle_timing(w, seconds, rows, threads=1)
+    main["host"] = host
+    by = {}
+    for name, wc, r in (("tiny_N8_B4_HV4_K64_L4_fp32", I.with_(I.TINY, staggered=True), 64),
+                        ("one_layer_B64_HV32_K128_L16_fp16", I.with_(I.QWEN3NEXT_LAYER, staggered=True), rows)):
+        by[name] = {"all_threads": cpu_oracle_timing(wc, seconds / 3, r, threads=n),
+                    "single_thread": cpu_oracle_timing(wc, seconds / 3, r, threads=1)}
+    main["by_config"] = by
+    return main
 
 
 def run_reference(args):
@@ -298,18 +365,33 @@ def run_reference(args):
     from linear_attention_decode_gb300 import inputs as I
     oracle.build()
     w = I.HEADLINE
-    s = OracleSample(w)
-    t_row = max(s.step(1) for _ in range(max(3, args.warmup)))
+    host = host_cpu_info()
+    nth = host["usable_threads"]
+    # each step: every thread decodes `rows` rows of its own 16-slot pool (the
+    # threads run the oracle's C code side by side on separate cores)
+    samples = [OracleSample(w, seed_offset=i) for i in range(nth)]
+    t_row = max(samples[0].step(1) for _ in range(max(3, args.warmup)))
     rows = int(min(16, max(1, args.ref_budget / max(1, args.steps) / t_row)))
-    t_total = sum(s.step(rows) for _ in range(args.steps))
-    value = args.steps * rows * w.HV / t_total
-    cpu = {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-           "sample": f"{args.steps} steps x {rows} rows x {w.HV} heads (pool of 16 slots of the "
-                     f"workload's shapes), one thread, {t_total:.1f} s"}
+
+    def one_step():
+        ths = [threading.Thread(target=smp.step, args=(rows,)) for smp in samples]
+        for t in ths:
+            t.start()
+        for t in ths:
+            t.join()
+
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    t_total = time.perf_counter() - t0
+    value = args.steps * nth * rows * w.HV / t_total
+    cpu = {"value": value, "unit": UNIT, "cores": nth, "kind": "oracle", "host": host,
+           "sample": f"{args.steps} steps x {nth} threads x {rows} rows x {w.HV} heads (a pool of 16 slots "
+                     f"of the workload's shapes per thread), {t_total:.1f} s"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name, "rows_per_step": rows},
+            "data": "synthetic", "config": {"workload": w.name, "rows_per_step": rows * nth},
             "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -327,17 +409,26 @@ def pick_workload(name):
         return I.with_(I.KDA_LAYER, staggered=True)
     if name == "stack30":
         return I.with_(I.STACK30, staggered=True)
+    if name.startswith("stack30:"):  # the 30-layer stack at another batch (same 320-slot pool)
+        B = int(name.split(":")[1])
+        N = max(I.STACK30.N, B)
+        return I.with_(I.STACK30, staggered=True, B=B, N=N,
+                       name=f"30-layer stack: N={N} B={B} HV=32 HK=16 K=V=128 L=16 fp16 ring bf16 qkv")
     if name.startswith("sweep:"):
         _, B, L, rd = name.split(":")
         return I.sweep_point(int(B), int(L), {"f16": F16, "f32": F32, "bf16": BF16}[rd])
     raise SystemExit(f"unknown workload {name}")
 
 
-def measure_replay(w, K, warmup, recon, dev, layers=1):
+def measure_replay(w, K, warmup, recon, dev, layers=1, overlap=False):
     """Kernel-only timing of K steps of `layers` layers sharing one cursor array:
     gdn_replayssm_decode on every layer but the last, gdn_replayssm_decode_advance
     on the last.  Inputs are resident on the device; nothing else runs between
-    launches.  Returns per-launch and per-step figures with the algorithmic bytes."""
+    launches.  overlap: every layer but the first is launched with
+    STEP_OVERLAP_PREVIOUS (true here: the launch before it is another layer's
+    decode, which writes neither this layer's cache nor the cursors; the first
+    layer follows the advance and waits).  Returns per-launch and per-step
+    figures with the algorithmic bytes."""
     import numpy as np
     import torch
 
@@ -356,6 +447,7 @@ def measure_replay(w, K, warmup, recon, dev, layers=1):
     pool = [I.step_inputs(gen, w, dev) for _ in range(4)]
     out = torch.empty((rows, w.HV, w.V), dtype=torch.bfloat16, device=dev)
     steps_in = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out) for b in pool]
+    steps_ov = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out, flags=Bd.STEP_OVERLAP_PREVIOUS) for b in pool]
     stream = torch.cuda.current_stream()
     adv_ws = Bd.decode_advance_workspace(dev)
     idx_h = idx.cpu().numpy()
@@ -364,9 +456,12 @@ def measure_replay(w, K, warmup, recon, dev, layers=1):
 
     def step(i):
         si = steps_in[i % len(steps_in)]
+        so = steps_ov[i % len(steps_ov)] if overlap else si
         for layer in range(layers - 1):
-            Bd.gdn_replayssm_decode(desc, caches[layer], wp, None, si, recon, None, None, stream)
-        Bd.gdn_replayssm_decode_advance(desc, caches[-1], wp, None, si, adv_ws, recon, None, None, stream)
+            Bd.gdn_replayssm_decode(desc, caches[layer], wp, None, si if layer == 0 else so, recon, None, None,
+                                    stream)
+        Bd.gdn_replayssm_decode_advance(desc, caches[-1], wp, None, si if layers == 1 else so, adv_ws, recon,
+                                        None, None, stream)
 
     def host_advance():
         live = idx_h[idx_h >= 0]
@@ -395,7 +490,8 @@ def measure_replay(w, K, warmup, recon, dev, layers=1):
     launch_s = step_s / layers
     peak, _ = measured_hbm_peak()
     gbs = total / K / step_s / 1e9
-    return {"workload": w.name, "layers": layers, "B": w.B, "L": w.L,
+    return {"workload": w.name, "layers": layers, "overlap_previous": bool(overlap and layers > 1),
+            "B": w.B, "L": w.L,
             "ring": {0: "f32", 1: "bf16", 2: "f16"}[w.ring_dtype], "steps": K,
             "ms_per_step": step_s * 1e3, "ms_per_launch": launch_s * 1e3,
             "head_steps_per_s_per_layer": w.B * w.HV / launch_s, "tokens_per_s_per_layer": w.B / launch_s,
@@ -405,28 +501,37 @@ def measure_replay(w, K, warmup, recon, dev, layers=1):
 
 def measure_packed(w, K, dev):
     """The in-repo packed decode (reads and writes the state every step) on the
-    workload's shapes: kernel-only, K launches back to back."""
+    workload's shapes: kernel-only, K launches back to back.  The state pool
+    holds at least four times the batch's slots and consecutive launches use
+    four disjoint slot sets in turn, so no launch finds its states in L2."""
     import torch
 
     from linear_attention_decode_gb300 import binding as Bd
     from linear_attention_decode_gb300 import inputs as I
 
     gen = I.generator(w.seed + 7, dev)
-    st = I.state(gen, w.N, w.HV, w.V, w.K, dev)
-    idx = I.indices(gen, w.B, w.N, w.n_pad, dev)
-    rows = idx.shape[0]
-    desc = Bd.layer_desc(w.N, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, ring_dtype=w.ring_dtype)
+    N = max(w.N, 4 * w.B)
+    st = I.state(gen, N, w.HV, w.V, w.K, dev)
+    perm = torch.randperm(N, generator=gen, device=dev).to(torch.int32)
+    sets = []
+    for j in range(4):
+        idx = torch.full((w.B + w.n_pad,), -1, dtype=torch.int32, device=dev)
+        live = torch.randperm(w.B + w.n_pad, generator=gen, device=dev)[:w.B]
+        idx[live] = perm[j * w.B:(j + 1) * w.B]
+        sets.append(idx)
+    rows = w.B + w.n_pad
+    desc = Bd.layer_desc(N, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, ring_dtype=w.ring_dtype)
     si = I.step_inputs(gen, w, dev)
     out = torch.empty((rows, w.HV, w.V), dtype=torch.bfloat16, device=dev)
-    step = Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out)
+    steps = [Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out) for idx in sets]
     stream = torch.cuda.current_stream()
-    for _ in range(4):
-        Bd.gdn_packed_decode(desc, st, step, None, stream)
+    for i in range(8):
+        Bd.gdn_packed_decode(desc, st, steps[i % 4], None, stream)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(K):
-        Bd.gdn_packed_decode(desc, st, step, None, stream)
+    for i in range(K):
+        Bd.gdn_packed_decode(desc, st, steps[i % 4], None, stream)
     b.record(stream)
     torch.cuda.synchronize()
     s = a.elapsed_time(b) / 1e3 / K
@@ -435,6 +540,27 @@ def measure_packed(w, K, dev):
     peak, _ = measured_hbm_peak()
     return {"ms_per_launch": s * 1e3, "head_steps_per_s": w.B * w.HV / s, "tokens_per_s": w.B / s,
             "hbm_gbs_algorithmic": nbytes / s / 1e9, "frac": nbytes / s / 1e9 / peak}
+
+
+def run_packed(args):
+    """Kernel-only timing of the in-repo packed decode (gdn_packed_decode, the
+    read + write baseline) on the workload's shapes: one JSON line."""
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import build as cuda_build
+
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cuda_build.build()
+    Bd.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = pick_workload(args.workload)
+    r = measure_packed(w, args.steps, dev)
+    r.update({"workload": w.name, "kernel": "gdn_packed_decode", "steps": args.steps})
+    print(json.dumps(r))
+    return 0
 
 
 def run_sweep(args):
@@ -456,13 +582,15 @@ def run_sweep(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     batches = [int(x) for x in args.sweep_batches.split(",")]
     lens = [int(x) for x in args.sweep_lens.split(",")]
+    rings = [{"f16": F16, "f32": F32}[x] for x in args.sweep_rings.split(",")]
     packed = {}
     for B in batches:
         for L in lens:
-            for ring in (F16, F32):
+            for ring in rings:
                 w = I.sweep_point(B, L, ring)
-                K = max(2 * L * 8, 128)
-                r = measure_replay(w, K, max(args.warmup, 2 * L), Bd.RECON_TENSOR, dev)
+                K = max(2 * L * 8, 128) // args.sweep_layers + 1
+                r = measure_replay(w, K, max(args.warmup, 2 * L), Bd.RECON_TENSOR, dev, layers=args.sweep_layers,
+                                   overlap=args.sweep_layers > 1 and not args.no_overlap)
                 if B not in packed:
                     packed[B] = measure_packed(w, 64, dev)
                 r["packed"] = packed[B]
@@ -787,11 +915,12 @@ def run_ours(args):
     Bd.load_library()
     dev = torch.device("cuda", torch.cuda.current_device())
     w = pick_workload(args.workload)
-    if args.workload == "stack30":
+    if args.workload.startswith("stack30"):
         # the 30-layer forward: 30 launches a step, the last one also advancing
         if not args.kernel_only:
             raise SystemExit("--workload stack30 is measured with --kernel-only")
-        r = measure_replay(w, args.steps, args.warmup, Bd.RECON_TENSOR, dev, layers=w.layers)
+        r = measure_replay(w, args.steps, args.warmup, Bd.RECON_TENSOR, dev, layers=w.layers,
+                           overlap=not args.no_overlap)
         if rank == 0:
             print(json.dumps(r))
         if ws > 1:
@@ -881,20 +1010,12 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
-    # in-repo packed decode on the same batches (baseline: reads and writes the state)
-    pk = max(64, K // 8)
-    pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for i in range(8):
-        Bd.gdn_packed_decode(desc, cache.state, steps_in[i % POOL], None, stream)
-    torch.cuda.synchronize()
-    pa.record(stream)
-    for i in range(pk):
-        Bd.gdn_packed_decode(desc, cache.state, steps_in[i % POOL], None, stream)
-    pb.record(stream)
-    torch.cuda.synchronize()
-    packed_s = pa.elapsed_time(pb) / 1e3 / pk
-    pbytes = (w.B * w.HV * packed_head_step_bytes(w.K, w.V, w.HV // w.HK, 2, 2, w.gate == Bd.GATE_PER_K)
-              + (rows - w.B) * w.HV * w.V * 2)
+    # in-repo packed decode on the workload's shapes (baseline: reads and writes
+    # the state; four disjoint slot sets in turn, so no launch hits L2)
+    pk = measure_packed(w, max(64, K // 8), dev)
+    packed_s = pk["ms_per_launch"] / 1e3
+    pbytes = pk["hbm_gbs_algorithmic"] * 1e9 * packed_s
+    torch.cuda.empty_cache()
 
     # end to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory to the device, runs the decode +
@@ -951,7 +1072,7 @@ def run_ours(args):
         if ws > 1:
             dist.destroy_process_group()
         return 0
-    cpu = cpu_oracle_timing(w, seconds_target=args.ref_seconds, rows=args.ref_rows) if ws == 1 else None
+    cpu = cpu_baseline_report(w, seconds=args.ref_seconds, rows=args.ref_rows) if ws == 1 else None
     clk = clocks.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
@@ -997,10 +1118,17 @@ def main():
     ap.add_argument("--workload", default="headline")
     ap.add_argument("--recon", choices=["tensor", "ffma", "output"], default="tensor")
     ap.add_argument("--kernel-only", action="store_true")
+    ap.add_argument("--packed", action="store_true",
+                    help="time only the packed decode baseline on the workload (kernel-only, one JSON line)")
     ap.add_argument("--sweep", action="store_true",
                     help="batch x ring length x ring dtype sweep of one layer (one JSON line per point)")
     ap.add_argument("--sweep-batches", default="1,8,64,128,256,512")
     ap.add_argument("--sweep-lens", default="1,4,8,16,32")
+    ap.add_argument("--sweep-rings", default="f16,f32")
+    ap.add_argument("--sweep-layers", type=int, default=1,
+                    help="layer buffers rotated per step (>= 4 keeps a layer's working set out of L2)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="multi-layer modes: launch every layer without STEP_OVERLAP_PREVIOUS")
     ap.add_argument("--spec", action="store_true",
                     help="speculative verify window sweep (one JSON line per batch x window)")
     ap.add_argument("--graph", action="store_true",
@@ -1021,6 +1149,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.packed:
+        return run_packed(args)
     if args.sweep:
         return run_sweep(args)
     if args.spec:

@@ -130,7 +130,27 @@ typedef struct {
     int32_t qk_l2norm;                /* 1: q, k <- x / sqrt(sum x^2 + 1e-6) first     */
     void *out;                        /* [B, HV, V] in out_dtype                       */
     int32_t out_dtype;                /* gdn_dtype_t                                   */
+    uint32_t flags;                   /* GDN_STEP_* bits below; 0 for none             */
 } gdn_step_t;
+
+/* gdn_step_t.flags.
+ * GDN_STEP_OVERLAP_PREVIOUS: the caller states that the launch issued on the
+ *   same stream just before this call writes none of this call's cache (state
+ *   and rings), write_pos, ssm_state_indices and force_flush, and, if that
+ *   launch was itself made with programmatic dependent launch, that it lets
+ *   the work after it start only after it has waited for the work before it
+ *   (every kernel of this library does; a kernel launched without programmatic
+ *   dependent launch is always fine).  Example: each layer of a forward but
+ *   the first, when the layers' decodes follow one another on the stream.
+ *   The tensor-core decode then reads its rows and cursors and starts
+ *   streaming checkpoints before that launch has finished, so its own start
+ *   overlaps that launch's tail; it still reads mixed_qkv, g and beta, and
+ *   writes anything at all, only after that launch has completed.  If the
+ *   statement is false the results are undefined.  The other recon modes and
+ *   gdn_packed_decode ignore the flag.  No counterpart in the pages: a
+ *   property of this library's launches. */
+#define GDN_STEP_OVERLAP_PREVIOUS 1u
+#define GDN_STEP_KNOWN_FLAGS      1u
 
 /* Packed decode, the read + write baseline ([P1] Motivation; [P2] section 1):
  * per row b with slot s = ssm_state_indices[b] >= 0 and every value head,
@@ -188,18 +208,28 @@ GDN_API gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, 
  * The scratch (one completion counter, GDN_DECODE_ADVANCE_WORKSPACE_BYTES)
  * comes from a 256-byte array compiled into the library, which every GPU that
  * loads the library keeps until the process exits; a call whose scratch need
- * exceeded it would be rejected with GDN_ERR_UNSUPPORTED.  The first call on a
- * device (the current one) looks the array's address up and clears it,
- * synchronously: make that first call before any stream capture.  All calls on
- * a device share the array, and every launch that runs to its end leaves the
- * counter at zero; calls that overlap on the GPU (e.g. on two streams) race on
- * it and must not be issued.  Nothing is allocated.  Arguments and results as
- * in gdn_replayssm_decode_advance. */
+ * exceeded it would be rejected with GDN_ERR_UNSUPPORTED.  The array is zero
+ * when the library's module loads into a context, and every launch leaves the
+ * counter at zero again, so nothing is ever cleared.  The first call in a
+ * context (that of the current device) looks the array's device address up on
+ * the host (cudaGetSymbolAddress); later calls in the same context reuse it,
+ * and a new context (after cudaDeviceReset, say) gets a fresh lookup.  Make
+ * that first call before any stream capture.  All calls in a context share
+ * the array: calls that overlap on the GPU (e.g. on two streams) race on it
+ * and must not be issued.  Nothing is allocated.  Arguments and results as in
+ * gdn_replayssm_decode_advance. */
 GDN_API gdn_status_t gdn_replayssm_decode_advance_noalloc(const gdn_layer_desc_t *desc,
                                                   const gdn_layer_cache_t *cache, int32_t *write_pos,
                                                   const uint8_t *force_flush, const gdn_step_t *step,
                                                   int32_t recon, uint8_t *flushed_out,
                                                   uint32_t *dev_status, gdn_stream_t stream);
+
+/* Diagnostic for gdn_replayssm_decode_advance_noalloc (the pages have no
+ * counterpart): copies the first n (1 .. 64) 32-bit words of the library's
+ * scratch array on the current device into host_words (HOST memory), with a
+ * blocking cudaMemcpy.  Between calls the first word, the completion counter,
+ * is zero.  Allocates nothing. */
+GDN_API gdn_status_t gdn_noalloc_scratch_peek(uint32_t *host_words, int32_t n);
 
 /* Cursor advance, once per forward after all layers ([P1] Design 3):
  * write_pos[s] <- (write_pos[s] == L-1 or force_flush[b]) ? 0 : write_pos[s] + 1
@@ -258,9 +288,10 @@ GDN_API gdn_status_t gdn_replayssm_spec_verify(const gdn_layer_desc_t *desc, con
                                        const int32_t *write_pos, const gdn_spec_step_t *step, int32_t recon,
                                        uint32_t *dev_status, gdn_stream_t stream);
 
-/* Commit after a verify window, once per forward ([P3] "rollback is a cursor
- * move"): write_pos[s] += accepted[b] (0 <= accepted[b] <= window); rejected
- * drafts stay in the ring past the cursor and are never read.  flush_slots[b]
+/* Commit after a verify window, once per forward ([P3] Core concept: a
+ * rejected draft is undone by moving the cursor, nothing else):
+ * write_pos[s] += accepted[b] (0 <= accepted[b] <= window); rejected drafts
+ * stay in the ring past the cursor and are never read.  flush_slots[b]
  * ([B] int32) receives s when the next window would not fit
  * (write_pos[s] + window > L - 1), else -1: pass it to gdn_replayssm_flush for
  * every layer and then to gdn_replayssm_reset_slots.  Padding rows get -1. */

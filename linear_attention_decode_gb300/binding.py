@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdnrepla
 
 from .constants import (BF16, DEV_BAD_ACCEPTED, DEV_BAD_SLOT, DEV_BAD_WRITE_POS, DEV_INTERNAL, DEV_TIMEOUT,  # noqa: F401
                         F16, F32, GATE_PER_K, GATE_SCALAR, GDN_DTYPE, RECON_FFMA, RECON_OUTPUT, RECON_TENSOR,
-                        TORCH_DTYPE)
+                        STEP_OVERLAP_PREVIOUS, TORCH_DTYPE)
 
 
 class GdnError(RuntimeError):
@@ -56,7 +56,7 @@ class _Step(ctypes.Structure):
                 ("beta", ctypes.c_void_p), ("ssm_state_indices", ctypes.c_void_p),
                 ("batch", ctypes.c_int32), ("q_scale", ctypes.c_float),
                 ("qk_l2norm", ctypes.c_int32), ("out", ctypes.c_void_p),
-                ("out_dtype", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
 
 
 def layer_desc(num_slots, num_v_heads, num_k_heads, k_dim, v_dim, ring_len,
@@ -84,6 +84,7 @@ class Step:
     out: torch.Tensor                # [B, HV, V]
     q_scale: float = 1.0
     qk_l2norm: bool = False
+    flags: int = 0                   # STEP_* bits (STEP_OVERLAP_PREVIOUS)
 
 
 _lib = None
@@ -111,10 +112,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_lossless_verify.argtypes = [dp, vp, ctypes.POINTER(_SpecStep), vp, vp, vp, u32p, vp]
         lib.gdn_lossless_commit.argtypes = [dp, vp, vp, vp, vp, i32, i32, vp, vp, vp, u32p, vp]
         lib.gdn_selftest_wait_timeout.argtypes = [u32p, ctypes.c_uint32, vp]
+        lib.gdn_noalloc_scratch_peek.argtypes = [vp, i32]
         for f in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_decode_advance",
                   "gdn_replayssm_decode_advance_noalloc", "gdn_replayssm_advance", "gdn_replayssm_flush",
                   "gdn_replayssm_reset_slots", "gdn_replayssm_spec_verify", "gdn_replayssm_spec_commit",
-                  "gdn_lossless_verify", "gdn_lossless_commit", "gdn_selftest_wait_timeout"):
+                  "gdn_lossless_verify", "gdn_lossless_commit", "gdn_selftest_wait_timeout",
+                  "gdn_noalloc_scratch_peek"):
             getattr(lib, f).restype = ctypes.c_int
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
@@ -174,7 +177,7 @@ def _pack_step(d: LayerDesc, s: Step) -> _Step:
                  _dev(s.beta, "beta", (B, HV), torch.float32),
                  _dev(s.ssm_state_indices, "ssm_state_indices", (B,), torch.int32),
                  B, float(s.q_scale), int(bool(s.qk_l2norm)),
-                 _dev(s.out, "out", (B, HV, V)), GDN_DTYPE[s.out.dtype])
+                 _dev(s.out, "out", (B, HV, V)), GDN_DTYPE[s.out.dtype], int(s.flags))
 
 
 def _pack_cache(d: LayerDesc, c: Cache) -> _Cache:
@@ -254,6 +257,15 @@ def gdn_replayssm_decode_advance_noalloc(desc: LayerDesc, cache: Cache, write_po
         ctypes.byref(s), int(recon),
         _dev(flushed_out, "flushed_out", (B,), torch.uint8, optional=True),
         _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_decode_advance_noalloc")
+
+
+def gdn_noalloc_scratch_peek(n: int = 1):
+    """The first n 32-bit words of the no-alloc entry point's scratch array on
+    the current device (a blocking copy; for tests and diagnostics)."""
+    buf = (ctypes.c_uint32 * n)()
+    _check(load_library().gdn_noalloc_scratch_peek(ctypes.cast(buf, ctypes.c_void_p), int(n)),
+           "gdn_noalloc_scratch_peek")
+    return list(buf)
 
 
 def _pack_spec_step(desc: LayerDesc, T: int, step: Step) -> _SpecStep:

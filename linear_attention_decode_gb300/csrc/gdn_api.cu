@@ -57,6 +57,7 @@ gdn_status_t check_step(const gdn_layer_desc_t *d, const gdn_step_t *s) {
     return fail(GDN_ERR_INVALID_ARG, "qkv_row_stride is shorter than 2*HK*K + HV*V");
   if ((int64_t)s->batch * d->num_v_heads >= (int64_t)1 << 31)
     return fail(GDN_ERR_UNSUPPORTED, "batch * num_v_heads must be < 2^31");
+  if (s->flags & ~GDN_STEP_KNOWN_FLAGS) return fail(GDN_ERR_INVALID_ARG, "unknown bits in step flags");
   return GDN_OK;
 }
 
@@ -83,6 +84,7 @@ void fill_step(gdn::DecodeParams &P, const gdn_step_t *s) {
   P.qk_l2norm = s->qk_l2norm;
   P.out = s->out;
   P.out_dtype = s->out_dtype;
+  P.overlap = (s->flags & GDN_STEP_OVERLAP_PREVIOUS) ? 1 : 0;
 }
 
 gdn_status_t check_cache(const gdn_layer_desc_t *d, const gdn_layer_cache_t *c) {

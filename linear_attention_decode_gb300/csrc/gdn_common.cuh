@@ -46,6 +46,10 @@ struct DecodeParams {
   uint32_t *sync;
   int32_t *write_pos_w;
   int T;  // speculative verify: tokens per row (token t of row b is input row b * T + t)
+  // GDN_STEP_OVERLAP_PREVIOUS (persistent tensor-core kernel only): the launch
+  // before this one leaves the cache, cursors, rows and force_flush alone, so
+  // they may be read before waiting for it
+  int overlap;
 };
 
 __device__ __forceinline__ float load_as_f32(const void *p, int64_t i, int dtype) {
@@ -96,15 +100,18 @@ struct RowInfo {
 };
 
 __device__ __forceinline__ RowInfo resolve_row(const DecodeParams &P, int b, bool report) {
+  // loads cached in L2 only: a kernel may read these before the launch ahead
+  // of it has completed (programmatic dependent launch), and no line of them
+  // left in this SM's L1 by an earlier kernel may be used
   RowInfo r{-1, 0, 0, false, 0u};
-  int slot = P.idx[b];
+  int slot = __ldcg(P.idx + b);
   if (slot < 0) return r;
   if (slot >= P.N) {
     r.bad = GDN_DEV_BAD_SLOT;
     if (report) set_status(P.status, r.bad);
     return r;
   }
-  int p = P.write_pos[slot];
+  int p = __ldcg(P.write_pos + slot);
   if (p < 0 || p >= P.L) {
     r.bad = GDN_DEV_BAD_WRITE_POS;
     if (report) set_status(P.status, r.bad);
@@ -112,7 +119,7 @@ __device__ __forceinline__ RowInfo resolve_row(const DecodeParams &P, int b, boo
   }
   r.slot = slot;
   r.p = p;
-  r.flush = (p == P.L - 1) || (P.force_flush != nullptr && P.force_flush[b] != 0);
+  r.flush = (p == P.L - 1) || (P.force_flush != nullptr && __ldcg(P.force_flush + b) != 0);
   r.live = true;
   return r;
 }
@@ -307,6 +314,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// The same load with an L2 cache policy (e.g. evict-first for data read once).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policy: lines brought in under it are the first to be evicted.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 // Contiguous bulk copy global -> shared (both 16-byte aligned, size a multiple

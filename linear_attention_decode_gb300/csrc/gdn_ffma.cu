@@ -156,7 +156,7 @@ __device__ __forceinline__ float4 mul4(const float4 &a, const float4 &b) {
 // REPLAY = false: packed decode (read S, write S every step).
 // REPLAY = true:  ReplaySSM decode with the replay sum on the CUDA cores.
 // OUT_ONLY (with REPLAY): a non-flush row never forms the replayed state; its
-// readout is factored through the ring ([P1] Design 1 "output-only"; [P2] 3.2):
+// readout is factored through the ring ([P1] Design 1, the output-only form; [P2] 3.2):
 //   GDN: S x = A (S0 x) + sum_j (w_j d_j) (k_j . x),
 //   KDA: S x = S0 (A o x) + sum_j d_j ((w_j o k_j) . x),   x = q, k (KDA: a o q, a o k),
 // O(V K + p (V + K)) per head instead of O(p V K).  Flush rows rebuild S as above.
@@ -779,9 +779,10 @@ __global__ void __launch_bounds__(kThreads) lossless_commit_kernel(const DecodeP
   }
 }
 
-// Commit after verification ([P3] "rollback is a cursor move"): the cursor
-// moves over the accepted tokens only; a slot whose next window would not fit
-// (p + a + T > L - 1) is listed in flush_slots (else -1) for a fold.
+// Commit after verification ([P3] Core concept: rejecting drafts only moves
+// the cursor): the cursor moves over the accepted tokens only; a slot whose
+// next window would not fit (p + a + T > L - 1) is listed in flush_slots
+// (else -1) for a fold.
 __global__ void spec_commit_kernel(const int32_t *idx, const int32_t *accepted, int B, int T, int N, int L,
                                    int32_t *write_pos, int32_t *flush_slots, uint32_t *status) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;

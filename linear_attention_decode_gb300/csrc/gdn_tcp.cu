@@ -247,7 +247,27 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   const int qes = P.qkv_dtype == GDN_F32 ? 4 : 2;
 
   if (smem_addr(smem) & 1023u) {  // the 128-byte swizzle assumes a 1024-byte aligned base
-    if (tid == 0) set_status(P.status, GDN_DEV_INTERNAL);
+    // No item runs.  A decode + advance launch still counts this block, so the
+    // counter ends the launch at zero, and the last block to count moves the
+    // cursors as the call promises (every other block has read them by then).
+    grid_dependency_wait();
+    grid_launch_dependents();
+    uint32_t last = 0u;
+    if (tid == 0) {
+      set_status(P.status, GDN_DEV_INTERNAL);
+      if (P.sync) {
+        __threadfence();
+        last = atomicAdd(P.sync, 1u) == gridDim.x - 1u ? 1u : 0u;
+      }
+    }
+    if (__syncthreads_or(last != 0u)) {
+      __threadfence();
+      for (int b = tid; b < P.B; b += kTcpThreads) {
+        const RowInfo ri = resolve_row(P, b, false);
+        if (ri.live) P.write_pos_w[ri.slot] = ri.flush ? 0 : ri.p + 1;
+      }
+      if (tid == 0) *P.sync = 0u;
+    }
     return;
   }
   int4 *table = reinterpret_cast<int4 *>(smem + lay.off_table);
@@ -273,32 +293,41 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   // Set-up that reads nothing an earlier kernel writes: barriers, TMEM, the
   // tensor map.  With a programmatic dependency on the previous launch in the
   // stream it overlaps that launch's tail; everything after the dependency
-  // wait (the cursors, the rows, the cache) sees the previous launch complete.
-  if (tid == 0) {
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(bars.bf(i), 1);
-      mbar_init(bars.be(i), 4);  // one arrival per epilogue warp
+  // wait sees the previous launch complete.  Without GDN_STEP_OVERLAP_PREVIOUS
+  // every thread waits before the dealing; with it the dealing (rows, cursors)
+  // and the producer's checkpoint stream run first, and the other roles wait
+  // before they read the step's inputs or write anything.  The next launch is
+  // let in only after this block has waited, so a launch never starts while
+  // the one two places ahead of it is still running.
+  // The last warp does this set-up, its lanes side by side, while the others
+  // start dealing the rows (it holds rows only when B > 512).  Barriers in
+  // address order: box full / empty, land full, info full / empty, tile
+  // empty, TMEM full / empty; the "empty" ones count one arrival per consumer
+  // warp, the others one arrival (or the transaction bytes).
+  constexpr int kSetupWarp = kTcpThreads / 32 - 1;
+  if (warp == kSetupWarp) {
+    const int nbar = 2 * NB + NL + 2 * NF + NT + 8;
+    for (int i = lane; i < nbar; i += 32) {
+      int k = i;
+      uint32_t count = 1;
+      if (k >= NB && k < 2 * NB) count = 4;  // one arrival per epilogue warp
+      k -= 2 * NB + NL;
+      if (k >= NF && k < 2 * NF) count = 4;
+      k -= 2 * NF + NT;
+      if (k >= 4 && k < 8) count = 4;
+      mbar_init(bar0 + 8u * (uint32_t)i, count);
     }
-    for (int i = 0; i < NL; ++i) mbar_init(bars.lf(i), 1);
-    for (int i = 0; i < NF; ++i) {
-      mbar_init(bars.inf(i), 1);
-      mbar_init(bars.ine(i), 4);
-    }
-    for (int i = 0; i < NT; ++i) mbar_init(bars.tle(i), 1);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(bars.tf(i), 1);
-      mbar_init(bars.te(i), 4);
-    }
-    misc[1] = 0u;
+    if (lane == 0) misc[1] = 0u;
     fence_mbar_init();
-  }
-  if (warp == 0) {
     tmem_alloc(smem_addr(misc), 4 * D);
     tmem_relinquish();
   }
   if (tid == 32) prefetch_tensormap(&tmap);
-  grid_launch_dependents();
-  grid_dependency_wait();
+  const bool overlap = P.overlap != 0;
+  if (!overlap) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
 
   // --- dealing: the item table of this CTA ---
   // Every CTA classifies every row: live without flush (0), live with flush (1)
@@ -330,7 +359,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         j = r + (y >= 1 ? min(nf, (y - 1) / 2 + 1) : 0);
       }
       const int hv = t - t_lo;
-      if (hv == 0) {  // the CTA holding head 0 reports the row
+      if (hv == 0 && !overlap) {  // the CTA holding head 0 reports the row (with overlap: block 0, later)
         if (ri.bad) set_status(P.status, ri.bad);
         if (P.flushed) P.flushed[b] = ri.live ? (uint8_t)ri.flush : 0;
       }
@@ -353,14 +382,32 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   if (P.B <= kTcpThreads) {  // one row per thread: one pass, one barrier
     const bool in = tid < P.B;
     const RowInfo ri = in ? resolve_row(P, tid, false) : RowInfo{-1, 0, 0, false, 0u};
-    if (P.sync) advq[tid] = (in && ri.live) ? ((ri.slot << 7) | (ri.flush ? 0 : ri.p + 1)) : -1;
+    // row tid: slot << 7 | next cursor when live (next == 0: flush), else -1
+    // (padding) or -1 - its status bit (an invalid slot or cursor)
+    advq[tid] = ri.live ? ((ri.slot << 7) | (ri.flush ? 0 : ri.p + 1)) : -1 - (int)ri.bad;
     int rank = 0;
     const int cat = classify(ri, in, rank);
     __syncthreads();
-    for (int w = 0; w < NW; ++w) {
-      NNF += wc[w];
-      NFL += wc[32 + w];
-      if (w < warp && cat < 3) rank += wc[cat * 32 + w];
+    {
+      // lane w holds warp w's counts; totals and this warp's offset by shuffles
+      const int c0 = lane < NW ? wc[lane] : 0, c1 = lane < NW ? wc[32 + lane] : 0,
+                c2 = lane < NW ? wc[64 + lane] : 0;
+      NNF = c0;
+      NFL = c1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        NNF += __shfl_xor_sync(0xffffffffu, NNF, o);
+        NFL += __shfl_xor_sync(0xffffffffu, NFL, o);
+      }
+      // counts of each category in the warps ahead of this one
+      int b0 = lane < warp ? c0 : 0, b1 = lane < warp ? c1 : 0, b2 = lane < warp ? c2 : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        b0 += __shfl_xor_sync(0xffffffffu, b0, o);
+        b1 += __shfl_xor_sync(0xffffffffu, b1, o);
+        b2 += __shfl_xor_sync(0xffffffffu, b2, o);
+      }
+      if (cat < 3) rank += cat == 0 ? b0 : (cat == 1 ? b1 : b2);
     }
     if (cat < 3) place(ri, tid, cat, rank, NNF, NFL);
   } else {  // a pass to count the categories, then one to rank and place the rows
@@ -413,7 +460,12 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // (never waits for the previous launch with overlap: it reads only this
+    // layer's checkpoint, which that launch does not write)
     if (lane == 0) {
+      // each checkpoint box is read once: let it leave L2 first, so the rows,
+      // cursors and inputs of the next launches stay there
+      const uint64_t policy = l2_policy_evict_first();
       // Each epilogue group has its own NBg box slots (its items' boxes only),
       // so consecutive users of a slot are always the same group: a slot's
       // barrier can then never be waited on a lap ahead of its last phase.
@@ -434,7 +486,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
           const int bs = g * NBg + bp.i();
           if (bp.lapped() && !(ok = wait_bar(bars.be(bs), bp.ph() ^ 1u, abort_flag, P.status))) break;
           mbar_arrive_expect_tx(bars.bf(bs), BOX_BYTES);
-          tma_load_2d(smem_addr(boxes + bs * BOX_BYTES), &tmap, 32 * c, row0, bars.bf(bs));
+          tma_load_2d_hint(smem_addr(boxes + bs * BOX_BYTES), &tmap, 32 * c, row0, bars.bf(bs), policy);
           bp.advance(1, NBg);
         }
         ++li;
@@ -448,6 +500,10 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     // ------------------------------------------------------------ prep + MMA
     // Group pg takes the live items with li % 2 == pg; its leader also issues
     // the item's contraction into TMEM accumulator 2 pg + (li / 2) % 2.
+    if (overlap) {  // the step's inputs come from the previous launch's stream order
+      grid_dependency_wait();
+      if (tid == 32) grid_launch_dependents();
+    }
     const int pg = (warp - 1) >> 2;
     const int pt = tid - 32 - 128 * pg;  // 0..127: operand row / key channel
     const uint32_t bar_id = 1 + pg;
@@ -724,6 +780,26 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (2 groups)
+    if (overlap) {
+      // nothing is written before the previous launch has completed
+      grid_dependency_wait();
+      if (warp == 9 && blockIdx.x == 0) {
+        // the rows' flush flags and status bits, held back by the dealing
+        if (P.B <= kTcpThreads) {
+          for (int b = lane; b < P.B; b += 32) {
+            const int q = advq[b];
+            if (q < -1) set_status(P.status, (uint32_t)(-1 - q));
+            if (P.flushed) P.flushed[b] = (q >= 0 && (q & 127) == 0) ? 1 : 0;
+          }
+        } else {  // read again: nothing moves the cursors before this block has counted
+          for (int b = lane; b < P.B; b += 32) {
+            const RowInfo ri = resolve_row(P, b, false);
+            if (ri.bad) set_status(P.status, ri.bad);
+            if (P.flushed) P.flushed[b] = ri.live ? (uint8_t)ri.flush : 0;
+          }
+        }
+      }
+    }
     // Decode + advance with one row per thread ([P1] Design 3): every CTA has
     // read its cursors by the end of the dealing, so the last CTA to get past
     // it may advance them at once.  The first epilogue warp does it while it
@@ -904,7 +980,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kSetupWarp) {  // the warp that allocated
     tc_fence_after();
     tmem_dealloc(tmem, 4 * D);
   }
@@ -987,7 +1063,7 @@ cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUte
       ((reinterpret_cast<uintptr_t>(P.qkv) & 15u) == 0 && ((P.qkv_stride * qes) & 15) == 0) ? 1 : 0;
   if (gate == GDN_GATE_PER_K && (reinterpret_cast<uintptr_t>(P.ring_g) & 15u) != 0) return cudaErrorNotSupported;
   if (P.HV >= 32768) return cudaErrorNotSupported;  // the item table packs hv and hk into 16 bits each
-  if (P.sync && P.N >= (1 << 24)) return cudaErrorNotSupported;  // decode + advance packs the slot in 24 bits
+  if (P.N >= (1 << 24)) return cudaErrorNotSupported;  // the dealing packs a row's slot in 24 bits
   const int T = P.B * P.HV;
   int grid = sms > 0 && sms < T ? sms : T;
   if ((T + grid - 1) / grid > kItemsMax) grid = (T + kItemsMax - 1) / kItemsMax;

@@ -368,7 +368,7 @@ int oracle_replay_fold(const oracle_geom *G, double *state, const double *ring_d
 }
 
 /* ------------------------------------------------------------------------- */
-/* Speculative-decode verify window and commit ([P3] "Core concept" and       */
+/* Speculative-decode verify window and commit ([P3] Core concept and       */
 /* "Design notes"): one checkpoint plus the ring; a window of T tokens is     */
 /* decoded from the committed ring and the window's own earlier tokens, every */
 /* token's (d, k, g) goes into the ring after the committed entries, and a    */

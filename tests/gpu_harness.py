@@ -142,9 +142,13 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
                force: Optional[Callable[[int, int], np.ndarray]] = None,
                out_dtype=torch.float32, layers: int = 1, tol: Optional[float] = None,
                check_untouched: bool = True, q_scale: float = 1.0, qk_l2norm: bool = False,
-               tweak: Optional[Callable[[int, "I.StepInputs"], None]] = None) -> RunReport:
+               tweak: Optional[Callable[[int, "I.StepInputs"], None]] = None, overlap: bool = False,
+               outputs: Optional[list] = None) -> RunReport:
     """Runs `steps` decode steps of `layers` layers sharing one cursor array
-    on both sides and asserts parity after every step."""
+    on both sides and asserts parity after every step.  overlap: every layer
+    but the first is launched with STEP_OVERLAP_PREVIOUS (the launch before it
+    touches neither its cache nor the cursors).  outputs: if given, receives
+    each step's outputs (float64, [rows, HV, V]) of every layer."""
     steps = w.steps if steps is None else steps
     tol = tolerance(w, recon) if tol is None else tol
     gen = I.generator(w.seed, "cpu")
@@ -173,8 +177,10 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
                 tweak(t, si)
             step_guards: list = []
             out = guarded(torch.full((rows, w.HV, w.V), float("nan"), dtype=out_dtype), step_guards)
+            flags = Bd.STEP_OVERLAP_PREVIOUS if (overlap and li > 0) else 0
             step = Bd.Step(guarded(si.mixed_qkv, step_guards), guarded(si.g, step_guards),
-                           guarded(si.beta, step_guards), idx_dev, out, q_scale=q_scale, qk_l2norm=qk_l2norm)
+                           guarded(si.beta, step_guards), idx_dev, out, q_scale=q_scale, qk_l2norm=qk_l2norm,
+                           flags=flags)
             Bd.gdn_replayssm_decode(desc, layer.dev, wp_dev, ff_dev, step, recon, flushed, status)
             o_ref, fl_ref, st_ref = O.replay_decode(G, layer.ora, wp_ora, idx.numpy(), ff,
                                                     si.mixed_qkv, si.g, si.beta, q_scale, int(qk_l2norm))
@@ -182,6 +188,8 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
             assert st_ref == 0 and int(status.item()) == 0, f"status gpu={status.item()} oracle={st_ref}"
             assert np.array_equal(flushed.cpu().numpy(), fl_ref), f"flush flags differ at step {t}"
             o = out.float().cpu().numpy()
+            if outputs is not None:
+                outputs.append(o.astype(np.float64))
             assert np.all(o[~live] == 0.0), "padding rows must be exactly zero"
             ref = o_ref
             if out_dtype != torch.float32:

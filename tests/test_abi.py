@@ -39,9 +39,9 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} is declared in include/ but not exported"
 
 
-def _step(batch=4, row=2 * 16 * 128 + 32 * 128):
+def _step(batch=4, row=2 * 16 * 128 + 32 * 128, flags=0):
     fake = ctypes.c_void_p(0x1000)  # never dereferenced: every case below fails a host check
-    return Bd._Step(fake, Bd.BF16, row, fake, fake, fake, batch, 1.0, 0, fake, Bd.F32)
+    return Bd._Step(fake, Bd.BF16, row, fake, fake, fake, batch, 1.0, 0, fake, Bd.F32, flags)
 
 
 def _desc(**kw):
@@ -81,6 +81,7 @@ def test_decode_rejects_bad_pointers_and_sizes(lib):
         (good, _step(batch=-1), 0x1000, 0),                                 # negative batch
         (good, _step(), None, 0),                                           # no write_pos
         (good, _step(), 0x1000, 5),                                         # unknown recon
+        (good, _step(flags=2), 0x1000, 0),                                  # unknown step flag
     ]
     for cache, step, wp, recon in calls:
         st = lib.gdn_replayssm_decode(ctypes.byref(d), ctypes.byref(cache), wp, None, ctypes.byref(step),
@@ -187,3 +188,18 @@ def test_wait_selftest_checks_its_arguments(lib):
     assert f(None, 10, None) == 1         # no status word
     assert f(0x1000, 0, None) == 1        # limit below 1 us
     assert f(0x1000, 100001, None) == 1   # limit above 100 ms
+
+
+def test_step_flag_constants_match_the_header():
+    text = open(os.path.join(ROOT, "include", "gdnreplay.h")).read()
+    m = re.search(r"#define GDN_STEP_OVERLAP_PREVIOUS\s+(\d+)u", text)
+    assert m and int(m.group(1)) == Bd.STEP_OVERLAP_PREVIOUS
+    m = re.search(r"#define GDN_STEP_KNOWN_FLAGS\s+(\d+)u", text)
+    assert m and int(m.group(1)) == Bd.STEP_OVERLAP_PREVIOUS
+
+
+def test_scratch_peek_checks_its_arguments(lib):
+    buf = (ctypes.c_uint32 * 64)()
+    for n in (0, -1, 65):
+        assert lib.gdn_noalloc_scratch_peek(ctypes.cast(buf, ctypes.c_void_p), n) == 1
+    assert lib.gdn_noalloc_scratch_peek(None, 1) == 1

@@ -121,3 +121,65 @@ def test_decode_advance_stack_shares_one_cursor_array(gdnlib):
         torch.cuda.synchronize()
         assert torch.equal(wp_got, wp_ref), f"step {t}: cursors differ"
     assert int(ws.item()) == 0
+
+
+OVERLAP_CASES = {
+    # more items than SMs, so consecutive launches really share the GPU
+    "persistent": I.Workload("overlap", N=96, B=48, n_pad=3, HV=8, HK=4, K=128, L=8, ring_dtype=Bd.F16,
+                             qkv_dtype=Bd.BF16, steps=10, staggered=True, seed=41),
+    # more rows than threads: block 0 reads the rows again for their flush flags
+    "rows_beyond_one_pass": I.Workload("overlap 600", N=700, B=600, n_pad=3, HV=2, HK=1, K=64, L=4,
+                                       ring_dtype=Bd.F16, qkv_dtype=Bd.BF16, steps=6, staggered=True, seed=42),
+}
+
+
+@pytest.mark.parametrize("name", list(OVERLAP_CASES))
+def test_overlap_flag_back_to_back_is_bitwise_the_same(gdnlib, name):
+    """Three layers per forward launched back to back with no host sync, the
+    last also advancing the cursors: with STEP_OVERLAP_PREVIOUS on the second
+    and third layer (their launches may start, read rows and cursors and stream
+    checkpoints while the previous layer's launch is still running) every
+    output, flush flag, cache and cursor equals the run without the flag bit
+    for bit, and the workspace ends at zero."""
+    w = OVERLAP_CASES[name]
+    layers = 3
+    gen = I.generator(w.seed, "cuda")
+    wp0 = I.write_pos(gen, w, "cuda")
+    c0 = [I.cache(gen, w, wp0, "cuda") for _ in range(layers)]
+    idx = I.indices(gen, w.B, w.N, w.n_pad, "cuda")
+    rows = idx.shape[0]
+    inputs = [[I.step_inputs(gen, w, "cuda") for _ in range(layers)] for _ in range(w.steps)]
+    desc = desc_of(w)
+
+    def run(flagged: bool):
+        caches = [Bd.Cache(c.state.clone(), c.ring_d.clone(), c.ring_k.clone(), c.ring_g.clone()) for c in c0]
+        wp = wp0.clone()
+        ws = Bd.decode_advance_workspace()
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        outs = torch.full((w.steps, layers, rows, w.HV, w.V), float("nan"), device="cuda")
+        fls = torch.full((w.steps, layers, rows), 7, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        for t in range(w.steps):
+            for layer in range(layers):
+                si = inputs[t][layer]
+                flags = Bd.STEP_OVERLAP_PREVIOUS if (flagged and layer > 0) else 0
+                step = Bd.Step(si.mixed_qkv, si.g, si.beta, idx, outs[t, layer], flags=flags)
+                if layer < layers - 1:
+                    Bd.gdn_replayssm_decode(desc, caches[layer], wp, None, step, TC, fls[t, layer], st)
+                else:
+                    Bd.gdn_replayssm_decode_advance(desc, caches[layer], wp, None, step, ws, TC, fls[t, layer], st)
+        torch.cuda.synchronize()
+        return caches, wp, outs, fls, int(ws.item()), int(st.item())
+
+    ref = run(False)
+    got = run(True)
+    assert ref[4] == 0 and got[4] == 0, "workspace not left at zero"
+    assert ref[5] == 0 and got[5] == 0, "status"
+    assert torch.equal(got[1], ref[1]), "cursors differ"
+    assert torch.equal(got[3], ref[3]), "flush flags differ"
+    assert int((ref[3] == 1).sum()) > 0, "the run should include flushing rows"
+    assert _same_bits(got[2], ref[2]), "outputs differ"
+    for layer in range(layers):
+        for name_ in ("state", "ring_d", "ring_k", "ring_g"):
+            assert _same_bits(getattr(got[0][layer], name_), getattr(ref[0][layer], name_)), \
+                f"layer {layer} {name_} differs"
