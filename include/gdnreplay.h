@@ -183,6 +183,23 @@ GDN_API gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gd
                                   const gdn_step_t *step, int32_t recon, uint8_t *flushed_out,
                                   uint32_t *dev_status, gdn_stream_t stream);
 
+/* Which kernel gdn_replayssm_decode (and _decode_advance) would launch for
+ * these arguments, without launching anything (host only; reads the current
+ * device's SM count and shared-memory limit).  *kernel receives one of:
+ *   GDN_KERNEL_PERSISTENT_TC  persistent warp-specialised tensor-core kernel,
+ *                             one block per SM (TENSOR recon)
+ *   GDN_KERNEL_PER_HEAD_TC    one block per (row, value head), tensor cores
+ *                             (TENSOR recon whose layout does not fit the
+ *                             persistent kernel)
+ *   GDN_KERNEL_CUDA_CORE      CUDA-core kernel (FFMA or OUTPUT recon)
+ * Argument checks and errors as in gdn_replayssm_decode.  No counterpart in
+ * the pages: a diagnostic of this library's dispatch. */
+#define GDN_KERNEL_PERSISTENT_TC 0
+#define GDN_KERNEL_PER_HEAD_TC   1
+#define GDN_KERNEL_CUDA_CORE     2
+GDN_API gdn_status_t gdn_replayssm_decode_kernel(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
+                                                 const gdn_step_t *step, int32_t recon, int32_t *kernel);
+
 /* gdn_replayssm_decode of the forward's last layer followed by
  * gdn_replayssm_advance for the same rows, with the same results as the two
  * calls: the cursors are read before any is advanced.  On the tensor-core path

@@ -113,11 +113,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_lossless_commit.argtypes = [dp, vp, vp, vp, vp, i32, i32, vp, vp, vp, u32p, vp]
         lib.gdn_selftest_wait_timeout.argtypes = [u32p, ctypes.c_uint32, vp]
         lib.gdn_noalloc_scratch_peek.argtypes = [vp, i32]
+        lib.gdn_replayssm_decode_kernel.argtypes = [dp, cp, sp, i32, vp]
         for f in ("gdn_packed_decode", "gdn_replayssm_decode", "gdn_replayssm_decode_advance",
                   "gdn_replayssm_decode_advance_noalloc", "gdn_replayssm_advance", "gdn_replayssm_flush",
                   "gdn_replayssm_reset_slots", "gdn_replayssm_spec_verify", "gdn_replayssm_spec_commit",
                   "gdn_lossless_verify", "gdn_lossless_commit", "gdn_selftest_wait_timeout",
-                  "gdn_noalloc_scratch_peek"):
+                  "gdn_noalloc_scratch_peek", "gdn_replayssm_decode_kernel"):
             getattr(lib, f).restype = ctypes.c_int
         lib.gdn_status_str.argtypes = [ctypes.c_int]
         lib.gdn_status_str.restype = ctypes.c_char_p
@@ -214,6 +215,20 @@ def gdn_replayssm_decode(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor,
         ctypes.byref(s), int(recon),
         _dev(flushed_out, "flushed_out", (B,), torch.uint8, optional=True),
         _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_decode")
+
+
+# gdn_replayssm_decode_kernel results
+KERNEL_PERSISTENT_TC, KERNEL_PER_HEAD_TC, KERNEL_CUDA_CORE = 0, 1, 2
+
+
+def gdn_replayssm_decode_kernel(desc: LayerDesc, cache: Cache, step: Step, recon: int = RECON_TENSOR) -> int:
+    """Which decode kernel a call with these arguments would launch (host only)."""
+    c = _pack_cache(desc, cache)
+    s = _pack_step(desc, step)
+    out = ctypes.c_int32(-1)
+    _check(load_library().gdn_replayssm_decode_kernel(ctypes.byref(desc), ctypes.byref(c), ctypes.byref(s),
+                                                      int(recon), ctypes.byref(out)), "gdn_replayssm_decode_kernel")
+    return int(out.value)
 
 
 DECODE_ADVANCE_WORKSPACE_BYTES = 4

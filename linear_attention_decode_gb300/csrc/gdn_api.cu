@@ -172,6 +172,29 @@ gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gdn_layer_
   return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_replayssm_decode launch");
 }
 
+gdn_status_t gdn_replayssm_decode_kernel(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
+                                         const gdn_step_t *step, int32_t recon, int32_t *kernel) {
+  gdn_status_t st = check_desc(desc);
+  if (st != GDN_OK) return st;
+  if ((st = check_step(desc, step)) != GDN_OK) return st;
+  if ((st = check_cache(desc, cache)) != GDN_OK) return st;
+  if (!kernel) return fail(GDN_ERR_INVALID_ARG, "kernel is NULL");
+  if (recon != GDN_RECON_TENSOR && recon != GDN_RECON_FFMA && recon != GDN_RECON_OUTPUT)
+    return fail(GDN_ERR_INVALID_ARG, "recon must be GDN_RECON_TENSOR, GDN_RECON_FFMA or GDN_RECON_OUTPUT");
+  if (recon != GDN_RECON_TENSOR) {
+    *kernel = GDN_KERNEL_CUDA_CORE;
+    return GDN_OK;
+  }
+  gdn::DecodeParams P = base_params(desc);
+  fill_step(P, step);
+  P.state = cache->state;
+  P.ring_d = cache->ring_d;
+  P.ring_k = cache->ring_k;
+  P.ring_g = cache->ring_g;
+  *kernel = gdn::tcp_decode_fits(P, desc->k_dim, desc->gate) ? GDN_KERNEL_PERSISTENT_TC : GDN_KERNEL_PER_HEAD_TC;
+  return GDN_OK;
+}
+
 gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
                                           int32_t *write_pos, const uint8_t *force_flush,
                                           const gdn_step_t *step, int32_t recon, uint8_t *flushed_out,

@@ -348,6 +348,9 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
                : "memory");
 }
 
+// Waits until every cp.async this thread has issued has landed in shared memory.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // One arrival on `bar` once every cp.async this thread issued so far has
 // landed; the arrival is not added to the barrier's expected count, so the
 // barrier must have been initialised to include it.

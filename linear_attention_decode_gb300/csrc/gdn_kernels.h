@@ -26,6 +26,8 @@ cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_
 // cudaErrorNotSupported, with nothing launched, when its shared-memory layout
 // does not fit the configuration.
 cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUtensorMap &map, cudaStream_t s);
+// Whether launch_tcp_decode would take this launch (host-side, launches nothing).
+bool tcp_decode_fits(const DecodeParams &P, int D, int gate);
 
 cudaError_t launch_fold(const DecodeParams &P, int D, int gate, int n, cudaStream_t s);
 

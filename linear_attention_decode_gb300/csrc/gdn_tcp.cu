@@ -42,9 +42,15 @@ namespace gdn {
 
 constexpr int kTcpThreads = 544;  // 17 warps
 constexpr int kItemsMax = 256;    // items one CTA may own (sets the table size)
+// Ring entries per landing slot and per operand tile stage when the whole
+// replay depth does not fit the shared-memory layout: the replay then runs in
+// chunks of kChunk entries that accumulate into the same TMEM accumulator;
+// chunks past the first come straight from the ring in global memory.
+constexpr int kChunk = 16;
 
 struct TcpLayout {
   int KD, KC, NT, NF, NL, NB;
+  int CH;        // ring entries per replay chunk (>= the deepest replay: one chunk)
   int qkv_bulk;  // 1: q, k, v arrive by bulk copy (16-byte aligned rows)
   uint32_t box_bytes, tile_bytes, field_bytes, land_bytes;
   uint32_t off_tile, off_field, off_land, off_table, off_adv, off_bars, total;
@@ -61,12 +67,14 @@ __host__ __device__ inline int field_floats(int D, int gate) { return (gate == G
 // Shared memory: NB checkpoint boxes | NT operand tile stages | NF field stages
 // | NL landing slots | item table | barriers.
 static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, int qkv_bytes, int qkv_bulk,
-                            int NT, int NL, int smem_budget) {
+                            int NT, int NL, int smem_budget, bool chunked) {
   TcpLayout t{};
   const int es = kind == 2 ? 4 : 2;
   const int kstep = 32 / es;
   const int depth = L > 1 ? L - 1 : 0;
-  t.KD = depth ? ((depth + kstep - 1) / kstep) * kstep : 0;
+  const int ldep = chunked && depth > kChunk ? kChunk : depth;  // ring entries of one chunk
+  t.CH = chunked && depth > kChunk ? kChunk : (depth > 0 ? depth : 1);
+  t.KD = ldep ? ((ldep + kstep - 1) / kstep) * kstep : 0;
   t.KC = t.KD * es / 16;
   t.qkv_bulk = qkv_bulk;
   t.box_bytes = (uint32_t)D * 128;
@@ -74,9 +82,9 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
   t.tile_bytes = (t.t_B + (uint32_t)(D * t.KD * es) + 127) & ~127u;
   t.field_bytes = ((uint32_t)field_floats(D, gate) * 4 + 127) & ~127u;
   t.ld_d = 0;
-  t.ld_k = t.ld_d + (uint32_t)(depth * D * ring_bytes);
-  t.ld_g = t.ld_k + (uint32_t)(depth * D * ring_bytes);
-  t.ld_q = t.ld_g + (uint32_t)(gate == GDN_GATE_PER_K ? depth * D * 4 : 0);
+  t.ld_k = t.ld_d + (uint32_t)(ldep * D * ring_bytes);
+  t.ld_g = t.ld_k + (uint32_t)(ldep * D * ring_bytes);
+  t.ld_q = t.ld_g + (uint32_t)(gate == GDN_GATE_PER_K ? ldep * D * 4 : 0);
   t.land_bytes = (t.ld_q + (uint32_t)(qkv_bulk ? 3 * D * qkv_bytes : 0) + 127) & ~127u;
   const uint32_t table = (uint32_t)kItemsMax * 16;  // item table
   const uint32_t adv = (uint32_t)kTcpThreads * 4;  // the rows' next cursors (decode + advance)
@@ -99,16 +107,23 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
 }
 
 // The first (tile stages, landing slots) choice that leaves room for two items'
-// checkpoint boxes plus one more; else the one with the most boxes.
+// checkpoint boxes plus one more; else the one with the most boxes.  The whole
+// replay depth in one chunk first (one contraction per item, nothing loaded
+// past the landing); chunks of kChunk entries only when that leaves too few
+// boxes (fp32 rings beyond L = 17, any ring beyond L = 33).
 static TcpLayout tcp_pick_layout(int D, int kind, int gate, int L, int ring_bytes, int qkv_bytes, int qkv_bulk,
                                  int smem_budget) {
   static const int cand[4][2] = {{4, 4}, {2, 4}, {4, 2}, {2, 2}};
   const int want = 2 * (D / 32) + 1;
   TcpLayout best{};
-  for (const auto &c : cand) {
-    const TcpLayout t = tcp_layout(D, kind, gate, L, ring_bytes, qkv_bytes, qkv_bulk, c[0], c[1], smem_budget);
-    if (t.NB >= want) return t;
-    if (t.NB > best.NB) best = t;
+  for (int chunked = 0; chunked < 2; ++chunked) {
+    for (const auto &c : cand) {
+      const TcpLayout t =
+          tcp_layout(D, kind, gate, L, ring_bytes, qkv_bytes, qkv_bulk, c[0], c[1], smem_budget, chunked != 0);
+      if (t.NB >= want) return t;
+      if (t.NB > best.NB) best = t;
+    }
+    if (best.NB >= 2 * (D / 32)) return best;  // enough for the pipeline without chunks
   }
   return best;
 }
@@ -513,6 +528,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     int li = 0, land_next = pg;  // leader: next live item to land
     int last_acc = -1;           // leader: accumulator and use count of its last contraction
     uint32_t last_use = 0;
+    bool last_committed = true;  // leader: that contraction's completion is signalled on tmem_full
     const int nlive = (int)misc[4];
     // The group's landing slots (li % NL with NL = 4: two per group) are filled
     // by its own leader two group-items ahead: right after the group has read a
@@ -522,7 +538,8 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
     auto land = [&](int lj) {
       const int4 el = table[lj];  // the live items are the table's first entries
       const int bl = el.z, hvl = tab_hv(el), hkl = tab_hk(el);
-      const int pl = tab_p(el), sl = el.x, l = lp.i();
+      const int pl0 = tab_p(el), sl = el.x, l = lp.i();
+      const int pl = pl0 < lay.CH ? pl0 : lay.CH;  // the first chunk's entries
       lp.advance(2, NL);
       uint8_t *ld = lands + l * lay.land_bytes;
       const uint32_t ring_bytes = (uint32_t)(pl * D * RB);
@@ -565,6 +582,25 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       cp.advance(2, NL);
       const int b = e.z, hv = tab_hv(e), hk = tab_hk(e);
       const int64_t bh = (int64_t)b * P.HV + hv;
+      // GDN with an fp32 ring, chunk c >= 1 of a long replay: this thread's
+      // row of the chunk's raw d and k goes by 4-byte async copies straight
+      // into its place in the chunk's tile stage; the thread later rewrites
+      // its own row in place (w_j d_j and k_j, rounded to tf32).
+      constexpr bool kStaged = RING_DT == GDN_F32 && GATE == GDN_GATE_SCALAR;
+      constexpr int KCC = kChunk * ES / 16;  // 16-byte column chunks of a full chunk
+      auto stage_rows = [&](int c, int tc) {
+        uint8_t *sA = tiles + tc * lay.tile_bytes, *sB = sA + lay.t_B;
+        const float *rd = reinterpret_cast<const float *>(P.ring_d) + ((int64_t)slot * P.HV + hv) * P.L * D + pt;
+        const float *rk = reinterpret_cast<const float *>(P.ring_k) + ((int64_t)slot * P.HK + hk) * P.L * D + pt;
+        if (pt < D) {
+#pragma unroll
+          for (int e2 = 0; e2 < kChunk; ++e2) {
+            const int jj = c * kChunk + e2, jc = jj < p - 1 ? jj : p - 1;
+            cp_async4(smem_addr(sA + tile_off(pt, e2, KCC, 4)), rd + (int64_t)jc * D);
+            cp_async4(smem_addr(sB + tile_off(pt, e2, KCC, 4)), rk + (int64_t)jc * D);
+          }
+        }
+      };
       // small loads first, so their latency overlaps the waits
       float gc = 0.f, qv = 0.f, kv = 0.f, vv = 0.f, g_lo = 0.f, g_hi = 0.f;
       if (GATE == GDN_GATE_SCALAR) {
@@ -594,7 +630,11 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
                   : 0u;
       named_bar_sync(bar_id, 128);
       if (*go == 0u) break;
-      uint8_t *tA = tiles + t * lay.tile_bytes, *tB = tA + lay.t_B;
+      // the newest chunk's stage is free now (checked with the landing): its
+      // copies overlap the work below
+      if constexpr (kStaged) {
+        if (p > lay.CH) stage_rows((p - 1) / kChunk, t);
+      }
       float *f = reinterpret_cast<float *>(fields + s * lay.field_bytes);
       float *fq = f, *fk = f + D, *fv = f + 2 * D, *fke = f + 3 * D, *fa = f + 4 * D, *fA = f + 5 * D,
             *fg = f + 6 * D, *scal = f + NVEC * D;
@@ -641,8 +681,11 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         kq = (pt >> 5) == 0 ? kq / (nq * nk) * P.q_scale : 0.f;
       }
 
-      // Operand rows, newest entry first (GDN: A row pt w_j d_j[pt], B row pt
-      // k_j[pt]; KDA: A row pt d_j[pt], B row pt w_j[pt] k_j[pt]).  Entries
+      // Operand rows, in chunks of kChunk ring entries, the newest chunk first
+      // (GDN: A row pt w_j d_j[pt], B row pt k_j[pt]; KDA: A row pt d_j[pt],
+      // B row pt w_j[pt] k_j[pt]).  Chunk 0 comes from the landing slot, later
+      // chunks straight from the ring in global memory; each chunk fills one
+      // tile stage and is contracted into the item's accumulator.  Entries
       // j >= p are zero (selected, never multiplied: stale ring rows may hold
       // anything); their loads read row min(j, p - 1) of the slot.  The
       // weights w_j are rounded to the operand type right after, so the fast
@@ -652,6 +695,12 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       float A = 1.f;
       const int jmax = p > 0 ? p - 1 : 0;
       const int ptc = pt < D ? pt : 0;
+      const int nch = p > lay.CH ? (p + kChunk - 1) / kChunk : 1;  // lay.CH is kChunk when it chunks
+      const int acc = 2 * pg + ((li >> 1) & 1);
+      const uint32_t ua = (uint32_t)(li >> 2);
+      const int64_t drow = ((int64_t)slot * P.HV + hv) * P.L;  // ring rows of (slot, hv) / (slot, hk)
+      const int64_t krow = ((int64_t)slot * P.HK + hk) * P.L;
+      float w_lo = 0.f, w_hi = 0.f;  // GDN: w_j of entry j sits in lane j (lo: j < 32, hi: j >= 32)
       if (GATE == GDN_GATE_SCALAR) {
         // Suffix sums of the log-gates by a warp scan (each warp on its own):
         // afterwards lane l holds T_l = sum_{l<=i<p} g_i; w_j = exp(T_{j+1}),
@@ -670,52 +719,15 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         }
         t_lo += hi_total;
         A = p > 0 ? expf(__shfl_sync(0xffffffffu, t_lo, 0)) : 1.f;
-        // w for entry j lives in lane j (lo: j < 32, hi: j >= 32)
         const float nxt_lo = __shfl_down_sync(0xffffffffu, t_lo, 1);
-        const float w_lo = __expf(lane == 31 ? hi_total : nxt_lo);
+        w_lo = __expf(lane == 31 ? hi_total : nxt_lo);
         const float nxt_hi = __shfl_down_sync(0xffffffffu, t_hi, 1);
-        const float w_hi = __expf(lane == 31 ? 0.f : nxt_hi);
-        for (int h = 0; h < lay.KC; ++h) {
-          float xa[EPC], xb[EPC];
-#pragma unroll
-          for (int e2 = 0; e2 < EPC; ++e2) {
-            const int jj = h * EPC + e2;
-            const int jc = jj < jmax ? jj : jmax;
-            const bool valid = jj < p && pt < D;
-            const float wj = __shfl_sync(0xffffffffu, jj < 32 ? w_lo : w_hi, jj & 31);
-            const float dj = load_as_f32(land_d, (int64_t)jc * D + ptc, RING_DT);
-            const float kj = load_as_f32(land_k, (int64_t)jc * D + ptc, RING_DT);
-            xa[e2] = valid ? wj * dj : 0.f;
-            xb[e2] = valid ? kj : 0.f;
-          }
-          put_chunk<KIND, EPC>(tA, pt, h, lay.KC, xa);
-          if (pt < D) put_chunk<KIND, EPC>(tB, pt, h, lay.KC, xb);
-        }
-      } else {
-        // channel c = pt: w_j[c] by a backward sum over the channel's gates, so
-        // the chunks of B are filled from the newest entry down
-        float sfx = 0.f;
-        for (int h = lay.KC - 1; h >= 0; --h) {
-          float xa[EPC], xb[EPC];
-#pragma unroll
-          for (int e2 = EPC - 1; e2 >= 0; --e2) {
-            const int jj = h * EPC + e2;
-            const int jc = jj < jmax ? jj : jmax;
-            const bool valid = jj < p && pt < D;
-            const float wj = __expf(sfx);
-            const float gj = land_g[jc * D + ptc];
-            const float dj = load_as_f32(land_d, (int64_t)jc * D + ptc, RING_DT);
-            const float kj = load_as_f32(land_k, (int64_t)jc * D + ptc, RING_DT);
-            sfx += valid ? gj : 0.f;
-            xa[e2] = valid ? dj : 0.f;
-            xb[e2] = valid ? wj * kj : 0.f;
-          }
-          put_chunk<KIND, EPC>(tA, pt, h, lay.KC, xa);
-          if (pt < D) put_chunk<KIND, EPC>(tB, pt, h, lay.KC, xb);
-        }
-        A = expf(sfx);
+        w_hi = __expf(lane == 31 ? 0.f : nxt_hi);
       }
-      // Epilogue inputs.
+      // Epilogue inputs (KDA: all but the total decay per channel, which comes
+      // out of the chunk loop, are written before it; GDN writes them after,
+      // which the register allocation of that variant prefers).
+      auto write_fields = [&]() {
       if (pt < D) {
         fk[pt] = kv;
         fv[pt] = vv;
@@ -724,7 +736,6 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
           fq[pt] = at * qv;
           fke[pt] = at * kv;
           fa[pt] = at;
-          fA[pt] = A;
           fg[pt] = gc;
         } else {
           fq[pt] = qv;
@@ -734,47 +745,203 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       if (pt == 0) {
         scal[0] = GATE == GDN_GATE_SCALAR ? expf(gc) : 1.f;
         scal[1] = beta;
-        scal[2] = A;
         scal[4] = gc;
       }
-      fence_proxy_async_smem();
-      named_bar_sync(bar_id, 128);
-      if (pt == 0) {
-        mbar_arrive(bars.inf(s));
-        // contraction into accumulator acc once the epilogue has read it out
-        const int acc = 2 * pg + ((li >> 1) & 1);
-        const uint32_t ua = (uint32_t)(li >> 2);
-        if (ua > 0 && !wait_bar(bars.te(acc), (ua - 1) & 1, abort_flag, P.status)) {
-          leader_ok = false;
-        } else {
-          tc_fence_after();
-          if (p > 0) {
-            const uint32_t a0 = smem_addr(tA), b0 = smem_addr(tB);
-            const uint32_t sbo = (uint32_t)lay.KC * 128;
-            const int nsteps = (p + KSTEP - 1) / KSTEP;
-            for (int i = 0; i < nsteps; ++i)
-              tc_mma<KIND == 2 ? 1 : 0>(tmem + acc * D, make_sdesc(a0 + 256 * i, 128, sbo),
-                                        make_sdesc(b0 + 256 * i, 128, sbo), idesc, i > 0 ? 1u : 0u);
-            tc_commit(bars.tf(acc));
-            tc_commit(bars.tle(t));
-          } else {
-            mbar_arrive(bars.tf(acc));
-            mbar_arrive(bars.tle(t));
+      };
+      if (GATE == GDN_GATE_PER_K) write_fields();
+      float sfx = 0.f;  // KDA: the sum of this channel's gates newer than the entry at hand
+      bool stop = false;
+      for (int c = nch - 1; c >= 0; --c) {
+        int tc = t;
+        if (c != nch - 1) {  // a later chunk: the next tile stage, once its last contraction is done
+          tc = tp.i();
+          const uint32_t phc = tp.ph();
+          const bool lapc = tp.lapped();
+          tp.advance(2, NT);
+          if (pt == 0)
+            *go = (leader_ok && (!lapc || wait_bar(bars.tle(tc), phc ^ 1u, abort_flag, P.status))) ? 1u : 0u;
+          named_bar_sync(bar_id, 128);
+          if (*go == 0u) {
+            stop = true;
+            break;
           }
-          last_acc = acc;
-          last_use = ua;
-          // the landing slot has been read: fill it for the item that uses it next
-          if (land_next < nlive) {
-            land(land_next);
-            land_next += 2;
+        }
+        uint8_t *tA = tiles + tc * lay.tile_bytes, *tB = tA + lay.t_B;
+        const int j0 = c * kChunk;
+        if (c == 0) {
+          if (GATE == GDN_GATE_SCALAR) {
+            for (int h = 0; h < lay.KC; ++h) {
+              float xa[EPC], xb[EPC];
+#pragma unroll
+              for (int e2 = 0; e2 < EPC; ++e2) {
+                const int jj = h * EPC + e2;
+                const int jc = jj < jmax ? jj : jmax;
+                const bool valid = jj < p && pt < D;
+                const float wj = __shfl_sync(0xffffffffu, jj < 32 ? w_lo : w_hi, jj & 31);
+                const float dj = load_as_f32(land_d, (int64_t)jc * D + ptc, RING_DT);
+                const float kj = load_as_f32(land_k, (int64_t)jc * D + ptc, RING_DT);
+                xa[e2] = valid ? wj * dj : 0.f;
+                xb[e2] = valid ? kj : 0.f;
+              }
+              put_chunk<KIND, EPC>(tA, pt, h, lay.KC, xa);
+              if (pt < D) put_chunk<KIND, EPC>(tB, pt, h, lay.KC, xb);
+            }
+          } else {
+            // channel c = pt: w_j[c] by a backward sum over the channel's
+            // gates, so the chunks of B are filled from the newest entry down
+            for (int h = lay.KC - 1; h >= 0; --h) {
+              float xa[EPC], xb[EPC];
+#pragma unroll
+              for (int e2 = EPC - 1; e2 >= 0; --e2) {
+                const int jj = h * EPC + e2;
+                const int jc = jj < jmax ? jj : jmax;
+                const bool valid = jj < p && pt < D;
+                const float wj = __expf(sfx);
+                const float gj = land_g[jc * D + ptc];
+                const float dj = load_as_f32(land_d, (int64_t)jc * D + ptc, RING_DT);
+                const float kj = load_as_f32(land_k, (int64_t)jc * D + ptc, RING_DT);
+                sfx += valid ? gj : 0.f;
+                xa[e2] = valid ? dj : 0.f;
+                xb[e2] = valid ? wj * kj : 0.f;
+              }
+              put_chunk<KIND, EPC>(tA, pt, h, lay.KC, xa);
+              if (pt < D) put_chunk<KIND, EPC>(tB, pt, h, lay.KC, xb);
+            }
+          }
+        } else if constexpr (kStaged) {
+          // a chunk past the landed one, staged by async copies: rewrite this
+          // thread's own row in place
+          if (c != nch - 1) stage_rows(c, tc);
+          cp_async_wait_all();
+#pragma unroll
+          for (int h = 0; h < KCC; ++h) {
+            const uint32_t off = (uint32_t)((pt >> 3) * (KCC * 128) + h * 128 + (pt & 7) * 16);
+            float4 ra = make_float4(0.f, 0.f, 0.f, 0.f), rb = ra;
+            if (pt < D) {
+              ra = *reinterpret_cast<const float4 *>(tA + off);
+              rb = *reinterpret_cast<const float4 *>(tB + off);
+            }
+            const float rav[4] = {ra.x, ra.y, ra.z, ra.w}, rbv[4] = {rb.x, rb.y, rb.z, rb.w};
+            float xa[EPC], xb[EPC];
+#pragma unroll
+            for (int e2 = 0; e2 < EPC; ++e2) {
+              const int jj = j0 + h * EPC + e2;
+              const bool valid = jj < p && pt < D;
+              const float wj = __shfl_sync(0xffffffffu, jj < 32 ? w_lo : w_hi, jj & 31);
+              xa[e2] = valid ? wj * rav[e2] : 0.f;
+              xb[e2] = valid ? rbv[e2] : 0.f;
+            }
+            put_chunk<KIND, EPC>(tA, pt, h, KCC, xa);
+            if (pt < D) put_chunk<KIND, EPC>(tB, pt, h, KCC, xb);
+          }
+        } else {
+          // a chunk past the landed one, straight from global memory in two
+          // halves, each half's loads in flight at once (registers allow no more)
+          constexpr int HALF = kChunk / 2;
+          constexpr int HPC = KCC / 2;           // column chunks per half
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int half = GATE == GDN_GATE_SCALAR ? hf : 1 - hf;  // KDA walks newest first
+            float dr[HALF], kr[HALF], gr[HALF];
+#pragma unroll
+            for (int e = 0; e < HALF; ++e) {
+              const int jj = j0 + half * HALF + e, jc = jj < jmax ? jj : jmax;
+              dr[e] = load_as_f32(P.ring_d, (drow + jc) * D + ptc, RING_DT);
+              kr[e] = load_as_f32(P.ring_k, (krow + jc) * D + ptc, RING_DT);
+              gr[e] = GATE == GDN_GATE_PER_K ? P.ring_g[(drow + jc) * D + ptc] : 0.f;
+            }
+            if (GATE == GDN_GATE_SCALAR) {
+#pragma unroll
+              for (int hh = 0; hh < HPC; ++hh) {
+                float xa[EPC], xb[EPC];
+#pragma unroll
+                for (int e2 = 0; e2 < EPC; ++e2) {
+                  const int e = hh * EPC + e2, jj = j0 + half * HALF + e;
+                  const bool valid = jj < p && pt < D;
+                  const float wj = __shfl_sync(0xffffffffu, jj < 32 ? w_lo : w_hi, jj & 31);
+                  xa[e2] = valid ? wj * dr[e] : 0.f;
+                  xb[e2] = valid ? kr[e] : 0.f;
+                }
+                put_chunk<KIND, EPC>(tA, pt, half * HPC + hh, KCC, xa);
+                if (pt < D) put_chunk<KIND, EPC>(tB, pt, half * HPC + hh, KCC, xb);
+              }
+            } else {
+#pragma unroll
+              for (int hh = HPC - 1; hh >= 0; --hh) {
+                float xa[EPC], xb[EPC];
+#pragma unroll
+                for (int e2 = EPC - 1; e2 >= 0; --e2) {
+                  const int e = hh * EPC + e2, jj = j0 + half * HALF + e;
+                  const bool valid = jj < p && pt < D;
+                  const float wj = __expf(sfx);
+                  sfx += valid ? gr[e] : 0.f;
+                  xa[e2] = valid ? dr[e] : 0.f;
+                  xb[e2] = valid ? wj * kr[e] : 0.f;
+                }
+                put_chunk<KIND, EPC>(tA, pt, half * HPC + hh, KCC, xa);
+                if (pt < D) put_chunk<KIND, EPC>(tB, pt, half * HPC + hh, KCC, xb);
+              }
+            }
+          }
+        }
+        if (c == 0) {  // the last chunk: the rest of the epilogue's inputs go with its tiles
+          if (GATE == GDN_GATE_PER_K) {
+            A = expf(sfx);
+            if (pt < D) fA[pt] = A;
+          } else {
+            write_fields();
+          }
+          if (pt == 0) scal[2] = A;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(bar_id, 128);
+        if (pt == 0 && c == 0) mbar_arrive(bars.inf(s));
+        if (pt == 0 && leader_ok) {
+          // the first chunk's contraction waits until the epilogue has read
+          // the accumulator's previous item out
+          if (c == nch - 1 && ua > 0 && !wait_bar(bars.te(acc), (ua - 1) & 1, abort_flag, P.status)) {
+            leader_ok = false;
+          } else {
+            tc_fence_after();
+            if (p > 0) {
+              const uint32_t a0 = smem_addr(tA), b0 = smem_addr(tB);
+              const uint32_t sbo = (uint32_t)lay.KC * 128;
+              const int cnt = p - j0 < lay.CH ? p - j0 : lay.CH;  // entries of this chunk
+              const int nsteps = (cnt + KSTEP - 1) / KSTEP;
+              for (int i = 0; i < nsteps; ++i)
+                tc_mma<KIND == 2 ? 1 : 0>(tmem + acc * D, make_sdesc(a0 + 256 * i, 128, sbo),
+                                          make_sdesc(b0 + 256 * i, 128, sbo), idesc,
+                                          (c != nch - 1 || i > 0) ? 1u : 0u);
+              last_acc = acc;
+              last_use = ua;
+              last_committed = false;
+              if (c == 0) {
+                tc_commit(bars.tf(acc));
+                last_committed = true;
+              }
+              tc_commit(bars.tle(tc));
+            } else {
+              mbar_arrive(bars.tf(acc));
+              mbar_arrive(bars.tle(tc));
+            }
+            // after the last chunk the landing slot has been read: fill it
+            // for the item that uses it next
+            if (c == 0 && land_next < nlive) {
+              land(land_next);
+              land_next += 2;
+            }
           }
         }
       }
+      if (stop) break;
       ++li;
     }
     // an aborted CTA lets its last contraction and its landings finish first
     if (pt == 0 && *abort_flag) {
-      if (last_acc >= 0) mbar_wait_bounded(bars.tf(last_acc), last_use & 1, kWaitLimitNs);
+      if (last_acc >= 0) {
+        if (!last_committed) tc_commit(bars.tf(last_acc));  // chunks issued for an item cut short
+        mbar_wait_bounded(bars.tf(last_acc), last_use & 1, kWaitLimitNs);
+      }
       for (int k = land_next - 2; k >= 0 && k >= land_next - NL; k -= 2)
         mbar_wait_bounded(bars.lf(k % NL), (uint32_t)(k / NL) & 1, kWaitLimitNs);
     }
@@ -1049,10 +1216,8 @@ static cudaError_t launch_tcp_ring(const DecodeParams &P, const CUtensorMap &map
   return launch_tcp_t<D, GATE, 2, GDN_F32>(P, map, lay, grid, s);
 }
 
-// Returns cudaErrorNotSupported (nothing launched) when the persistent layout
-// does not fit; the caller then uses the one-CTA-per-head kernel.
-cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUtensorMap &map,
-                              cudaStream_t s) {
+// Whether the persistent kernel takes this launch, with its layout and grid.
+static bool tcp_plan(const DecodeParams &P, int D, int gate, TcpLayout *lay, int *grid) {
   static const int sms = device_attr(cudaDevAttrMultiProcessorCount);
   static const int optin = device_attr(cudaDevAttrMaxSharedMemoryPerBlockOptin);
   const int kind = P.ring_dtype == GDN_F16 ? 0 : (P.ring_dtype == GDN_BF16 ? 1 : 2);
@@ -1061,14 +1226,29 @@ cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUte
   // q, k, v rows can be bulk-copied when every vector starts on 16 bytes
   const int qkv_bulk =
       ((reinterpret_cast<uintptr_t>(P.qkv) & 15u) == 0 && ((P.qkv_stride * qes) & 15) == 0) ? 1 : 0;
-  if (gate == GDN_GATE_PER_K && (reinterpret_cast<uintptr_t>(P.ring_g) & 15u) != 0) return cudaErrorNotSupported;
-  if (P.HV >= 32768) return cudaErrorNotSupported;  // the item table packs hv and hk into 16 bits each
-  if (P.N >= (1 << 24)) return cudaErrorNotSupported;  // the dealing packs a row's slot in 24 bits
+  if (gate == GDN_GATE_PER_K && (reinterpret_cast<uintptr_t>(P.ring_g) & 15u) != 0) return false;
+  if (P.HV >= 32768) return false;       // the item table packs hv and hk into 16 bits each
+  if (P.N >= (1 << 24)) return false;    // the dealing packs a row's slot in 24 bits
   const int T = P.B * P.HV;
-  int grid = sms > 0 && sms < T ? sms : T;
-  if ((T + grid - 1) / grid > kItemsMax) grid = (T + kItemsMax - 1) / kItemsMax;
-  const TcpLayout lay = tcp_pick_layout(D, kind, gate, P.L, ring_bytes, qes, qkv_bulk, optin);
-  if (lay.NB < 2 * (D / 32) || lay.total > (uint32_t)optin) return cudaErrorNotSupported;
+  *grid = sms > 0 && sms < T ? sms : T;
+  if ((T + *grid - 1) / *grid > kItemsMax) *grid = (T + kItemsMax - 1) / kItemsMax;
+  *lay = tcp_pick_layout(D, kind, gate, P.L, ring_bytes, qes, qkv_bulk, optin);
+  return lay->NB >= 2 * (D / 32) && lay->total <= (uint32_t)optin;
+}
+
+bool tcp_decode_fits(const DecodeParams &P, int D, int gate) {
+  TcpLayout lay;
+  int grid = 0;
+  return tcp_plan(P, D, gate, &lay, &grid);
+}
+
+// Returns cudaErrorNotSupported (nothing launched) when the persistent layout
+// does not fit; the caller then uses the one-CTA-per-head kernel.
+cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUtensorMap &map,
+                              cudaStream_t s) {
+  TcpLayout lay;
+  int grid = 0;
+  if (!tcp_plan(P, D, gate, &lay, &grid)) return cudaErrorNotSupported;
   if (D == 128)
     return gate == GDN_GATE_SCALAR ? launch_tcp_ring<128, 0>(P, map, lay, grid, s)
                                    : launch_tcp_ring<128, 1>(P, map, lay, grid, s);

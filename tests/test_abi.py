@@ -203,3 +203,17 @@ def test_scratch_peek_checks_its_arguments(lib):
     for n in (0, -1, 65):
         assert lib.gdn_noalloc_scratch_peek(ctypes.cast(buf, ctypes.c_void_p), n) == 1
     assert lib.gdn_noalloc_scratch_peek(None, 1) == 1
+
+
+def test_decode_kernel_query_checks_arguments_and_reports_cuda_core_recons(lib):
+    d = _desc()
+    cache = Bd._Cache(0x1000, 0x1000, 0x1000, 0x1000)
+    out = ctypes.c_int32(-1)
+    f = lib.gdn_replayssm_decode_kernel
+    assert f(ctypes.byref(d), ctypes.byref(cache), ctypes.byref(_step()), 0, None) == 1
+    assert f(ctypes.byref(d), ctypes.byref(cache), ctypes.byref(_step()), 7, ctypes.byref(out)) == 1
+    assert f(ctypes.byref(_desc(k_dim=96, v_dim=96)), ctypes.byref(cache), ctypes.byref(_step()), 0,
+             ctypes.byref(out)) == 2
+    for recon in (Bd.RECON_FFMA, Bd.RECON_OUTPUT):  # decided without looking at the device
+        assert f(ctypes.byref(d), ctypes.byref(cache), ctypes.byref(_step()), recon, ctypes.byref(out)) == 0
+        assert out.value == Bd.KERNEL_CUDA_CORE

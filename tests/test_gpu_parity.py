@@ -61,13 +61,46 @@ def test_head_dim_64(recon, gate, L):
 @pytest.mark.parametrize("ring", [Bd.F16, Bd.F32], ids=["f16", "f32"])
 @pytest.mark.parametrize("gate", [Bd.GATE_SCALAR, Bd.GATE_PER_K], ids=["gdn", "kda"])
 def test_longest_ring(recon, ring, gate):
-    """L = 64: replay depth beyond what a prep thread keeps in registers; with an
-    fp32 ring the persistent kernel's stages do not fit and the one-CTA-per-head
-    tensor-core kernel runs instead."""
+    """L = 64: the replay runs in up to four chunks of 16 ring entries on the
+    persistent tensor-core kernel (the first chunk landed by bulk copy, the
+    others loaded from the ring directly), each contracted into the same
+    accumulator; 70 steps from an empty ring take p through 0 .. 63.  A KDA
+    layer with an fp32 ring keeps too few checkpoint boxes beside its per-channel
+    gates, and there the one-block-per-head tensor-core kernel runs."""
     w = I.Workload("L64", N=3, B=2, HV=2, HK=1 if gate == Bd.GATE_SCALAR else 2, K=128, L=64,
                    ring_dtype=ring, qkv_dtype=Bd.BF16, gate=gate, steps=70, seed=14)
+    if recon == TC:
+        want = Bd.KERNEL_PER_HEAD_TC if (gate == Bd.GATE_PER_K and ring == Bd.F32) else Bd.KERNEL_PERSISTENT_TC
+        assert _kernel_for(w, recon) == want
     rep = run_parity(w, recon)
     assert sum(s.flushes for s in rep.steps) == 2
+
+
+def _kernel_for(w: I.Workload, recon: int) -> int:
+    """The decode kernel the library picks for the workload's shapes (device
+    buffers laid out as the parity harness lays them out)."""
+    gen = I.generator(w.seed, "cuda")
+    wp = I.write_pos(gen, w, "cuda")
+    c = I.cache(gen, w, wp, "cuda")
+    idx = I.indices(gen, w.B, w.N, w.n_pad, "cuda")
+    si = I.step_inputs(gen, w, "cuda")
+    out = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
+    return Bd.gdn_replayssm_decode_kernel(desc_of(w), Bd.Cache(c.state, c.ring_d, c.ring_k, c.ring_g),
+                                          Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out), recon)
+
+
+@pytest.mark.parametrize("ring", [Bd.F16, Bd.BF16, Bd.F32], ids=["f16", "bf16", "f32"])
+@pytest.mark.parametrize("L", [24, 34])
+def test_chunked_replay_boundaries(ring, L):
+    """Staggered cursors put replay depths on both sides of 16 and 32 in one
+    launch, on the persistent kernel: L = 24 replays up to 23 entries in one
+    contraction (16-bit rings) or in chunks of 16 (fp32 ring); L = 34 chunks
+    every ring type (p = 15, 16, 17, 31, 32, 33 all occur)."""
+    w = I.Workload(f"L{L}", N=40, B=24, n_pad=2, HV=4, HK=2, K=128, L=L, ring_dtype=ring,
+                   qkv_dtype=Bd.BF16, steps=L + 6, staggered=True, seed=15)
+    assert _kernel_for(w, TC) == Bd.KERNEL_PERSISTENT_TC
+    rep = run_parity(w, TC)
+    assert sum(s.flushes for s in rep.steps) > 0
 
 
 @pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
@@ -314,6 +347,14 @@ def test_host_side_rejects_bad_arguments():
                          ids=["qwen3next_layer", "headline_B256_L16", "kda_layer"])
 def test_full_size_sampled(w):
     """The launch configuration the benchmark times, checked on sampled rows."""
+    run_sampled(w, TC, steps=3)
+
+
+def test_full_size_sampled_long_fp32_ring():
+    """B = 256, L = 32 with an fp32 ring (tf32 operands), the launch the sweep
+    times: two replay chunks per long item, on the persistent kernel."""
+    w = I.sweep_point(256, 32, Bd.F32)
+    assert _kernel_for(w, TC) == Bd.KERNEL_PERSISTENT_TC
     run_sampled(w, TC, steps=3)
 
 
