@@ -420,7 +420,7 @@ def pick_workload(name):
     raise SystemExit(f"unknown workload {name}")
 
 
-def measure_replay(w, K, warmup, recon, dev, layers=1, overlap=False):
+def measure_replay(w, K, warmup, recon, dev, layers=1, overlap=False, extra_flags=0):
     """Kernel-only timing of K steps of `layers` layers sharing one cursor array:
     gdn_replayssm_decode on every layer but the last, gdn_replayssm_decode_advance
     on the last.  Inputs are resident on the device; nothing else runs between
@@ -446,8 +446,9 @@ def measure_replay(w, K, warmup, recon, dev, layers=1, overlap=False):
     desc = Bd.layer_desc(w.N, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, ring_dtype=w.ring_dtype)
     pool = [I.step_inputs(gen, w, dev) for _ in range(4)]
     out = torch.empty((rows, w.HV, w.V), dtype=torch.bfloat16, device=dev)
-    steps_in = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out) for b in pool]
-    steps_ov = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out, flags=Bd.STEP_OVERLAP_PREVIOUS) for b in pool]
+    steps_in = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out, flags=extra_flags) for b in pool]
+    steps_ov = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out, flags=Bd.STEP_OVERLAP_PREVIOUS | extra_flags)
+                for b in pool]
     stream = torch.cuda.current_stream()
     adv_ws = Bd.decode_advance_workspace(dev)
     idx_h = idx.cpu().numpy()
@@ -490,7 +491,10 @@ def measure_replay(w, K, warmup, recon, dev, layers=1, overlap=False):
     launch_s = step_s / layers
     peak, _ = measured_hbm_peak()
     gbs = total / K / step_s / 1e9
-    return {"workload": w.name, "layers": layers, "overlap_previous": bool(overlap and layers > 1),
+    r0 = Bd.gdn_replayssm_decode_kernel(desc, caches[0], steps_in[0], recon)
+    kname = {Bd.KERNEL_PERSISTENT_TC: "persistent_tc", Bd.KERNEL_PER_HEAD_TC: "per_head_tc",
+             Bd.KERNEL_CUDA_CORE: "cuda_core", Bd.KERNEL_SMALL_BATCH: "small_batch"}[r0]
+    return {"workload": w.name, "kernel": kname, "layers": layers, "overlap_previous": bool(overlap and layers > 1),
             "B": w.B, "L": w.L,
             "ring": {0: "f32", 1: "bf16", 2: "f16"}[w.ring_dtype], "steps": K,
             "ms_per_step": step_s * 1e3, "ms_per_launch": launch_s * 1e3,
@@ -590,7 +594,8 @@ def run_sweep(args):
                 w = I.sweep_point(B, L, ring)
                 K = max(2 * L * 8, 128) // args.sweep_layers + 1
                 r = measure_replay(w, K, max(args.warmup, 2 * L), Bd.RECON_TENSOR, dev, layers=args.sweep_layers,
-                                   overlap=args.sweep_layers > 1 and not args.no_overlap)
+                                   overlap=args.sweep_layers > 1 and not args.no_overlap,
+                                   extra_flags=Bd.STEP_PERSISTENT_KERNEL if args.persistent_kernel else 0)
                 if B not in packed:
                     packed[B] = measure_packed(w, 64, dev)
                 r["packed"] = packed[B]
@@ -806,7 +811,7 @@ def measure_lossless(B, T, K, warmup, dev, rate=0.7):
             "packed_decode_ms_per_step": pk_s * 1e3}
 
 
-def measure_graph(B, n, warmup, dev):
+def measure_graph(B, n, warmup, dev, extra_flags=0):
     """One GDN layer's decode + advance at batch B (L=16, fp16 ring): n steps
     launched one by one, against the same n steps captured once in a CUDA graph
     and replayed (the library allocates nothing and never synchronises, so its
@@ -824,7 +829,8 @@ def measure_graph(B, n, warmup, dev):
     idx = I.indices(gen, w.B, w.N, w.n_pad, dev)
     desc = Bd.layer_desc(w.N, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, ring_dtype=w.ring_dtype)
     out = torch.empty((idx.shape[0], w.HV, w.V), dtype=torch.bfloat16, device=dev)
-    steps_in = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out) for b in (I.step_inputs(gen, w, dev) for _ in range(4))]
+    steps_in = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out, flags=extra_flags)
+                for b in (I.step_inputs(gen, w, dev) for _ in range(4))]
     ws = Bd.decode_advance_workspace(dev)
 
     def seq(stream):
@@ -853,9 +859,31 @@ def measure_graph(B, n, warmup, dev):
     graph.replay()
     torch.cuda.synchronize()
     graph_us = timed(graph.replay, cur)
-    return {"workload": w.name, "B": B, "steps_per_graph": n, "eager_us_per_step": eager_us,
+    kernel = Bd.gdn_replayssm_decode_kernel(desc, cache, steps_in[0], Bd.RECON_TENSOR)
+
+    # the packed decode on the same batch, one by one and as a graph (its own state pool)
+    pstate = I.state(gen, w.N, w.HV, w.V, w.K, dev)
+
+    def pseq(stream):
+        for i in range(n):
+            Bd.gdn_packed_decode(desc, pstate, steps_in[i % 4], None, stream)
+
+    for _ in range(max(1, warmup // n + 1)):
+        pseq(cur)
+    p_eager_us = timed(lambda: pseq(cur), cur)
+    pgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(pgraph, stream=cs):
+            pseq(cs)
+    pgraph.replay()
+    torch.cuda.synchronize()
+    p_graph_us = timed(pgraph.replay, cur)
+    return {"workload": w.name, "B": B, "kernel": {0: "persistent_tc", 1: "per_head_tc", 3: "small_batch"}.get(kernel),
+            "steps_per_graph": n, "eager_us_per_step": eager_us,
             "graph_us_per_step": graph_us, "graph_head_steps_per_s": B * w.HV / (graph_us * 1e-6),
-            "graph_vs_eager": eager_us / graph_us}
+            "graph_vs_eager": eager_us / graph_us,
+            "packed_eager_us_per_step": p_eager_us, "packed_graph_us_per_step": p_graph_us,
+            "eager_vs_packed": p_eager_us / eager_us, "graph_vs_packed_graph": p_graph_us / graph_us}
 
 
 def run_graph(args):
@@ -872,7 +900,8 @@ def run_graph(args):
     Bd.load_library()
     dev = torch.device("cuda", torch.cuda.current_device())
     for B in [int(x) for x in args.graph_batches.split(",")]:
-        print(json.dumps(measure_graph(B, 64, args.warmup, dev)), flush=True)
+        print(json.dumps(measure_graph(B, 64, args.warmup, dev,
+                                       Bd.STEP_PERSISTENT_KERNEL if args.persistent_kernel else 0)), flush=True)
         torch.cuda.empty_cache()
     return 0
 
@@ -1127,6 +1156,8 @@ def main():
     ap.add_argument("--sweep-rings", default="f16,f32")
     ap.add_argument("--sweep-layers", type=int, default=1,
                     help="layer buffers rotated per step (>= 4 keeps a layer's working set out of L2)")
+    ap.add_argument("--persistent-kernel", action="store_true",
+                    help="sweep: run every point on the persistent tensor-core kernel (no small-batch kernel)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="multi-layer modes: launch every layer without STEP_OVERLAP_PREVIOUS")
     ap.add_argument("--spec", action="store_true",

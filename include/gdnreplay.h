@@ -150,7 +150,13 @@ typedef struct {
  *   gdn_packed_decode ignore the flag.  No counterpart in the pages: a
  *   property of this library's launches. */
 #define GDN_STEP_OVERLAP_PREVIOUS 1u
-#define GDN_STEP_KNOWN_FLAGS      1u
+/* GDN_STEP_PERSISTENT_KERNEL: with GDN_RECON_TENSOR, always run the
+ *   persistent tensor-core kernel.  By default a batch of at most 64
+ *   (row, value head) items runs the small-batch kernel instead (see
+ *   gdn_replayssm_decode_kernel); this flag keeps the tensor-core arithmetic at
+ *   any batch size.  Ignored by the other recon modes. */
+#define GDN_STEP_PERSISTENT_KERNEL 2u
+#define GDN_STEP_KNOWN_FLAGS      3u
 
 /* Packed decode, the read + write baseline ([P1] Motivation; [P2] section 1):
  * per row b with slot s = ssm_state_indices[b] >= 0 and every value head,
@@ -192,11 +198,19 @@ GDN_API gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gd
  *                             (TENSOR recon whose layout does not fit the
  *                             persistent kernel)
  *   GDN_KERNEL_CUDA_CORE      CUDA-core kernel (FFMA or OUTPUT recon)
+ *   GDN_KERNEL_SMALL_BATCH    TENSOR recon of a batch with at most 64
+ *                             (row, value head) items (unless the step has
+ *                             GDN_STEP_PERSISTENT_KERNEL): one block per (row,
+ *                             value head, 16 state rows), every block on its
+ *                             rows' whole step, replay sum in fp32 on the CUDA
+ *                             cores (so within the FFMA bound), so that a
+ *                             small batch still spreads over every SM
  * Argument checks and errors as in gdn_replayssm_decode.  No counterpart in
  * the pages: a diagnostic of this library's dispatch. */
 #define GDN_KERNEL_PERSISTENT_TC 0
 #define GDN_KERNEL_PER_HEAD_TC   1
 #define GDN_KERNEL_CUDA_CORE     2
+#define GDN_KERNEL_SMALL_BATCH   3
 GDN_API gdn_status_t gdn_replayssm_decode_kernel(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
                                                  const gdn_step_t *step, int32_t recon, int32_t *kernel);
 

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdnrepla
 
 from .constants import (BF16, DEV_BAD_ACCEPTED, DEV_BAD_SLOT, DEV_BAD_WRITE_POS, DEV_INTERNAL, DEV_TIMEOUT,  # noqa: F401
                         F16, F32, GATE_PER_K, GATE_SCALAR, GDN_DTYPE, RECON_FFMA, RECON_OUTPUT, RECON_TENSOR,
-                        STEP_OVERLAP_PREVIOUS, TORCH_DTYPE)
+                        STEP_OVERLAP_PREVIOUS, STEP_PERSISTENT_KERNEL, TORCH_DTYPE)
 
 
 class GdnError(RuntimeError):
@@ -84,7 +84,7 @@ class Step:
     out: torch.Tensor                # [B, HV, V]
     q_scale: float = 1.0
     qk_l2norm: bool = False
-    flags: int = 0                   # STEP_* bits (STEP_OVERLAP_PREVIOUS)
+    flags: int = 0                   # STEP_* bits (STEP_OVERLAP_PREVIOUS, STEP_PERSISTENT_KERNEL)
 
 
 _lib = None
@@ -218,7 +218,7 @@ def gdn_replayssm_decode(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor,
 
 
 # gdn_replayssm_decode_kernel results
-KERNEL_PERSISTENT_TC, KERNEL_PER_HEAD_TC, KERNEL_CUDA_CORE = 0, 1, 2
+KERNEL_PERSISTENT_TC, KERNEL_PER_HEAD_TC, KERNEL_CUDA_CORE, KERNEL_SMALL_BATCH = 0, 1, 2, 3
 
 
 def gdn_replayssm_decode_kernel(desc: LayerDesc, cache: Cache, step: Step, recon: int = RECON_TENSOR) -> int:

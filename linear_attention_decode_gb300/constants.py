@@ -8,7 +8,7 @@ GATE_SCALAR, GATE_PER_K = 0, 1
 # gdn_recon_t
 RECON_TENSOR, RECON_FFMA, RECON_OUTPUT = 0, 1, 2
 # gdn_step_t.flags bits
-STEP_OVERLAP_PREVIOUS = 1
+STEP_OVERLAP_PREVIOUS, STEP_PERSISTENT_KERNEL = 1, 2
 # dev_status bits
 DEV_BAD_SLOT, DEV_BAD_WRITE_POS, DEV_TIMEOUT, DEV_INTERNAL, DEV_BAD_ACCEPTED = 1, 2, 4, 8, 16
 

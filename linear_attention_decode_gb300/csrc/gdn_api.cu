@@ -85,6 +85,7 @@ void fill_step(gdn::DecodeParams &P, const gdn_step_t *s) {
   P.out = s->out;
   P.out_dtype = s->out_dtype;
   P.overlap = (s->flags & GDN_STEP_OVERLAP_PREVIOUS) ? 1 : 0;
+  P.persistent_only = (s->flags & GDN_STEP_PERSISTENT_KERNEL) ? 1 : 0;
 }
 
 gdn_status_t check_cache(const gdn_layer_desc_t *d, const gdn_layer_cache_t *c) {
@@ -191,7 +192,10 @@ gdn_status_t gdn_replayssm_decode_kernel(const gdn_layer_desc_t *desc, const gdn
   P.ring_d = cache->ring_d;
   P.ring_k = cache->ring_k;
   P.ring_g = cache->ring_g;
-  *kernel = gdn::tcp_decode_fits(P, desc->k_dim, desc->gate) ? GDN_KERNEL_PERSISTENT_TC : GDN_KERNEL_PER_HEAD_TC;
+  if (gdn::slab_decode_takes(P, desc->gate))
+    *kernel = GDN_KERNEL_SMALL_BATCH;
+  else
+    *kernel = gdn::tcp_decode_fits(P, desc->k_dim, desc->gate) ? GDN_KERNEL_PERSISTENT_TC : GDN_KERNEL_PER_HEAD_TC;
   return GDN_OK;
 }
 

@@ -50,6 +50,9 @@ struct DecodeParams {
   // before this one leaves the cache, cursors, rows and force_flush alone, so
   // they may be read before waiting for it
   int overlap;
+  // GDN_STEP_PERSISTENT_KERNEL: tensor-core recon always takes the persistent
+  // kernel, never the small-batch one
+  int persistent_only;
 };
 
 __device__ __forceinline__ float load_as_f32(const void *p, int64_t i, int dtype) {
@@ -245,6 +248,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 
 __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// atomicAdd with release semantics at GPU scope: this thread's earlier memory
+// accesses are performed before the addition is (the result is not waited on
+// until it is used).
+__device__ __forceinline__ uint32_t atomic_add_release_gpu(uint32_t *addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
 }
 
 // Programmatic dependent launch: wait until the grid this one depends on has

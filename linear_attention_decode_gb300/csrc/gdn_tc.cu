@@ -340,6 +340,11 @@ cudaError_t make_state_tmap(const DecodeParams &P, int D, CUtensorMap *map, cons
 cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why,
                              bool *fused) {
   *fused = false;
+  if (slab_decode_takes(P, gate)) {  // few items: the small-batch kernel spreads them over the GPU
+    const cudaError_t e = launch_slab_decode(P, D, gate, s);
+    *fused = e == cudaSuccess && P.sync != nullptr;
+    return e;
+  }
   CUtensorMap map;
   const cudaError_t em = make_state_tmap(P, D, &map, why);
   if (em != cudaSuccess) return em;

@@ -3,7 +3,7 @@ binding) and the CPU oracle on the same seeded inputs, step by step, and
 compares everything a step produces."""
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 from typing import Callable, Optional
 
 import numpy as np
@@ -22,7 +22,26 @@ TOL_FFMA_F32 = 1e-5
 TOL_TC = 2e-3
 
 
+# The tensor-core recon runs two ways in the parity tests: as a caller gets it
+# (a batch with few (row, head) items takes the small-batch kernel) and, as
+# TCP, forced onto the persistent tensor-core kernel (STEP_PERSISTENT_KERNEL).
+TCP = 1000
+
+
+def recon_and_flags(recon: int):
+    """The C recon value and the extra step flags of a test's recon id."""
+    return (Bd.RECON_TENSOR, Bd.STEP_PERSISTENT_KERNEL) if recon == TCP else (recon, 0)
+
+
+def decode(desc, cache, write_pos, force_flush, step, recon=Bd.RECON_TENSOR, *args, **kw):
+    """gdn_replayssm_decode with a test recon id (TCP included)."""
+    r, f = recon_and_flags(recon)
+    return Bd.gdn_replayssm_decode(desc, cache, write_pos, force_flush, replace(step, flags=step.flags | f), r,
+                                   *args, **kw)
+
+
 def tolerance(w: I.Workload, recon: int) -> float:
+    recon, _ = recon_and_flags(recon)
     if recon in (Bd.RECON_FFMA, Bd.RECON_OUTPUT) and w.ring_dtype == Bd.F32:
         return TOL_FFMA_F32
     if w.ring_dtype == Bd.BF16:
@@ -181,7 +200,7 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
             step = Bd.Step(guarded(si.mixed_qkv, step_guards), guarded(si.g, step_guards),
                            guarded(si.beta, step_guards), idx_dev, out, q_scale=q_scale, qk_l2norm=qk_l2norm,
                            flags=flags)
-            Bd.gdn_replayssm_decode(desc, layer.dev, wp_dev, ff_dev, step, recon, flushed, status)
+            decode(desc, layer.dev, wp_dev, ff_dev, step, recon, flushed, status)
             o_ref, fl_ref, st_ref = O.replay_decode(G, layer.ora, wp_ora, idx.numpy(), ff,
                                                     si.mixed_qkv, si.g, si.beta, q_scale, int(qk_l2norm))
             torch.cuda.synchronize()
@@ -291,7 +310,7 @@ def run_sampled(w: I.Workload, recon: int, steps: int = 2, samples: int = 6) -> 
         mini = O.Cache.from_arrays(dev.state[sl], dev.ring_d[sl], dev.ring_k[sl], dev.ring_g[sl])
         out = torch.full((rows, w.HV, w.V), float("nan"), dtype=torch.float32, device="cuda")
         step = Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out)
-        Bd.gdn_replayssm_decode(desc, dev, wp, None, step, recon, flushed, status)
+        decode(desc, dev, wp, None, step, recon, flushed, status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         Gm = O.geom(len(slots), w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, state_dtype=O.F32,

@@ -81,7 +81,7 @@ def test_decode_rejects_bad_pointers_and_sizes(lib):
         (good, _step(batch=-1), 0x1000, 0),                                 # negative batch
         (good, _step(), None, 0),                                           # no write_pos
         (good, _step(), 0x1000, 5),                                         # unknown recon
-        (good, _step(flags=2), 0x1000, 0),                                  # unknown step flag
+        (good, _step(flags=4), 0x1000, 0),                                  # unknown step flag
     ]
     for cache, step, wp, recon in calls:
         st = lib.gdn_replayssm_decode(ctypes.byref(d), ctypes.byref(cache), wp, None, ctypes.byref(step),
@@ -194,8 +194,14 @@ def test_step_flag_constants_match_the_header():
     text = open(os.path.join(ROOT, "include", "gdnreplay.h")).read()
     m = re.search(r"#define GDN_STEP_OVERLAP_PREVIOUS\s+(\d+)u", text)
     assert m and int(m.group(1)) == Bd.STEP_OVERLAP_PREVIOUS
+    m = re.search(r"#define GDN_STEP_PERSISTENT_KERNEL\s+(\d+)u", text)
+    assert m and int(m.group(1)) == Bd.STEP_PERSISTENT_KERNEL
     m = re.search(r"#define GDN_STEP_KNOWN_FLAGS\s+(\d+)u", text)
-    assert m and int(m.group(1)) == Bd.STEP_OVERLAP_PREVIOUS
+    assert m and int(m.group(1)) == Bd.STEP_OVERLAP_PREVIOUS | Bd.STEP_PERSISTENT_KERNEL
+    for name, val in (("PERSISTENT_TC", Bd.KERNEL_PERSISTENT_TC), ("PER_HEAD_TC", Bd.KERNEL_PER_HEAD_TC),
+                      ("CUDA_CORE", Bd.KERNEL_CUDA_CORE), ("SMALL_BATCH", Bd.KERNEL_SMALL_BATCH)):
+        m = re.search(r"#define GDN_KERNEL_%s\s+(\d+)" % name, text)
+        assert m and int(m.group(1)) == val
 
 
 def test_scratch_peek_checks_its_arguments(lib):

@@ -51,9 +51,14 @@ def _same_bits(a: torch.Tensor, b: torch.Tensor) -> bool:
     return torch.equal(a, b)
 
 
+@pytest.mark.parametrize("persistent", [False, True], ids=["default", "persistent"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_decode_advance_matches_decode_then_advance(gdnlib, name):
+def test_decode_advance_matches_decode_then_advance(gdnlib, name, persistent):
+    """Small batches run the small-batch kernel by default; `persistent` forces
+    the tensor-core recon onto the persistent kernel (STEP_PERSISTENT_KERNEL),
+    whose fused advance counts its blocks differently."""
     w, recon, forced = CASES[name]
+    flags = Bd.STEP_PERSISTENT_KERNEL if persistent else 0
     gen = I.generator(w.seed, "cuda")
     wp0 = I.write_pos(gen, w, "cuda")
     c0 = I.cache(gen, w, wp0, "cuda")
@@ -73,10 +78,11 @@ def test_decode_advance_matches_decode_then_advance(gdnlib, name):
         ff = (torch.rand(rows, generator=gen, device="cuda") < 0.3).to(torch.uint8) if forced else None
         out_two = torch.full((rows, w.HV, w.V), float("nan"), device="cuda")
         out_one = torch.full((rows, w.HV, w.V), float("nan"), device="cuda")
-        Bd.gdn_replayssm_decode(desc, two, wp_two, ff, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out_two),
-                                recon, fl_two, st_two)
+        Bd.gdn_replayssm_decode(desc, two, wp_two, ff,
+                                Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out_two, flags=flags), recon, fl_two, st_two)
         Bd.gdn_replayssm_advance(idx, ff, w.N, w.L, wp_two, st_two)
-        Bd.gdn_replayssm_decode_advance(desc, one, wp_one, ff, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out_one),
+        Bd.gdn_replayssm_decode_advance(desc, one, wp_one, ff,
+                                        Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out_one, flags=flags),
                                         ws, recon, fl_one, st_one)
         torch.cuda.synchronize()
         assert _same_bits(out_one, out_two), f"step {t}: outputs differ"
@@ -124,6 +130,9 @@ def test_decode_advance_stack_shares_one_cursor_array(gdnlib):
 
 
 OVERLAP_CASES = {
+    # few items: the small-batch kernel (one block per 16 state rows)
+    "small_batch": I.Workload("overlap small", N=24, B=6, n_pad=2, HV=8, HK=4, K=128, L=8, ring_dtype=Bd.F16,
+                              qkv_dtype=Bd.BF16, steps=10, staggered=True, seed=43),
     # more items than SMs, so consecutive launches really share the GPU
     "persistent": I.Workload("overlap", N=96, B=48, n_pad=3, HV=8, HK=4, K=128, L=8, ring_dtype=Bd.F16,
                              qkv_dtype=Bd.BF16, steps=10, staggered=True, seed=41),

@@ -9,7 +9,8 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_harness import (TOL_TC, Layer, desc_of, oracle_geom, rel_err, run_parity, run_sampled)
+from gpu_harness import (TCP, TOL_TC, Layer, decode, desc_of, oracle_geom, recon_and_flags, rel_err, run_parity,
+                         run_sampled)
 from linear_attention_decode_gb300 import binding as Bd
 from linear_attention_decode_gb300 import inputs as I
 
@@ -30,25 +31,25 @@ def _lib(gdnlib):
     yield
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 def test_tiny_fp32(recon):
     rep = run_parity(I.TINY, recon)
     assert sum(s.flushes for s in rep.steps) == 8 * I.TINY.B  # 32 steps, L = 4
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 @pytest.mark.parametrize("ring", [Bd.F16, Bd.BF16, Bd.F32], ids=["f16", "bf16", "f32"])
 def test_ragged_staggered(recon, ring):
     rep = run_parity(I.with_(RAGGED, ring_dtype=ring), recon)
     assert sum(s.flushes for s in rep.steps) > 0 and sum(s.appends for s in rep.steps) > 0
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 def test_kda(recon):
     run_parity(KDA_SMALL, recon)
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 @pytest.mark.parametrize("gate,L", [(Bd.GATE_SCALAR, 8), (Bd.GATE_PER_K, 8), (Bd.GATE_PER_K, 24)],
                          ids=["gdn_L8", "kda_L8", "kda_L24"])
 def test_head_dim_64(recon, gate, L):
@@ -57,7 +58,7 @@ def test_head_dim_64(recon, gate, L):
     run_parity(w, recon)
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 @pytest.mark.parametrize("ring", [Bd.F16, Bd.F32], ids=["f16", "f32"])
 @pytest.mark.parametrize("gate", [Bd.GATE_SCALAR, Bd.GATE_PER_K], ids=["gdn", "kda"])
 def test_longest_ring(recon, ring, gate):
@@ -69,9 +70,11 @@ def test_longest_ring(recon, ring, gate):
     gates, and there the one-block-per-head tensor-core kernel runs."""
     w = I.Workload("L64", N=3, B=2, HV=2, HK=1 if gate == Bd.GATE_SCALAR else 2, K=128, L=64,
                    ring_dtype=ring, qkv_dtype=Bd.BF16, gate=gate, steps=70, seed=14)
-    if recon == TC:
+    if recon == TCP:
         want = Bd.KERNEL_PER_HEAD_TC if (gate == Bd.GATE_PER_K and ring == Bd.F32) else Bd.KERNEL_PERSISTENT_TC
         assert _kernel_for(w, recon) == want
+    elif recon == TC:
+        assert _kernel_for(w, recon) == Bd.KERNEL_SMALL_BATCH
     rep = run_parity(w, recon)
     assert sum(s.flushes for s in rep.steps) == 2
 
@@ -85,8 +88,9 @@ def _kernel_for(w: I.Workload, recon: int) -> int:
     idx = I.indices(gen, w.B, w.N, w.n_pad, "cuda")
     si = I.step_inputs(gen, w, "cuda")
     out = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
+    r, f = recon_and_flags(recon)
     return Bd.gdn_replayssm_decode_kernel(desc_of(w), Bd.Cache(c.state, c.ring_d, c.ring_k, c.ring_g),
-                                          Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out), recon)
+                                          Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out, flags=f), r)
 
 
 @pytest.mark.parametrize("ring", [Bd.F16, Bd.BF16, Bd.F32], ids=["f16", "bf16", "f32"])
@@ -98,29 +102,30 @@ def test_chunked_replay_boundaries(ring, L):
     every ring type (p = 15, 16, 17, 31, 32, 33 all occur)."""
     w = I.Workload(f"L{L}", N=40, B=24, n_pad=2, HV=4, HK=2, K=128, L=L, ring_dtype=ring,
                    qkv_dtype=Bd.BF16, steps=L + 6, staggered=True, seed=15)
-    assert _kernel_for(w, TC) == Bd.KERNEL_PERSISTENT_TC
-    rep = run_parity(w, TC)
+    assert _kernel_for(w, TCP) == Bd.KERNEL_PERSISTENT_TC
+    rep = run_parity(w, TCP)
     assert sum(s.flushes for s in rep.steps) > 0
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 def test_forced_flush_mid_ring(recon):
     sched = lambda t, rows: (np.arange(rows) % 3 == t % 3).astype(np.uint8) if t % 5 == 2 else np.zeros(rows, np.uint8)
     rep = run_parity(I.with_(RAGGED, steps=20), recon, force=sched)
     assert sum(s.flushes for s in rep.steps) > 0
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 def test_three_layer_stack_shared_cursor(recon):
     run_parity(I.with_(RAGGED, steps=18), recon, layers=3)
 
 
-def test_two_layers_second_overlaps_previous():
+@pytest.mark.parametrize("recon", [TC, TCP], ids=["small_batch", "persistent"])
+def test_two_layers_second_overlaps_previous(recon):
     """Two layers per forward sharing one cursor array, the second launched
     with STEP_OVERLAP_PREVIOUS (its rows, cursors and checkpoints may be read
     before the first layer's launch has finished): parity with the oracle,
     flush flags and status included."""
-    rep = run_parity(I.with_(RAGGED, steps=18), TC, layers=2, overlap=True)
+    rep = run_parity(I.with_(RAGGED, steps=18), recon, layers=2, overlap=True)
     assert sum(s.flushes for s in rep.steps) > 0
 
 
@@ -129,12 +134,12 @@ def test_bf16_output():
     run_parity(I.with_(RAGGED, steps=10), TC, out_dtype=torch.bfloat16, tol=TOL_TC + 2.0 ** -8)
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 def test_in_kernel_l2norm_and_scale(recon):
     run_parity(I.with_(RAGGED, steps=6), recon, q_scale=0.37, qk_l2norm=True)
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 def test_beta0_g0_leaves_checkpoint_bit_identical(recon):
     """beta = 0 and g = 0 at every step: d = 0 and alpha = 1, so after a full
     ring cycle the flushed checkpoint equals S0 bit for bit."""
@@ -159,13 +164,13 @@ def test_beta0_g0_leaves_checkpoint_bit_identical(recon):
         si = I.step_inputs(gen, w, "cpu")
         zero_gates(t, si)
         out = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
-        Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wpd, None,
+        decode(desc_of(w), layer.dev, wpd, None,
                                 Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx, out), recon)
         Bd.gdn_replayssm_advance(idx, None, w.N, w.L, wpd)
     assert torch.equal(layer.dev.state.cpu().view(torch.int32), S0.view(torch.int32))
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 def test_erased_history_closed_form(recon):
     """g = -1e4 makes alpha underflow to 0: out = beta v (k^T q) whatever the history."""
     w = I.with_(RAGGED, steps=1)
@@ -176,7 +181,7 @@ def test_erased_history_closed_form(recon):
     si = I.step_inputs(gen, w, "cpu")
     si.g.fill_(-1e4)
     out = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
-    Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wp.cuda(), None,
+    decode(desc_of(w), layer.dev, wp.cuda(), None,
                             Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx.cuda(), out), recon)
     x = si.mixed_qkv.double()
     R = x.shape[0]
@@ -205,7 +210,7 @@ def test_l1_replay_is_packed_decode_bitwise():
         si = I.step_inputs(gen, w, "cuda")
         oa = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
         ob = torch.empty_like(oa)
-        Bd.gdn_replayssm_decode(d, Bd.Cache(sa), wp, None, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, oa), FF, flushed)
+        decode(d, Bd.Cache(sa), wp, None, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, oa), FF, flushed)
         Bd.gdn_packed_decode(d, sb, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, ob))
         Bd.gdn_replayssm_advance(idx, None, w.N, 1, wp)
         assert torch.equal(oa, ob) and torch.equal(sa, sb)
@@ -213,7 +218,8 @@ def test_l1_replay_is_packed_decode_bitwise():
     assert torch.all(wp == 0)
 
 
-def test_l1_tensor_path_matches_packed():
+@pytest.mark.parametrize("recon", [TC, TCP], ids=["small_batch", "persistent"])
+def test_l1_tensor_path_matches_packed(recon):
     w = I.Workload("L1", N=6, B=4, HV=8, HK=4, K=128, L=1, ring_dtype=Bd.F16, qkv_dtype=Bd.BF16,
                    steps=4, seed=16)
     gen = I.generator(w.seed, "cpu")
@@ -226,7 +232,7 @@ def test_l1_tensor_path_matches_packed():
         si = I.step_inputs(gen, w, "cuda")
         oa = torch.empty((w.B, w.HV, w.V), device="cuda")
         ob = torch.empty_like(oa)
-        Bd.gdn_replayssm_decode(d, Bd.Cache(sa), wp, None, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, oa), TC)
+        decode(d, Bd.Cache(sa), wp, None, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, oa), recon)
         Bd.gdn_packed_decode(d, sb, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, ob))
         assert rel_err(oa.cpu().numpy(), ob.cpu().numpy()) <= 1e-5
         assert rel_err(sa.cpu().numpy(), sb.cpu().numpy()) <= 1e-5
@@ -254,7 +260,7 @@ def test_packed_decode_vs_oracle(gate):
         assert rel_err(dev.cpu().numpy(), ora) <= 1e-5
 
 
-@pytest.mark.parametrize("recon", [FF, TC, OUT], ids=["ffma", "tensor", "output"])
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 def test_bad_rows_set_status_and_touch_nothing(recon):
     w = I.with_(RAGGED, steps=1)
     gen = I.generator(w.seed, "cpu")
@@ -267,7 +273,7 @@ def test_bad_rows_set_status_and_touch_nothing(recon):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     flushed = torch.full((4,), 7, dtype=torch.uint8, device="cuda")
     before = layer.dev.state.clone()
-    Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wp.cuda(), None,
+    decode(desc_of(w), layer.dev, wp.cuda(), None,
                             Bd.Step(si.mixed_qkv.cuda(), si.g.cuda(), si.beta.cuda(), idx.cuda(), out),
                             recon, flushed, status)
     torch.cuda.synchronize()
@@ -294,8 +300,8 @@ def test_empty_and_all_padding_batches():
         idx = torch.full((rows,), -1, dtype=torch.int32, device="cuda")
         si = I.step_inputs(gen, w, "cuda", rows=rows)
         out = torch.full((rows, w.HV, w.V), float("nan"), device="cuda")
-        for recon in (FF, TC, OUT):
-            Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wp.cuda(), None,
+        for recon in (FF, TC, TCP, OUT):
+            decode(desc_of(w), layer.dev, wp.cuda(), None,
                                     Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out), recon)
         Bd.gdn_packed_decode(desc_of(w), layer.dev.state, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out))
         torch.cuda.synchronize()
@@ -338,9 +344,9 @@ def test_host_side_rejects_bad_arguments():
            Bd.layer_desc(w.N, w.HV, w.HK, 128, 128, 65)]
     for d in bad:
         with pytest.raises(Bd.GdnError):
-            Bd.gdn_replayssm_decode(d, layer.dev, wp.cuda(), None, step, TC)
+            decode(d, layer.dev, wp.cuda(), None, step, TC)
     with pytest.raises(Bd.GdnError):
-        Bd.gdn_replayssm_decode(desc_of(w), layer.dev, wp.cuda(), None, step, 7)
+        decode(desc_of(w), layer.dev, wp.cuda(), None, step, 7)
 
 
 @pytest.mark.parametrize("w", [I.QWEN3NEXT_LAYER, I.HEADLINE, I.KDA_LAYER],
@@ -356,6 +362,18 @@ def test_full_size_sampled_long_fp32_ring():
     w = I.sweep_point(256, 32, Bd.F32)
     assert _kernel_for(w, TC) == Bd.KERNEL_PERSISTENT_TC
     run_sampled(w, TC, steps=3)
+
+
+@pytest.mark.parametrize("B,ring,kernel", [(1, Bd.F16, Bd.KERNEL_SMALL_BATCH), (2, Bd.F32, Bd.KERNEL_SMALL_BATCH),
+                                           (8, Bd.F16, Bd.KERNEL_PERSISTENT_TC)],
+                         ids=["B1_f16", "B2_f32", "B8_f16"])
+def test_full_size_sampled_small_batches(B, ring, kernel):
+    """The pages' head shapes (HV=32, HK=16, K=V=128, L=16) at batch 1, 2 and
+    8, staggered cursors: B <= 2 runs the small-batch kernel, B = 8 the
+    persistent one; sampled rows against the oracle."""
+    w = I.sweep_point(B, 16, ring)
+    assert _kernel_for(w, TC) == kernel
+    run_sampled(w, TC, steps=4)
 
 
 def test_full_size_sampled_output_only():
@@ -378,7 +396,7 @@ def test_drift_after_four_rings(ring):
 
     w = I.with_(RAGGED, staggered=False, steps=64, n_pad=0, ring_dtype=ring)
     outs: list = []
-    rep = run_parity(w, TC, outputs=outs)
+    rep = run_parity(w, TCP, outputs=outs)  # the tensor-core arithmetic
     # the same seeded draws as run_parity: cursors, cache, rows, then each step's inputs
     gen = I.generator(w.seed, "cpu")
     wp = I.write_pos(gen, w, "cpu")
