@@ -153,7 +153,9 @@ __device__ __forceinline__ float dot4(const float4 &a, const float4 &b, float ac
   return acc;
 }
 
-// Sum of x and of y over the 128 threads of the CTA, returned to every thread.
+// Sum of x and of y over the first 128 threads of the CTA, returned to every
+// thread (a CTA of more threads passes zeros from the others, which add nothing
+// and are not read).
 __device__ __forceinline__ float2 block_sum2(float x, float y, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -161,7 +163,7 @@ __device__ __forceinline__ float2 block_sum2(float x, float y, float *red) {
     x += __shfl_xor_sync(0xffffffffu, x, o);
     y += __shfl_xor_sync(0xffffffffu, y, o);
   }
-  if (lane == 0) {
+  if (lane == 0 && warp < 4) {
     red[warp] = x;
     red[4 + warp] = y;
   }

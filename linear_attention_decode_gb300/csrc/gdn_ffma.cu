@@ -96,9 +96,22 @@ __device__ float stage_replay(const DecodeParams &P, int slot, int hv, int p, fl
 // the lossless verify and commit so that they agree bit for bit: every rounding
 // is pinned (mul.rn / sub.rn / fma.rn; nothing the compiler may contract).
 //
-// token_out: once the row's 8 lanes hold partial sums of S x (x = q, k; KDA
-// a o q, a o k), sums them (xor 1, 2, 4) and forms
+// token_out: once the row's 8 lanes hold partial sums s_0..s_7 of S x (x = q,
+// k; KDA a o q, a o k), sums them (xor 1, 2, 4), which leaves every lane with
+// ((s_0 + s_1) + (s_2 + s_3)) + ((s_4 + s_5) + (s_6 + s_7)) (each add is
+// commutative, so the lanes agree bit for bit), and calls token_finish:
 //   GDN: sq, sk <- alpha sq, alpha sk;   d = beta (v_r - sk);   o = sq + d (k^T q).
+template <int GATE>
+__device__ __forceinline__ float token_finish(float sq, float sk, float alpha, float beta, float vr, float kq,
+                                              float &d) {
+  if (GATE == GDN_GATE_SCALAR) {
+    sq = __fmul_rn(sq, alpha);
+    sk = __fmul_rn(sk, alpha);
+  }
+  d = __fmul_rn(beta, __fsub_rn(vr, sk));
+  return __fmaf_rn(d, kq, sq);
+}
+
 template <int GATE>
 __device__ __forceinline__ float token_out(float sq, float sk, float alpha, float beta, float vr, float kq,
                                            float &d) {
@@ -107,12 +120,7 @@ __device__ __forceinline__ float token_out(float sq, float sk, float alpha, floa
     sq += __shfl_xor_sync(0xffffffffu, sq, o);
     sk += __shfl_xor_sync(0xffffffffu, sk, o);
   }
-  if (GATE == GDN_GATE_SCALAR) {
-    sq = __fmul_rn(sq, alpha);
-    sk = __fmul_rn(sk, alpha);
-  }
-  d = __fmul_rn(beta, __fsub_rn(vr, sk));
-  return __fmaf_rn(d, kq, sq);
+  return token_finish<GATE>(sq, sk, alpha, beta, vr, kq, d);
 }
 
 // token_update: four columns of the row after the token,
@@ -685,6 +693,316 @@ __global__ void __launch_bounds__(kThreads) lossless_verify_kernel(const DecodeP
   }
 }
 
+// Block sums of NV values at once over the first 128 threads, each summed as
+// block_sum2 sums one (a 32-lane xor tree per warp, then the four warps'
+// partials as (w0 + w1) + (w2 + w3)), so each result is bit-identical to a
+// block_sum2 of that value; two barriers for all NV instead of two each.
+// red: NV * 4 floats.
+template <int NV>
+__device__ __forceinline__ void block_sums(float (&x)[NV], float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < NV; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], o);
+  if (lane == 0 && warp < 4)
+#pragma unroll
+    for (int i = 0; i < NV; ++i) red[4 * i + warp] = x[i];
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < NV; ++i) x[i] = (red[4 * i] + red[4 * i + 1]) + (red[4 * i + 2] + red[4 * i + 3]);
+  __syncthreads();
+}
+
+// The same verify with LPR (2 or 4) lanes per state row and two rows per
+// thread (K = V = 128 only; D * LPR / 2 threads): lane LPR i + h of warp w holds
+// rows R w + i and R w + i + R / 2 (R = 64 / LPR rows per warp), columns of the
+// packed decode's column groups l = NL h .. NL h + NL - 1 (NL = 8 / LPR; float4
+// chunks 8 m + l).  Each lane forms its partial sums s_l exactly as a
+// packed-decode lane does (lane_dot), adds them as the first rounds of the
+// packed decode's tree would, and exchanges with its LPR - 1 partners for the
+// rest of the tree, so every output and correction is bit-identical to the
+// 8-lane form.  A lane's operand loads from shared memory serve two rows, and
+// with four lanes per row a thread holds 64 state registers, so two blocks of
+// eight warps fit on an SM.
+//
+// The grid is persistent (items (row, value head) dealt round robin).  One
+// thread stages an item with nine TMA loads: the checkpoint as M tiles of
+// 128-byte swizzled rows (a quarter warp's reads of its rows' chunks fall in
+// distinct banks) and the window's q, k, v, gate and beta tiles.  Once an item's
+// rows are in registers and its window's vectors are formed, the staging area
+// is free, and the block's next item streams into it while this item's window
+// runs: an item starts with its data on chip.
+constexpr uint64_t kVerifyWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms per wait
+
+template <int LPR>
+__host__ __device__ constexpr int verify_lane_threads() {
+  return 128 * LPR / 2;
+}
+
+// The tensor maps the verify stages an item with: the checkpoint ([N HV V rows,
+// K] fp32, 128-byte swizzle, [V x 32] boxes), mixed_qkv ([B T rows, used
+// columns], [T x D] boxes: one key or value head's span for the window's T
+// tokens), the log-gates ([B T rows, HV] with [T x 4] boxes for GDN, [B T rows,
+// HV K] with [T x K] boxes for KDA) and beta ([B T rows, HV], [T x 4] boxes).
+struct VerifyMaps {
+  CUtensorMap state, qkv, g, beta;
+};
+
+template <int D, int GATE, int LPR>
+__global__ void __launch_bounds__(verify_lane_threads<LPR>(), 2)
+    lossless_verify_lanes_kernel(const DecodeParams P, float *tup_u, float *tup_k, float *tup_g,
+                                 const __grid_constant__ VerifyMaps maps) {
+  static_assert(D == 128 && (LPR == 2 || LPR == 4), "a 128-row state, two or four lanes per row");
+  constexpr int kT = verify_lane_threads<LPR>();
+  constexpr int M = D / 32;
+  constexpr int NL = 8 / LPR;        // column groups per lane
+  constexpr int RW = 64 / LPR;       // rows per warp
+  constexpr int GW = GATE == GDN_GATE_PER_K ? D : 4;  // columns of a staged gate row
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int h = lane % LPR;
+  const int row0 = warp * RW + lane / LPR, row1 = row0 + RW / 2;
+  const bool stores = h < 2;                   // lane 0 of a row group stores row0, lane 1 row1
+  const int my_row = h == 1 ? row1 : row0;
+  const int T = P.T;
+  const int items = P.B * P.HV;
+  const int esz = P.qkv_dtype == GDN_F32 ? 4 : 2;
+  extern __shared__ uint8_t verify_smem[];
+  // the checkpoint tiles need a 1024-byte aligned base (128-byte swizzle); the
+  // allocation has 1024 bytes of slack for it
+  uint8_t *sm = verify_smem + (((smem_addr(verify_smem) + 1023u) & ~1023u) - smem_addr(verify_smem));
+  // Checkpoint: M tiles of [D rows x 32 columns], row r's 16-byte chunk j of
+  // tile m at m * 128 D + 128 r + 16 (j ^ (r mod 8)).  Then the raw window
+  // inputs as the maps deliver them (q, k, v: [T][D] of the input type; gates
+  // [T][GW] and beta [T][4] fp32), each region 128-byte aligned, then the
+  // window's vectors.
+  const int qbytes = (T * D * esz + 127) & ~127;
+  uint8_t *rq = sm + M * D * 128, *rk = rq + qbytes, *rv = rk + qbytes;
+  float *rg = reinterpret_cast<float *>(rv + qbytes);
+  float *rb = rg + ((T * GW + 31) & ~31);
+  float *wq = rb + ((T * 4 + 31) & ~31);
+  float *wk = wq + T * D, *wv = wk + T * D, *wsc = wv + T * D;
+  float *wke = GATE == GDN_GATE_PER_K ? wsc + 4 * T : wk;  // KDA: a o k
+  float *wa = GATE == GDN_GATE_PER_K ? wke + T * D : wk;   // KDA: a
+  float *red = GATE == GDN_GATE_PER_K ? wa + T * D : wsc + 4 * T;  // [2 * kStageBatch][4]
+  const uint32_t bar = (smem_addr(red + 8 * kStageBatch) + 7u) & ~7u;  // the mbarrier, 8-byte aligned
+  const uint32_t s_base = smem_addr(sm);
+  const uint32_t tx_bytes = D * D * 4 + 3 * T * D * esz + T * GW * 4 + T * 16;
+
+  // One thread stages an item: nine TMA loads completing on `bar`.
+  auto stage = [&](int slot_, int b_, int hv_) {
+    const int hk_ = hv_ / P.G;
+    mbar_arrive_expect_tx(bar, tx_bytes);
+    const int y = (slot_ * P.HV + hv_) * D;
+#pragma unroll
+    for (int m = 0; m < M; ++m) tma_load_2d(s_base + m * D * 128, &maps.state, 32 * m, y, bar);
+    tma_load_2d(smem_addr(rq), &maps.qkv, hk_ * D, b_ * T, bar);
+    tma_load_2d(smem_addr(rk), &maps.qkv, (P.HK + hk_) * D, b_ * T, bar);
+    tma_load_2d(smem_addr(rv), &maps.qkv, 2 * P.HK * D + hv_ * D, b_ * T, bar);
+    tma_load_2d(smem_addr(rg), &maps.g, GATE == GDN_GATE_PER_K ? hv_ * D : hv_ & ~3, b_ * T, bar);
+    tma_load_2d(smem_addr(rb), &maps.beta, hv_ & ~3, b_ * T, bar);
+  };
+  if (t == 0) {
+    prefetch_tensormap(&maps.state);
+    prefetch_tensormap(&maps.qkv);
+    prefetch_tensormap(&maps.g);
+    prefetch_tensormap(&maps.beta);
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  int staged = -1;  // the item whose checkpoint and inputs are in flight to shared memory
+  bool failed = false;
+  int slot = blockIdx.x < items ? P.idx[blockIdx.x / P.HV] : -1;  // then carried from the item before
+
+#pragma unroll 1
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int b = item / P.HV, hv = item % P.HV;
+    const int next = item + gridDim.x;
+    const int next_slot = next < items ? P.idx[next / P.HV] : -1;  // used once this item's inputs are formed
+    const int cur = slot;
+    slot = next_slot;
+    if (cur >= P.N && hv == 0 && t == 0) set_status(P.status, GDN_DEV_BAD_SLOT);
+    if (cur < 0 || cur >= P.N) {  // padding row: zeros for every token, tuples untouched
+      for (int tok = 0; tok < T; ++tok)
+        if (t < D) store_from_f32(P.out, (((int64_t)b * T + tok) * P.HV + hv) * D + t, P.out_dtype, 0.f);
+      continue;
+    }
+    const int hk = hv / P.G;
+    if (staged != item && t == 0) stage(cur, b, hv);  // else it arrived during the previous item's window
+    staged = item;
+    const bool landed = mbar_wait_bounded(bar, phase, kVerifyWaitLimitNs);
+    phase ^= 1u;
+    if (__syncthreads_or(!landed)) {  // the copies did not land: report, stop this block
+      if (t == 0) set_status(P.status, GDN_DEV_TIMEOUT);
+      failed = true;
+      break;
+    }
+
+    for (int tok0 = 0; tok0 < T; tok0 += kStageBatch) {
+      // finish_qkv's arithmetic for kStageBatch tokens at once: the optional L2
+      // norm, q_scale, k^T q, each block sum formed as block_sum2 forms it
+      float qt[kStageBatch], kt[kStageBatch], kq[kStageBatch];
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int tok = tok0 + u;
+        qt[u] = kt[u] = 0.f;
+        if (t < D && tok < T) {
+          const int i = tok * D + t;
+          const QkvBits bits = esz == 4 ? QkvBits{reinterpret_cast<const uint32_t *>(rq)[i],
+                                                  reinterpret_cast<const uint32_t *>(rk)[i],
+                                                  reinterpret_cast<const uint32_t *>(rv)[i]}
+                                        : QkvBits{reinterpret_cast<const uint16_t *>(rq)[i],
+                                                  reinterpret_cast<const uint16_t *>(rk)[i],
+                                                  reinterpret_cast<const uint16_t *>(rv)[i]};
+          const QkvRaw x = qkv_from_bits(bits, P.qkv_dtype);
+          qt[u] = x.q;
+          kt[u] = x.k;
+          wv[i] = x.v;
+        }
+      }
+      if (P.qk_l2norm) {
+        float n[2 * kStageBatch];
+#pragma unroll
+        for (int u = 0; u < kStageBatch; ++u) {
+          n[u] = __fmul_rn(qt[u], qt[u]);
+          n[kStageBatch + u] = __fmul_rn(kt[u], kt[u]);
+        }
+        block_sums<2 * kStageBatch>(n, red);
+#pragma unroll
+        for (int u = 0; u < kStageBatch; ++u) {
+          qt[u] = __fdiv_rn(qt[u], __fsqrt_rn(__fadd_rn(n[u], 1e-6f)));
+          kt[u] = __fdiv_rn(kt[u], __fsqrt_rn(__fadd_rn(n[kStageBatch + u], 1e-6f)));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        qt[u] = __fmul_rn(qt[u], P.q_scale);
+        kq[u] = __fmul_rn(kt[u], qt[u]);
+      }
+      block_sums<kStageBatch>(kq, red);
+      const bool key_writer = hv % P.G == 0;
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int tok = tok0 + u;
+        if (tok < T) {
+          const int64_t row = (int64_t)b * T + tok;
+          if (t < D) {
+            if (GATE == GDN_GATE_PER_K) {
+              const float graw = rg[tok * GW + t];
+              const float a = expf(graw);
+              wq[tok * D + t] = __fmul_rn(a, qt[u]);
+              wke[tok * D + t] = __fmul_rn(a, kt[u]);
+              wa[tok * D + t] = a;
+              tup_g[(row * P.HV + hv) * D + t] = graw;
+            } else {
+              wq[tok * D + t] = qt[u];
+            }
+            wk[tok * D + t] = kt[u];
+            if (key_writer) tup_k[(row * P.HK + hk) * D + t] = kt[u];
+          }
+          if (t == tok) {  // the token's scalars, one thread per token
+            const float graw = rg[tok * GW + (GATE == GDN_GATE_PER_K ? 0 : (hv & 3))];
+            wsc[4 * tok + 0] = GATE == GDN_GATE_SCALAR ? expf(graw) : 1.f;
+            wsc[4 * tok + 1] = rb[tok * 4 + (hv & 3)];
+            wsc[4 * tok + 2] = kq[u];
+            if (GATE == GDN_GATE_SCALAR) tup_g[row * P.HV + hv] = graw;
+          }
+        }
+      }
+    }
+
+    float4 st[2][M * NL];  // [row][m * NL + li]: chunk 8 m + NL h + li of the row
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+      for (int li = 0; li < NL; ++li) {
+        const int j = NL * h + li;
+        st[0][m * NL + li] = *reinterpret_cast<const float4 *>(sm + m * D * 128 + row0 * 128 + 16 * (j ^ (row0 & 7)));
+        st[1][m * NL + li] = *reinterpret_cast<const float4 *>(sm + m * D * 128 + row1 * 128 + 16 * (j ^ (row1 & 7)));
+      }
+    // the window's vectors are in place, and the staged checkpoint and raw
+    // inputs are free: the next item's stream in under this window
+    fence_proxy_async_smem();
+    __syncthreads();
+    staged = -1;
+    if (next_slot >= 0 && next_slot < P.N) {
+      if (t == 0) stage(next_slot, next / P.HV, next % P.HV);
+      staged = next;
+    }
+
+#pragma unroll 1
+    for (int tok = 0; tok < T; ++tok) {
+      const float alpha = wsc[4 * tok], beta = wsc[4 * tok + 1], kq = wsc[4 * tok + 2];
+      const float4 *xq4 = reinterpret_cast<const float4 *>(wq + tok * D);
+      const float4 *xk4 = reinterpret_cast<const float4 *>(wke + tok * D);
+      const float4 *kr4 = reinterpret_cast<const float4 *>(wk + tok * D);
+      const float4 *a44 = reinterpret_cast<const float4 *>(wa + tok * D);
+      float pq[2][NL], pk[2][NL];
+#pragma unroll
+      for (int li = 0; li < NL; ++li) {
+        float2 loq[2], hiq[2], lok[2], hik[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) loq[j] = hiq[j] = lok[j] = hik[j] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const float4 xq = xq4[8 * m + NL * h + li], xk = xk4[8 * m + NL * h + li];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float4 &s = st[j][m * NL + li];
+            loq[j] = __ffma2_rn(make_float2(s.x, s.y), make_float2(xq.x, xq.y), loq[j]);
+            hiq[j] = __ffma2_rn(make_float2(s.z, s.w), make_float2(xq.z, xq.w), hiq[j]);
+            lok[j] = __ffma2_rn(make_float2(s.x, s.y), make_float2(xk.x, xk.y), lok[j]);
+            hik[j] = __ffma2_rn(make_float2(s.z, s.w), make_float2(xk.z, xk.w), hik[j]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          pq[j][li] = __fadd_rn(__fadd_rn(loq[j].x, loq[j].y), __fadd_rn(hiq[j].x, hiq[j].y));
+          pk[j][li] = __fadd_rn(__fadd_rn(lok[j].x, lok[j].y), __fadd_rn(hik[j].x, hik[j].y));
+        }
+      }
+      float d[2], o[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float sq, sk;
+        if constexpr (NL == 4) {
+          sq = __fadd_rn(__fadd_rn(pq[j][0], pq[j][1]), __fadd_rn(pq[j][2], pq[j][3]));
+          sk = __fadd_rn(__fadd_rn(pk[j][0], pk[j][1]), __fadd_rn(pk[j][2], pk[j][3]));
+        } else {
+          sq = __fadd_rn(pq[j][0], pq[j][1]);
+          sk = __fadd_rn(pk[j][0], pk[j][1]);
+        }
+#pragma unroll
+        for (int x = 1; x < LPR; x <<= 1) {
+          sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, x));
+          sk = __fadd_rn(sk, __shfl_xor_sync(0xffffffffu, sk, x));
+        }
+        o[j] = token_finish<GATE>(sq, sk, alpha, beta, wv[tok * D + (j ? row1 : row0)], kq, d[j]);
+      }
+      const int64_t orow = ((int64_t)b * T + tok) * P.HV + hv;
+      if (stores) {
+        store_from_f32(P.out, orow * D + my_row, P.out_dtype, h == 1 ? o[1] : o[0]);
+        tup_u[orow * D + my_row] = h == 1 ? d[1] : d[0];
+      }
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int li = 0; li < NL; ++li) {
+          const float4 kr = kr4[8 * m + NL * h + li];
+          const float4 a4 = GATE == GDN_GATE_PER_K ? a44[8 * m + NL * h + li] : make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            st[j][m * NL + li] = token_update<GATE>(st[j][m * NL + li], kr, a4, alpha, d[j]);
+        }
+    }
+    __syncthreads();  // the next item's inputs overwrite the window's vectors
+  }
+  if (failed)  // copies may still be in flight: give them the limit again before the block leaves
+    mbar_wait_bounded(bar, phase ^ 1u, kVerifyWaitLimitNs);
+}
+
 // Exact-order commit ([P5] Modifications, Commit): row b's first a =
 // accepted[b] tuples are replayed from state[src], src = ssm_state_indices[b],
 // with the packed decode's own update (token_update: fl(alpha s), then one fma
@@ -913,18 +1231,13 @@ cudaError_t launch_spec_verify(const DecodeParams &P, int D, int gate, cudaStrea
   return gate == GDN_GATE_SCALAR ? launch_spec_t<64, 0>(P, s) : launch_spec_t<64, 1>(P, s);
 }
 
-// Row groups of four rows a verify thread keeps in registers at once (of 8 for K = 128;
-// two measured fastest: more raise the registers per thread and cut occupancy).
-#ifndef GDN_VERIFY_ROW_GROUPS
-#define GDN_VERIFY_ROW_GROUPS 2
-#endif
-constexpr int kVerifyRowGroups = GDN_VERIFY_ROW_GROUPS;
-
-template <int D, int GATE>
-static cudaError_t launch_lossless_verify_t(const DecodeParams &P, float *tu, float *tk, float *tg,
-                                            cudaStream_t s) {
+// D = 64: the 8-lane layout with all four row groups of a warp in registers.
+template <int GATE>
+static cudaError_t launch_lossless_verify_64(const DecodeParams &P, float *tu, float *tk, float *tg,
+                                             cudaStream_t s) {
+  constexpr int D = 64;
   const size_t smem = (5 * (size_t)P.T * D + 4 * (size_t)P.T + 3 * (size_t)D + 8) * sizeof(float);
-  auto kern = lossless_verify_kernel<D, GATE, (D == 128 ? kVerifyRowGroups : 4)>;
+  auto kern = lossless_verify_kernel<D, GATE, 4>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -933,13 +1246,76 @@ static cudaError_t launch_lossless_verify_t(const DecodeParams &P, float *tu, fl
   return cudaGetLastError();
 }
 
+// D = 128: two lanes per row, two rows per thread; the checkpoint tiles, the
+// window's raw tiles and vectors (three of them for GDN, five for KDA) share the
+// block's shared memory, at most 203 KB (a 32-token KDA window of fp32 inputs).
+// Where the tensor maps cannot describe the inputs (a buffer or row stride not a
+// multiple of 16 bytes, HV not a multiple of 4, coordinates past 2^31), the
+// 8-lane form runs.
+template <int GATE>
+static cudaError_t launch_lossless_verify_128(const DecodeParams &P, float *tu, float *tk, float *tg,
+                                              cudaStream_t s) {
+  constexpr int D = 128;
+  constexpr int GW = GATE == GDN_GATE_PER_K ? D : 4;
+  const size_t esz = P.qkv_dtype == GDN_F32 ? 4 : 2;
+  const int64_t rows = (int64_t)P.B * P.T;
+  const int64_t cols = 2 * (int64_t)P.HK * D + (int64_t)P.HV * D;
+  const int64_t gcols = (int64_t)P.HV * (GATE == GDN_GATE_PER_K ? D : 1);
+  VerifyMaps maps;
+  const char *why = nullptr;
+  bool ok = (int64_t)P.N * P.HV * D < ((int64_t)1 << 31) && cols < ((int64_t)1 << 31) &&
+            rows < ((int64_t)1 << 31) && P.HV % 4 == 0 && ((size_t)P.qkv_stride * esz) % 16 == 0 &&
+            reinterpret_cast<uintptr_t>(P.qkv) % 16 == 0 && reinterpret_cast<uintptr_t>(P.g) % 16 == 0 &&
+            reinterpret_cast<uintptr_t>(P.beta) % 16 == 0;
+  ok = ok && make_state_tmap(P, D, &maps.state, &why) == cudaSuccess;
+  ok = ok && make_tmap_2d(P.qkv, P.qkv_dtype, cols, rows, (uint64_t)P.qkv_stride * esz, D, P.T, &maps.qkv) == cudaSuccess;
+  ok = ok && make_tmap_2d(P.g, GDN_F32, gcols, rows, gcols * 4, GW, P.T, &maps.g) == cudaSuccess;
+  ok = ok && make_tmap_2d(P.beta, GDN_F32, P.HV, rows, (uint64_t)P.HV * 4, 4, P.T, &maps.beta) == cudaSuccess;
+  if (!ok) {
+    const size_t smem = (5 * (size_t)P.T * D + 4 * (size_t)P.T + 3 * (size_t)D + 8) * sizeof(float);
+    auto kern = lossless_verify_kernel<D, GATE, 2>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)P.B * P.HV, kThreads, smem, s>>>(P, tu, tk, tg);
+    return cudaGetLastError();
+  }
+  const size_t vecs = GATE == GDN_GATE_PER_K ? 5 : 3;
+  const size_t qbytes = ((size_t)P.T * D * esz + 127) & ~(size_t)127;
+  const size_t smem = 1024 + (size_t)D * D * 4 + 3 * qbytes +
+                      (((size_t)P.T * GW + 31) & ~(size_t)31) * 4 + (((size_t)P.T * 4 + 31) & ~(size_t)31) * 4 +
+                      (vecs * (size_t)P.T * D + 4 * (size_t)P.T + 8 * kStageBatch) * sizeof(float) + 16;
+  constexpr int LPR = 2;
+  constexpr int kT = verify_lane_threads<LPR>();
+  auto kern = lossless_verify_lanes_kernel<D, GATE, LPR>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // resident blocks on this device for this shared-memory size (the window
+  // length and the input width change it), looked up once per (device, window, width)
+  static int resident[64][33][2] = {};
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  const int wide = P.qkv_dtype == GDN_F32;
+  int slots = dev < 64 ? resident[dev][P.T][wide] : 0;
+  if (slots == 0) {
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kT, smem)) != cudaSuccess) return e;
+    slots = (per_sm < 1 ? 1 : per_sm) * sms;
+    if (dev < 64) resident[dev][P.T][wide] = slots;
+  }
+  const int64_t items = (int64_t)P.B * P.HV;
+  const int64_t grid = items < slots ? items : slots;
+  kern<<<(unsigned)grid, kT, smem, s>>>(P, tu, tk, tg, maps);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lossless_verify(const DecodeParams &P, int D, int gate, float *tup_u, float *tup_k,
                                    float *tup_g, cudaStream_t s) {
   if (D == 128)
-    return gate == GDN_GATE_SCALAR ? launch_lossless_verify_t<128, 0>(P, tup_u, tup_k, tup_g, s)
-                                   : launch_lossless_verify_t<128, 1>(P, tup_u, tup_k, tup_g, s);
-  return gate == GDN_GATE_SCALAR ? launch_lossless_verify_t<64, 0>(P, tup_u, tup_k, tup_g, s)
-                                 : launch_lossless_verify_t<64, 1>(P, tup_u, tup_k, tup_g, s);
+    return gate == GDN_GATE_SCALAR ? launch_lossless_verify_128<0>(P, tup_u, tup_k, tup_g, s)
+                                   : launch_lossless_verify_128<1>(P, tup_u, tup_k, tup_g, s);
+  return gate == GDN_GATE_SCALAR ? launch_lossless_verify_64<0>(P, tup_u, tup_k, tup_g, s)
+                                 : launch_lossless_verify_64<1>(P, tup_u, tup_k, tup_g, s);
 }
 
 template <int D, int GATE>

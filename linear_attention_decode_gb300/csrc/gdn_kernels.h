@@ -43,6 +43,10 @@ cudaError_t launch_fold(const DecodeParams &P, int D, int gate, int n, cudaStrea
 // Tensor map of the checkpoint as [N*HV*V rows, K fp32 columns] with boxes of
 // [V rows x 32 columns], 128-byte swizzled.  Writes a reason into *why on failure.
 cudaError_t make_state_tmap(const DecodeParams &P, int D, CUtensorMap *map, const char **why);
+// A plain (unswizzled) 2-D tensor map: `rows` rows of `inner` elements of
+// `dtype` (a gdn_dtype_t), `row_bytes` apart, boxes of box_rows x box_inner.
+cudaError_t make_tmap_2d(const void *base, int dtype, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_rows, CUtensorMap *map);
 
 // Speculative verify window (P.T tokens per row) on the CUDA cores, and the
 // commit that follows.

@@ -337,6 +337,23 @@ cudaError_t make_state_tmap(const DecodeParams &P, int D, CUtensorMap *map, cons
   return cudaSuccess;
 }
 
+cudaError_t make_tmap_2d(const void *base, int dtype, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_rows, CUtensorMap *map) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt = dtype == GDN_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dtype == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_tc_decode(const DecodeParams &P, int D, int gate, cudaStream_t s, const char **why,
                              bool *fused) {
   *fused = false;

@@ -108,6 +108,14 @@ CASES = {
                                        seed=63), 32, torch.float32),
     "kda_k128_T8": (I.Workload("l", N=8, B=4, n_pad=1, HV=8, HK=4, K=128, L=1, ring_dtype=Bd.F32, qkv_dtype=Bd.BF16,
                                gate=Bd.GATE_PER_K, seed=64), 8, torch.float32),
+    # the longest window: the staged checkpoint and 32 tokens' vectors in one block's shared memory
+    "gdn_k128_T32": (I.Workload("l", N=6, B=3, n_pad=1, HV=4, HK=2, K=128, L=1, ring_dtype=Bd.F32, qkv_dtype=Bd.BF16,
+                                seed=66), 32, torch.float32),
+    "kda_k128_T32_f16out": (I.Workload("l", N=6, B=3, n_pad=0, HV=4, HK=2, K=128, L=1, ring_dtype=Bd.F32,
+                                       qkv_dtype=Bd.F16, gate=Bd.GATE_PER_K, seed=67), 32, torch.float16),
+    # HV not a multiple of 4: the gate and beta tiles cannot be mapped, the 8-lane form runs
+    "gdn_k128_hv6_T5": (I.Workload("l", N=6, B=3, n_pad=1, HV=6, HK=3, K=128, L=1, ring_dtype=Bd.F32,
+                                   qkv_dtype=Bd.BF16, seed=68), 5, torch.float32),
     "kda_k64_T3": (I.Workload("l", N=8, B=4, n_pad=1, HV=4, HK=4, K=64, L=1, ring_dtype=Bd.F32, qkv_dtype=Bd.F32,
                               gate=Bd.GATE_PER_K, seed=65), 3, torch.float32),
 }
@@ -252,12 +260,12 @@ def test_bad_rows_are_reported_and_touch_nothing(gdnlib):
         assert _same_bits(st, S_dev), (src, acc, dst)
 
 
-def test_layer_size_bit_identical(gdnlib):
-    """One Qwen3-Next-like layer (HV=32, HK=16, K=V=128) at B=256 and a 4-token
-    window: verify outputs and the committed states against the packed decodes,
-    bit for bit, over the whole batch."""
+@pytest.mark.parametrize("T", [4, 8])
+def test_layer_size_bit_identical(gdnlib, T):
+    """One Qwen3-Next-like layer (HV=32, HK=16, K=V=128) at B=256 and a 4- or
+    8-token window: verify outputs and the committed states against the packed
+    decodes, bit for bit, over the whole batch."""
     w = I.Workload("layer", N=256, B=256, n_pad=0, HV=32, HK=16, K=128, L=1, ring_dtype=Bd.F32, qkv_dtype=Bd.BF16, seed=73)
-    T = 4
     gen = I.generator(w.seed, "cuda")
     S_dev = I.state(gen, w.N, w.HV, w.V, w.K, "cuda")
     idx_dev = I.indices(gen, w.B, w.N, 0, "cuda")
