@@ -994,7 +994,72 @@ def run_ours(args):
         host_advance()
     torch.cuda.synchronize()
 
+    # Untimed legs first (the packed decode beside it and the end-to-end run
+    # through host buffers): they also bring the GPU to its working clocks and
+    # state before the K timed steps, which a short timed region would
+    # otherwise partly spend on.
     K = args.steps
+    if not args.kernel_only:
+        # in-repo packed decode on the workload's shapes (baseline: reads and writes
+        # the state; four disjoint slot sets in turn, so no launch hits L2)
+        pk = measure_packed(w, max(64, K // 8), dev)
+        packed_s = pk["ms_per_launch"] / 1e3
+        pbytes = pk["hbm_gbs_algorithmic"] * 1e9 * packed_s
+        torch.cuda.empty_cache()
+
+        # end to end through the public API with host buffers: every step copies
+        # its inputs from pinned host memory to the device, runs the decode +
+        # advance, and copies its output back to pinned host memory.  As a serving
+        # loop would, the copies run on their own streams with two device buffer
+        # sets, so step i + 1's inputs and step i - 1's output move while step i
+        # computes; events order every reuse of a buffer.
+        hq = [b.mixed_qkv.cpu().pin_memory() for b in batches]
+        hg = [b.g.cpu().pin_memory() for b in batches]
+        hb = [b.beta.cpu().pin_memory() for b in batches]
+        hi = idx.cpu().pin_memory()
+        NBUF = 2
+        houts = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(NBUF)]
+        dbuf = [(torch.empty_like(batches[0].mixed_qkv), torch.empty_like(batches[0].g),
+                 torch.empty_like(batches[0].beta), torch.empty_like(idx), torch.empty_like(out)) for _ in range(NBUF)]
+        h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        in_ready = [torch.cuda.Event() for _ in range(NBUF)]  # step's inputs on the device
+        used = [torch.cuda.Event() for _ in range(NBUF)]      # step's decode done with its buffers
+        out_back = [torch.cuda.Event() for _ in range(NBUF)]  # step's output in host memory
+        e2e_steps = max(64, K // 8)
+        h2d = hq[0].numel() * hq[0].element_size() + hg[0].numel() * 4 + hb[0].numel() * 4 + hi.numel() * 4
+        d2h = houts[0].numel() * houts[0].element_size()
+
+        def e2e_run(n):
+            for i in range(n):
+                k, j = i % NBUF, i % POOL
+                dq, dg, db, di, do = dbuf[k]
+                if i >= NBUF:
+                    h2d_s.wait_event(used[k])  # the decode of step i - 2 has read these inputs
+                with torch.cuda.stream(h2d_s):
+                    dq.copy_(hq[j], non_blocking=True)
+                    dg.copy_(hg[j], non_blocking=True)
+                    db.copy_(hb[j], non_blocking=True)
+                    di.copy_(hi, non_blocking=True)
+                in_ready[k].record(h2d_s)
+                stream.wait_event(in_ready[k])
+                if i >= NBUF:
+                    stream.wait_event(out_back[k])  # step i - 2's output has left this buffer
+                Bd.gdn_replayssm_decode_advance(desc, cache, wp, None, Bd.Step(dq, dg, db, di, do), adv_ws, recon,
+                                                None, None, stream)
+                used[k].record(stream)
+                d2h_s.wait_event(used[k])
+                with torch.cuda.stream(d2h_s):
+                    houts[k].copy_(do, non_blocking=True)
+                out_back[k].record(d2h_s)
+            torch.cuda.synchronize()
+
+        e2e_run(8)  # warm the streams and events
+        t0 = time.perf_counter()
+        e2e_run(e2e_steps)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        for _ in range(8 + e2e_steps):  # the e2e steps advanced the cursors too
+            host_advance()
+
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # the cursors follow the advance rule, so every timed launch's bytes are
     # known up front (no host bookkeeping inside the timed region)
@@ -1038,64 +1103,6 @@ def run_ours(args):
         if ws > 1:
             dist.destroy_process_group()
         return 0
-
-    # in-repo packed decode on the workload's shapes (baseline: reads and writes
-    # the state; four disjoint slot sets in turn, so no launch hits L2)
-    pk = measure_packed(w, max(64, K // 8), dev)
-    packed_s = pk["ms_per_launch"] / 1e3
-    pbytes = pk["hbm_gbs_algorithmic"] * 1e9 * packed_s
-    torch.cuda.empty_cache()
-
-    # end to end through the public API with host buffers: every step copies
-    # its inputs from pinned host memory to the device, runs the decode +
-    # advance, and copies its output back to pinned host memory.  As a serving
-    # loop would, the copies run on their own streams with two device buffer
-    # sets, so step i + 1's inputs and step i - 1's output move while step i
-    # computes; events order every reuse of a buffer.
-    hq = [b.mixed_qkv.cpu().pin_memory() for b in batches]
-    hg = [b.g.cpu().pin_memory() for b in batches]
-    hb = [b.beta.cpu().pin_memory() for b in batches]
-    hi = idx.cpu().pin_memory()
-    NBUF = 2
-    houts = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(NBUF)]
-    dbuf = [(torch.empty_like(batches[0].mixed_qkv), torch.empty_like(batches[0].g),
-             torch.empty_like(batches[0].beta), torch.empty_like(idx), torch.empty_like(out)) for _ in range(NBUF)]
-    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    in_ready = [torch.cuda.Event() for _ in range(NBUF)]  # step's inputs on the device
-    used = [torch.cuda.Event() for _ in range(NBUF)]      # step's decode done with its buffers
-    out_back = [torch.cuda.Event() for _ in range(NBUF)]  # step's output in host memory
-    e2e_steps = max(64, K // 8)
-    h2d = hq[0].numel() * hq[0].element_size() + hg[0].numel() * 4 + hb[0].numel() * 4 + hi.numel() * 4
-    d2h = houts[0].numel() * houts[0].element_size()
-
-    def e2e_run(n):
-        for i in range(n):
-            k, j = i % NBUF, i % POOL
-            dq, dg, db, di, do = dbuf[k]
-            if i >= NBUF:
-                h2d_s.wait_event(used[k])  # the decode of step i - 2 has read these inputs
-            with torch.cuda.stream(h2d_s):
-                dq.copy_(hq[j], non_blocking=True)
-                dg.copy_(hg[j], non_blocking=True)
-                db.copy_(hb[j], non_blocking=True)
-                di.copy_(hi, non_blocking=True)
-            in_ready[k].record(h2d_s)
-            stream.wait_event(in_ready[k])
-            if i >= NBUF:
-                stream.wait_event(out_back[k])  # step i - 2's output has left this buffer
-            Bd.gdn_replayssm_decode_advance(desc, cache, wp, None, Bd.Step(dq, dg, db, di, do), adv_ws, recon,
-                                            None, None, stream)
-            used[k].record(stream)
-            d2h_s.wait_event(used[k])
-            with torch.cuda.stream(d2h_s):
-                houts[k].copy_(do, non_blocking=True)
-            out_back[k].record(d2h_s)
-        torch.cuda.synchronize()
-
-    e2e_run(8)  # warm the streams and events
-    t0 = time.perf_counter()
-    e2e_run(e2e_steps)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
 
     if rank != 0:
         if ws > 1:
