@@ -113,6 +113,14 @@ CASES = {
                                 seed=66), 32, torch.float32),
     "kda_k128_T32_f16out": (I.Workload("l", N=6, B=3, n_pad=0, HV=4, HK=2, K=128, L=1, ring_dtype=Bd.F32,
                                        qkv_dtype=Bd.F16, gate=Bd.GATE_PER_K, seed=67), 32, torch.float16),
+    # one-token window, and the largest staging (a 32-token KDA window of fp32 inputs, 210 KB)
+    "gdn_k128_T1": (I.Workload("l", N=6, B=4, n_pad=1, HV=4, HK=2, K=128, L=1, ring_dtype=Bd.F32, qkv_dtype=Bd.BF16,
+                               seed=69), 1, torch.float32),
+    "kda_k128_T32_fp32qkv": (I.Workload("l", N=4, B=2, n_pad=0, HV=4, HK=4, K=128, L=1, ring_dtype=Bd.F32,
+                                        qkv_dtype=Bd.F32, gate=Bd.GATE_PER_K, seed=70), 32, torch.float32),
+    # several items per block of the persistent verify, padding rows among them
+    "gdn_k128_many_items_padded": (I.Workload("l", N=64, B=48, n_pad=8, HV=32, HK=16, K=128, L=1,
+                                              ring_dtype=Bd.F32, qkv_dtype=Bd.BF16, seed=71), 3, torch.bfloat16),
     # HV not a multiple of 4: the gate and beta tiles cannot be mapped, the 8-lane form runs
     "gdn_k128_hv6_T5": (I.Workload("l", N=6, B=3, n_pad=1, HV=6, HK=3, K=128, L=1, ring_dtype=Bd.F32,
                                    qkv_dtype=Bd.BF16, seed=68), 5, torch.float32),
