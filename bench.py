@@ -14,7 +14,7 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|referenc
        [--sweep [--sweep-batches 1,8,...] [--sweep-lens 1,4,...]]  (one JSON line per point)
        [--spec [--spec-batches 64,256] [--spec-windows 2,4,8] [--spec-accept 0.7]]
                          (speculative verify window + commit + fold, one JSON line per point)
-       [--graph [--graph-batches 1,8,64,256]]  (CUDA-graph replay vs one-by-one launches)
+       [--graph [--graph-batches 1,8,64,256] [--graph-layers 30]]  (CUDA-graph replay vs one-by-one launches)
        [--lossless [--spec-batches ...] [--spec-windows ...]]
                          (lossless verify + exact-order commit, one JSON line per point)
 Under torchrun each rank runs an independent replica on its own GPU (the
@@ -886,6 +886,89 @@ def measure_graph(B, n, warmup, dev, extra_flags=0):
             "eager_vs_packed": p_eager_us / eager_us, "graph_vs_packed_graph": p_graph_us / graph_us}
 
 
+def measure_graph_stack(B, layers, n, warmup, dev):
+    """A model's decode steps at batch B: `layers` GDN layers (L=16, fp16 ring,
+    each with its own cache and one cursor array), one step = gdn_replayssm_decode
+    on every layer but the last (every layer after the first with
+    STEP_OVERLAP_PREVIOUS: the launch before it is another layer's decode) and
+    gdn_replayssm_decode_advance on the last; against the packed decode on every
+    layer (its own state pools).  n steps launched one by one (prepared calls on
+    both sides) and as one captured CUDA graph; per-layer times.  Kernel-only,
+    inputs resident."""
+    import torch
+
+    from linear_attention_decode_gb300 import binding as Bd
+    from linear_attention_decode_gb300 import inputs as I
+
+    w = I.with_(I.sweep_point(B, 16, Bd.F16), N=max(B, 16))
+    gen = I.generator(w.seed, dev)
+    wp = I.write_pos(gen, w, dev)
+    caches, pstates = [], []
+    for _ in range(layers):
+        c = I.cache(gen, w, wp, dev)
+        caches.append(Bd.Cache(c.state, c.ring_d, c.ring_k, c.ring_g))
+        pstates.append(I.state(gen, w.N, w.HV, w.V, w.K, dev))
+    idx = I.indices(gen, w.B, w.N, w.n_pad, dev)
+    desc = Bd.layer_desc(w.N, w.HV, w.HK, w.K, w.V, w.L, gate=w.gate, ring_dtype=w.ring_dtype)
+    out = torch.empty((idx.shape[0], w.HV, w.V), dtype=torch.bfloat16, device=dev)
+    ins = [I.step_inputs(gen, w, dev) for _ in range(2)]
+    first = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out) for b in ins]
+    later = [Bd.Step(b.mixed_qkv, b.g, b.beta, idx, out, flags=Bd.STEP_OVERLAP_PREVIOUS) for b in ins]
+    ws = Bd.decode_advance_workspace(dev)
+
+    # every call prepared once (checked and packed), as a serving loop would,
+    # on both sides, so the eager numbers compare launches, not marshalling
+    rcalls = [[Bd.prepare_replayssm_decode(desc, caches[layer], wp, None, (first if layer == 0 else later)[k],
+                                           Bd.RECON_TENSOR, ws if layer == layers - 1 else None)
+               for layer in range(layers)] for k in range(2)]
+    pcalls = [[Bd.prepare_packed_decode(desc, pstates[layer], first[k]) for layer in range(layers)]
+              for k in range(2)]
+
+    def seq(stream):
+        h = stream.cuda_stream
+        for i in range(n):
+            for layer in range(layers):
+                rcalls[(i + layer) % 2][layer].run(h)
+
+    def pseq(stream):
+        h = stream.cuda_stream
+        for i in range(n):
+            for layer in range(layers):
+                pcalls[(i + layer) % 2][layer].run(h)
+
+    def timed(fn, stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (n * layers)
+
+    cur = torch.cuda.current_stream()
+    res = {}
+    for name, f in (("replay", seq), ("packed", pseq)):
+        for _ in range(max(1, warmup // n + 1)):
+            f(cur)
+        eager = timed(lambda: f(cur), cur)
+        graph = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(graph, stream=cs):
+                f(cs)
+        graph.replay()
+        torch.cuda.synchronize()
+        res[name] = (eager, timed(graph.replay, cur))
+    kernel = Bd.gdn_replayssm_decode_kernel(desc, caches[0], later[0], Bd.RECON_TENSOR)
+    return {"workload": f"{layers}-layer stack: N={w.N} B={B} HV={w.HV} HK={w.HK} K=V={w.K} L={w.L} fp16 ring bf16 qkv",
+            "B": B, "layers": layers,
+            "kernel": {0: "persistent_tc", 1: "per_head_tc", 3: "small_batch"}.get(kernel),
+            "steps_per_graph": n, "eager_us_per_layer": res["replay"][0], "graph_us_per_layer": res["replay"][1],
+            "packed_eager_us_per_layer": res["packed"][0], "packed_graph_us_per_layer": res["packed"][1],
+            "eager_vs_packed": res["packed"][0] / res["replay"][0],
+            "graph_vs_packed_graph": res["packed"][1] / res["replay"][1]}
+
+
 def run_graph(args):
     """CUDA-graph replay against one-by-one launches: one JSON line per batch."""
     import torch
@@ -900,8 +983,11 @@ def run_graph(args):
     Bd.load_library()
     dev = torch.device("cuda", torch.cuda.current_device())
     for B in [int(x) for x in args.graph_batches.split(",")]:
-        print(json.dumps(measure_graph(B, 64, args.warmup, dev,
-                                       Bd.STEP_PERSISTENT_KERNEL if args.persistent_kernel else 0)), flush=True)
+        if args.graph_layers > 1:
+            print(json.dumps(measure_graph_stack(B, args.graph_layers, 8, args.warmup, dev)), flush=True)
+        else:
+            print(json.dumps(measure_graph(B, 64, args.warmup, dev,
+                                           Bd.STEP_PERSISTENT_KERNEL if args.persistent_kernel else 0)), flush=True)
         torch.cuda.empty_cache()
     return 0
 
@@ -1172,6 +1258,8 @@ def main():
     ap.add_argument("--graph", action="store_true",
                     help="CUDA-graph replay of 64 decode + advance steps against one-by-one launches")
     ap.add_argument("--graph-batches", default="1,8,64,256")
+    ap.add_argument("--graph-layers", type=int, default=1,
+                    help="with --graph: a stack of this many layers per step (overlap flag on all but the first)")
     ap.add_argument("--lossless", action="store_true",
                     help="lossless verify + exact-order commit sweep (one JSON line per batch x window)")
     ap.add_argument("--spec-batches", default="64,256")

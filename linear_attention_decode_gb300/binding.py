@@ -256,6 +256,61 @@ def gdn_replayssm_decode_advance(desc: LayerDesc, cache: Cache, write_pos: torch
         _status_ptr(dev_status), _stream(stream)), "gdn_replayssm_decode_advance")
 
 
+class PreparedCall:
+    """One decode call's arguments checked and packed once, for a loop that
+    calls it again and again with the same tensors (the buffers of a serving
+    step: the caller refills them in place, keeps them alive and keeps their
+    shapes, dtypes and addresses).  ``run()`` is then a single foreign call:
+    what a Python loop pays per launch at small batch, where the kernels take a
+    few microseconds.  Built by ``prepare_packed_decode`` and
+    ``prepare_replayssm_decode``."""
+
+    def __init__(self, fn, args, keep, name):
+        self._fn, self._args, self._keep, self._name = fn, args, keep, name
+
+    def run(self, stream=None) -> None:
+        """The call on `stream` (a torch stream or a raw handle; default: the
+        current stream)."""
+        status = self._fn(*self._args, _stream(stream))
+        if status != 0:
+            _check(status, self._name)
+
+
+def prepare_packed_decode(desc: LayerDesc, state: torch.Tensor, step: Step,
+                          dev_status: Optional[torch.Tensor] = None) -> PreparedCall:
+    """gdn_packed_decode with its arguments checked and packed once."""
+    st = _dev(state, "state", (desc.num_slots, desc.num_v_heads, desc.v_dim, desc.k_dim), torch.float32)
+    d = LayerDesc.from_buffer_copy(desc)
+    s = _pack_step(desc, step)
+    lib = load_library()
+    return PreparedCall(lib.gdn_packed_decode, (ctypes.byref(d), st, ctypes.byref(s), _status_ptr(dev_status)),
+                        (d, s, state, step, dev_status), "gdn_packed_decode")
+
+
+def prepare_replayssm_decode(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor,
+                             force_flush: Optional[torch.Tensor], step: Step,
+                             recon: int = RECON_TENSOR, workspace: Optional[torch.Tensor] = None,
+                             flushed_out: Optional[torch.Tensor] = None,
+                             dev_status: Optional[torch.Tensor] = None) -> PreparedCall:
+    """gdn_replayssm_decode (or, with a workspace, gdn_replayssm_decode_advance)
+    with its arguments checked and packed once."""
+    B = step.ssm_state_indices.shape[0]
+    d = LayerDesc.from_buffer_copy(desc)
+    c = _pack_cache(desc, cache)
+    s = _pack_step(desc, step)
+    common = (ctypes.byref(d), ctypes.byref(c), _dev(write_pos, "write_pos", (desc.num_slots,), torch.int32),
+              _dev(force_flush, "force_flush", (B,), torch.uint8, optional=True), ctypes.byref(s), int(recon),
+              _dev(flushed_out, "flushed_out", (B,), torch.uint8, optional=True))
+    keep = (d, c, s, cache, write_pos, force_flush, step, workspace, flushed_out, dev_status)
+    lib = load_library()
+    if workspace is None:
+        return PreparedCall(lib.gdn_replayssm_decode, common + (_status_ptr(dev_status),), keep,
+                            "gdn_replayssm_decode")
+    ws = _dev(workspace, "workspace", (DECODE_ADVANCE_WORKSPACE_BYTES // 4,), torch.int32)
+    return PreparedCall(lib.gdn_replayssm_decode_advance, common + (ws, _status_ptr(dev_status)), keep,
+                        "gdn_replayssm_decode_advance")
+
+
 def gdn_replayssm_decode_advance_noalloc(desc: LayerDesc, cache: Cache, write_pos: torch.Tensor,
                                          force_flush: Optional[torch.Tensor], step: Step,
                                          recon: int = RECON_TENSOR, flushed_out: Optional[torch.Tensor] = None,
