@@ -107,6 +107,20 @@ def test_chunked_replay_boundaries(ring, L):
     assert sum(s.flushes for s in rep.steps) > 0
 
 
+@pytest.mark.parametrize("ring", [Bd.F16, Bd.F32], ids=["f16", "f32"])
+@pytest.mark.parametrize("L", [24, 34])
+def test_chunked_replay_boundaries_kda(ring, L):
+    """The same depths with per-channel gates (KDA: the decays fold onto each
+    chunk's keys).  Where the persistent layout does not fit (a KDA ring of
+    fp32 entries carries K gate floats per entry as well), the per-head
+    tensor-core kernel takes the launch; either must match the oracle."""
+    w = I.Workload(f"kda L{L}", N=24, B=12, n_pad=1, HV=4, HK=4, K=128, L=L, ring_dtype=ring,
+                   qkv_dtype=Bd.BF16, gate=Bd.GATE_PER_K, steps=L + 4, staggered=True, seed=16)
+    assert _kernel_for(w, TCP) in (Bd.KERNEL_PERSISTENT_TC, Bd.KERNEL_PER_HEAD_TC)
+    rep = run_parity(w, TCP)
+    assert sum(s.flushes for s in rep.steps) > 0
+
+
 @pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
 def test_forced_flush_mid_ring(recon):
     sched = lambda t, rows: (np.arange(rows) % 3 == t % 3).astype(np.uint8) if t % 5 == 2 else np.zeros(rows, np.uint8)
