@@ -9,7 +9,7 @@ uniformly over [0, L) so flush and append rows mix in every launch.  Every step
 reads 512 MiB of checkpoint (4x the 129 MB L2), so no L2 flush is needed.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       [--workload headline|qwen3next_layer|kda_layer|stack30|sweep:B:L:f16|f32] [--recon tensor|ffma|output]
+       [--workload headline|qwen3next_layer|kda_layer|kda_layer:L:f16|f32|stack30|stack30:B|sweep:B:L:f16|f32] [--recon tensor|ffma|output]
        [--kernel-only]   (timed decode loop only: for profiling and sweeps)
        [--sweep [--sweep-batches 1,8,...] [--sweep-lens 1,4,...]]  (one JSON line per point)
        [--spec [--spec-batches 64,256] [--spec-windows 2,4,8] [--spec-accept 0.7]]
@@ -407,6 +407,11 @@ def pick_workload(name):
         return I.with_(I.QWEN3NEXT_LAYER, staggered=True)
     if name == "kda_layer":
         return I.with_(I.KDA_LAYER, staggered=True)
+    if name.startswith("kda_layer:"):  # the KDA layer with another ring length / ring type
+        _, L, rd = name.split(":")
+        tag = {"f16": "fp16", "f32": "fp32", "bf16": "bf16"}[rd]
+        return I.with_(I.KDA_LAYER, staggered=True, L=int(L), ring_dtype={"f16": F16, "f32": F32, "bf16": BF16}[rd],
+                       name=f"KDA layer: N=256 B=128 HV=HK=32 K=V=128 L={L} {tag} ring bf16 qkv")
     if name == "stack30":
         return I.with_(I.STACK30, staggered=True)
     if name.startswith("stack30:"):  # the 30-layer stack at another batch (same 320-slot pool)

@@ -45,8 +45,14 @@ constexpr int kItemsMax = 256;    // items one CTA may own (sets the table size)
 // Ring entries per landing slot and per operand tile stage when the whole
 // replay depth does not fit the shared-memory layout: the replay then runs in
 // chunks of kChunk entries that accumulate into the same TMEM accumulator;
-// chunks past the first come straight from the ring in global memory.
+// chunks past the first come straight from the ring in global memory.  A KDA
+// layer with an fp32 ring takes chunks of 8 entries (one tf32 K-step): that
+// halves its operand tiles and landing slots (d, k and the per-channel gates,
+// 4 bytes each) so that two items' checkpoint boxes still fit beside them.
 constexpr int kChunk = 16;
+__host__ __device__ constexpr int chunk_entries(int kind, int gate) {
+  return kind == 2 && gate == GDN_GATE_PER_K ? 8 : kChunk;
+}
 
 struct TcpLayout {
   int KD, KC, NT, NF, NL, NB;
@@ -72,8 +78,9 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
   const int es = kind == 2 ? 4 : 2;
   const int kstep = 32 / es;
   const int depth = L > 1 ? L - 1 : 0;
-  const int ldep = chunked && depth > kChunk ? kChunk : depth;  // ring entries of one chunk
-  t.CH = chunked && depth > kChunk ? kChunk : (depth > 0 ? depth : 1);
+  const int chunk = chunk_entries(kind, gate);
+  const int ldep = chunked && depth > chunk ? chunk : depth;  // ring entries of one chunk
+  t.CH = chunked && depth > chunk ? chunk : (depth > 0 ? depth : 1);
   t.KD = ldep ? ((ldep + kstep - 1) / kstep) * kstep : 0;
   t.KC = t.KD * es / 16;
   t.qkv_bulk = qkv_bulk;
@@ -109,8 +116,8 @@ static TcpLayout tcp_layout(int D, int kind, int gate, int L, int ring_bytes, in
 // The first (tile stages, landing slots) choice that leaves room for two items'
 // checkpoint boxes plus one more; else the one with the most boxes.  The whole
 // replay depth in one chunk first (one contraction per item, nothing loaded
-// past the landing); chunks of kChunk entries only when that leaves too few
-// boxes (fp32 rings beyond L = 17, any ring beyond L = 33).
+// past the landing); chunks only when that leaves too few boxes (GDN fp32
+// rings beyond L = 17, KDA fp32 rings beyond L = 9, any ring beyond L = 33).
 static TcpLayout tcp_pick_layout(int D, int kind, int gate, int L, int ring_bytes, int qkv_bytes, int qkv_bulk,
                                  int smem_budget) {
   static const int cand[4][2] = {{4, 4}, {2, 4}, {4, 2}, {2, 2}};
@@ -248,6 +255,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
   constexpr int BOX_BYTES = D * 128;
   constexpr int RB = RING_DT == GDN_F32 ? 4 : 2;
   constexpr int NVEC = GATE == GDN_GATE_PER_K ? 7 : 3;  // epilogue vectors per item
+  constexpr int kCh = chunk_entries(KIND, GATE);  // ring entries per replay chunk
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -587,15 +595,15 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       // into its place in the chunk's tile stage; the thread later rewrites
       // its own row in place (w_j d_j and k_j, rounded to tf32).
       constexpr bool kStaged = RING_DT == GDN_F32 && GATE == GDN_GATE_SCALAR;
-      constexpr int KCC = kChunk * ES / 16;  // 16-byte column chunks of a full chunk
+      constexpr int KCC = kCh * ES / 16;  // 16-byte column chunks of a full chunk
       auto stage_rows = [&](int c, int tc) {
         uint8_t *sA = tiles + tc * lay.tile_bytes, *sB = sA + lay.t_B;
         const float *rd = reinterpret_cast<const float *>(P.ring_d) + ((int64_t)slot * P.HV + hv) * P.L * D + pt;
         const float *rk = reinterpret_cast<const float *>(P.ring_k) + ((int64_t)slot * P.HK + hk) * P.L * D + pt;
         if (pt < D) {
 #pragma unroll
-          for (int e2 = 0; e2 < kChunk; ++e2) {
-            const int jj = c * kChunk + e2, jc = jj < p - 1 ? jj : p - 1;
+          for (int e2 = 0; e2 < kCh; ++e2) {
+            const int jj = c * kCh + e2, jc = jj < p - 1 ? jj : p - 1;
             cp_async4(smem_addr(sA + tile_off(pt, e2, KCC, 4)), rd + (int64_t)jc * D);
             cp_async4(smem_addr(sB + tile_off(pt, e2, KCC, 4)), rk + (int64_t)jc * D);
           }
@@ -633,7 +641,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       // the newest chunk's stage is free now (checked with the landing): its
       // copies overlap the work below
       if constexpr (kStaged) {
-        if (p > lay.CH) stage_rows((p - 1) / kChunk, t);
+        if (p > lay.CH) stage_rows((p - 1) / kCh, t);
       }
       float *f = reinterpret_cast<float *>(fields + s * lay.field_bytes);
       float *fq = f, *fk = f + D, *fv = f + 2 * D, *fke = f + 3 * D, *fa = f + 4 * D, *fA = f + 5 * D,
@@ -681,7 +689,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         kq = (pt >> 5) == 0 ? kq / (nq * nk) * P.q_scale : 0.f;
       }
 
-      // Operand rows, in chunks of kChunk ring entries, the newest chunk first
+      // Operand rows, in chunks of kCh ring entries, the newest chunk first
       // (GDN: A row pt w_j d_j[pt], B row pt k_j[pt]; KDA: A row pt d_j[pt],
       // B row pt w_j[pt] k_j[pt]).  Chunk 0 comes from the landing slot, later
       // chunks straight from the ring in global memory; each chunk fills one
@@ -695,7 +703,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
       float A = 1.f;
       const int jmax = p > 0 ? p - 1 : 0;
       const int ptc = pt < D ? pt : 0;
-      const int nch = p > lay.CH ? (p + kChunk - 1) / kChunk : 1;  // lay.CH is kChunk when it chunks
+      const int nch = p > lay.CH ? (p + kCh - 1) / kCh : 1;  // lay.CH is kCh when it chunks
       const int acc = 2 * pg + ((li >> 1) & 1);
       const uint32_t ua = (uint32_t)(li >> 2);
       const int64_t drow = ((int64_t)slot * P.HV + hv) * P.L;  // ring rows of (slot, hv) / (slot, hk)
@@ -767,7 +775,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
           }
         }
         uint8_t *tA = tiles + tc * lay.tile_bytes, *tB = tA + lay.t_B;
-        const int j0 = c * kChunk;
+        const int j0 = c * kCh;
         if (c == 0) {
           if (GATE == GDN_GATE_SCALAR) {
             for (int h = 0; h < lay.KC; ++h) {
@@ -837,7 +845,7 @@ __global__ void __launch_bounds__(kTcpThreads, 1)
         } else {
           // a chunk past the landed one, straight from global memory in two
           // halves, each half's loads in flight at once (registers allow no more)
-          constexpr int HALF = kChunk / 2;
+          constexpr int HALF = kCh / 2;
           constexpr int HPC = KCC / 2;           // column chunks per half
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {

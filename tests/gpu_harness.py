@@ -68,26 +68,29 @@ GUARD_WORD = 0x7FA5A5A5
 
 
 class Guarded:
-    """A device copy of a tensor between two guard bands (16-byte aligned body)."""
+    """A device copy of a tensor between two guard bands; the body starts
+    `offset` bytes past a 16-byte boundary (a multiple of the element size)."""
 
-    def __init__(self, t: torch.Tensor):
+    def __init__(self, t: torch.Tensor, offset: int = 0):
         self.nbytes = t.numel() * t.element_size()
-        total = 2 * GUARD_BYTES + ((self.nbytes + 15) // 16) * 16
+        assert offset % t.element_size() == 0 and 0 <= offset < 16
+        self.start = GUARD_BYTES + offset
+        total = 2 * GUARD_BYTES + ((offset + self.nbytes + 15) // 16) * 16
         self.raw = torch.full((total // 4,), GUARD_WORD, dtype=torch.int32, device="cuda")
         u8 = self.raw.view(torch.uint8)
-        self.body = u8[GUARD_BYTES:GUARD_BYTES + self.nbytes].view(t.dtype).view(t.shape)
+        self.body = u8[self.start:self.start + self.nbytes].view(t.dtype).view(t.shape)
         self.body.copy_(t.to("cuda"))
-        self.bands = torch.cat([u8[:GUARD_BYTES], u8[GUARD_BYTES + self.nbytes:]]).clone()
+        self.bands = torch.cat([u8[:self.start], u8[self.start + self.nbytes:]]).clone()
 
     def check(self, what: str) -> None:
         u8 = self.raw.view(torch.uint8)
-        now = torch.cat([u8[:GUARD_BYTES], u8[GUARD_BYTES + self.nbytes:]])
+        now = torch.cat([u8[:self.start], u8[self.start + self.nbytes:]])
         assert torch.equal(now, self.bands), f"{what}: a write landed in the guard band around the tensor"
 
 
-def guarded(t: torch.Tensor, keep: list) -> torch.Tensor:
+def guarded(t: torch.Tensor, keep: list, offset: int = 0) -> torch.Tensor:
     """Device tensor with t's contents inside guard bands; its checker goes to keep."""
-    g = Guarded(t)
+    g = Guarded(t, offset)
     keep.append(g)
     return g.body
 
@@ -124,10 +127,11 @@ class Layer:
     guards: list = field(default_factory=list)
 
     @staticmethod
-    def make(w: I.Workload, gen, wp_cpu: torch.Tensor) -> "Layer":
+    def make(w: I.Workload, gen, wp_cpu: torch.Tensor, ring_g_offset: int = 0) -> "Layer":
         c = I.cache(gen, w, wp_cpu, "cpu")
         g: list = []
-        dev = Bd.Cache(guarded(c.state, g), guarded(c.ring_d, g), guarded(c.ring_k, g), guarded(c.ring_g, g))
+        dev = Bd.Cache(guarded(c.state, g), guarded(c.ring_d, g), guarded(c.ring_k, g),
+                       guarded(c.ring_g, g, ring_g_offset))
         return Layer(w, dev, O.Cache.from_arrays(c.state, c.ring_d, c.ring_k, c.ring_g), c, g)
 
 
@@ -162,17 +166,19 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
                out_dtype=torch.float32, layers: int = 1, tol: Optional[float] = None,
                check_untouched: bool = True, q_scale: float = 1.0, qk_l2norm: bool = False,
                tweak: Optional[Callable[[int, "I.StepInputs"], None]] = None, overlap: bool = False,
-               outputs: Optional[list] = None) -> RunReport:
+               outputs: Optional[list] = None, ring_g_offset: int = 0) -> RunReport:
     """Runs `steps` decode steps of `layers` layers sharing one cursor array
     on both sides and asserts parity after every step.  overlap: every layer
     but the first is launched with STEP_OVERLAP_PREVIOUS (the launch before it
     touches neither its cache nor the cursors).  outputs: if given, receives
-    each step's outputs (float64, [rows, HV, V]) of every layer."""
+    each step's outputs (float64, [rows, HV, V]) of every layer.  ring_g_offset:
+    the g ring starts that many bytes past a 16-byte boundary (the ABI asks
+    only for float alignment there)."""
     steps = w.steps if steps is None else steps
     tol = tolerance(w, recon) if tol is None else tol
     gen = I.generator(w.seed, "cpu")
     wp = I.write_pos(gen, w, "cpu")
-    Ls = [Layer.make(w, gen, wp) for _ in range(layers)]
+    Ls = [Layer.make(w, gen, wp, ring_g_offset) for _ in range(layers)]
     idx = I.indices(gen, w.B, w.N, w.n_pad, "cpu")
     rows = idx.shape[0]
     live = idx.numpy() >= 0

@@ -127,3 +127,18 @@ def test_lossless_tuple_ratio_matches_the_pages():
         return bench.lossless_verify_head_bytes(128, 128, G, 1, 2, 2) - 65536 - inputs - 128 * 2
     assert round(4 * 128 * 128 / tuple_bytes(1), 1) == 63.8
     assert 4 * 128 * 128 / tuple_bytes(2) > 80
+
+
+def test_workload_names_parse():
+    """The named workloads the bench and its profiles use resolve to the shapes
+    their names state."""
+    from linear_attention_decode_gb300.constants import F16, F32, GATE_PER_K
+    w = bench.pick_workload("kda_layer:64:f32")
+    assert (w.L, w.ring_dtype, w.gate, w.B, w.N, w.HV, w.HK) == (64, F32, GATE_PER_K, 128, 256, 32, 32)
+    assert "L=64 fp32 ring" in w.name
+    w = bench.pick_workload("stack30:64")
+    assert (w.B, w.N, w.L, w.ring_dtype, w.layers) == (64, 320, 16, F16, 30)
+    w = bench.pick_workload("sweep:128:32:f32")
+    assert (w.B, w.L, w.ring_dtype) == (128, 32, F32)
+    with pytest.raises(SystemExit):
+        bench.pick_workload("no_such_workload")

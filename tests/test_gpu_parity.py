@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_harness import (TCP, TOL_TC, Layer, decode, desc_of, oracle_geom, recon_and_flags, rel_err, run_parity,
-                         run_sampled)
+from gpu_harness import (TCP, TOL_TC, Layer, decode, desc_of, guarded, oracle_geom, recon_and_flags, rel_err,
+                         run_parity, run_sampled)
 from linear_attention_decode_gb300 import binding as Bd
 from linear_attention_decode_gb300 import inputs as I
 
@@ -66,25 +66,28 @@ def test_longest_ring(recon, ring, gate):
     persistent tensor-core kernel (the first chunk landed by bulk copy, the
     others loaded from the ring directly), each contracted into the same
     accumulator; 70 steps from an empty ring take p through 0 .. 63.  A KDA
-    layer with an fp32 ring keeps too few checkpoint boxes beside its per-channel
-    gates, and there the one-block-per-head tensor-core kernel runs."""
+    layer with an fp32 ring replays in chunks of 8 entries (its landing slots
+    carry the per-channel gates as well), up to eight of them."""
     w = I.Workload("L64", N=3, B=2, HV=2, HK=1 if gate == Bd.GATE_SCALAR else 2, K=128, L=64,
                    ring_dtype=ring, qkv_dtype=Bd.BF16, gate=gate, steps=70, seed=14)
     if recon == TCP:
-        want = Bd.KERNEL_PER_HEAD_TC if (gate == Bd.GATE_PER_K and ring == Bd.F32) else Bd.KERNEL_PERSISTENT_TC
-        assert _kernel_for(w, recon) == want
+        assert _kernel_for(w, recon) == Bd.KERNEL_PERSISTENT_TC
     elif recon == TC:
         assert _kernel_for(w, recon) == Bd.KERNEL_SMALL_BATCH
     rep = run_parity(w, recon)
     assert sum(s.flushes for s in rep.steps) == 2
 
 
-def _kernel_for(w: I.Workload, recon: int) -> int:
+def _kernel_for(w: I.Workload, recon: int, ring_g_offset: int = 0) -> int:
     """The decode kernel the library picks for the workload's shapes (device
-    buffers laid out as the parity harness lays them out)."""
+    buffers laid out as the parity harness lays them out; ring_g_offset as in
+    run_parity)."""
     gen = I.generator(w.seed, "cuda")
     wp = I.write_pos(gen, w, "cuda")
     c = I.cache(gen, w, wp, "cuda")
+    keep: list = []
+    if ring_g_offset:
+        c = I.CacheTensors(c.state, c.ring_d, c.ring_k, guarded(c.ring_g, keep, ring_g_offset))
     idx = I.indices(gen, w.B, w.N, w.n_pad, "cuda")
     si = I.step_inputs(gen, w, "cuda")
     out = torch.empty((idx.shape[0], w.HV, w.V), device="cuda")
@@ -108,17 +111,31 @@ def test_chunked_replay_boundaries(ring, L):
 
 
 @pytest.mark.parametrize("ring", [Bd.F16, Bd.F32], ids=["f16", "f32"])
-@pytest.mark.parametrize("L", [24, 34])
+@pytest.mark.parametrize("L", [10, 24, 34])
 def test_chunked_replay_boundaries_kda(ring, L):
     """The same depths with per-channel gates (KDA: the decays fold onto each
-    chunk's keys).  Where the persistent layout does not fit (a KDA ring of
-    fp32 entries carries K gate floats per entry as well), the per-head
-    tensor-core kernel takes the launch; either must match the oracle."""
+    chunk's keys), on the persistent kernel.  An fp32 KDA ring replays in
+    chunks of 8 entries (p = 7, 8, 9, 15, 16, 17, ... all occur; L = 10 is the
+    shortest ring that chunks); 16-bit rings in chunks of 16 from L = 34."""
     w = I.Workload(f"kda L{L}", N=24, B=12, n_pad=1, HV=4, HK=4, K=128, L=L, ring_dtype=ring,
                    qkv_dtype=Bd.BF16, gate=Bd.GATE_PER_K, steps=L + 4, staggered=True, seed=16)
-    assert _kernel_for(w, TCP) in (Bd.KERNEL_PERSISTENT_TC, Bd.KERNEL_PER_HEAD_TC)
+    assert _kernel_for(w, TCP) == Bd.KERNEL_PERSISTENT_TC
     rep = run_parity(w, TCP)
     assert sum(s.flushes for s in rep.steps) > 0
+
+
+@pytest.mark.parametrize("ring", [Bd.F16, Bd.F32], ids=["f16", "f32"])
+def test_per_head_kernel_on_unaligned_gate_ring(ring):
+    """A KDA g ring that starts 4 bytes past a 16-byte boundary (the ABI asks
+    only for float alignment there) cannot be bulk-copied, so the one-block-
+    per-head tensor-core kernel takes the launch; it must match the oracle
+    with the same guard bands, padding rows and flushes."""
+    w = I.Workload("kda unaligned g", N=24, B=12, n_pad=1, HV=4, HK=4, K=128, L=24, ring_dtype=ring,
+                   qkv_dtype=Bd.BF16, gate=Bd.GATE_PER_K, steps=28, staggered=True, seed=17)
+    assert _kernel_for(w, TCP) == Bd.KERNEL_PERSISTENT_TC
+    assert _kernel_for(w, TCP, ring_g_offset=4) == Bd.KERNEL_PER_HEAD_TC
+    rep = run_parity(w, TCP, ring_g_offset=4)
+    assert sum(s.flushes for s in rep.steps) > 0 and sum(s.appends for s in rep.steps) > 0
 
 
 @pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
