@@ -207,8 +207,9 @@ GDN_API gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gd
  *   GDN_KERNEL_PERSISTENT_TC  persistent warp-specialised tensor-core kernel,
  *                             one block per SM (TENSOR recon)
  *   GDN_KERNEL_PER_HEAD_TC    one block per (row, value head), tensor cores
- *                             (TENSOR recon whose layout does not fit the
- *                             persistent kernel)
+ *                             (TENSOR recon the persistent kernel cannot
+ *                             take, e.g. a KDA g ring not 16-byte aligned,
+ *                             32768 or more value heads, 2^24 or more slots)
  *   GDN_KERNEL_CUDA_CORE      CUDA-core kernel (FFMA or OUTPUT recon)
  *   GDN_KERNEL_SMALL_BATCH    TENSOR recon of a batch with at most 64
  *                             (row, value head) items (unless the step has
