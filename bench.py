@@ -1080,15 +1080,9 @@ def run_ours(args):
     def step(i):
         Bd.gdn_replayssm_decode_advance(desc, cache, wp, None, steps_in[i % POOL], adv_ws, recon, None, None, stream)
 
-    for i in range(args.warmup):
-        step(i)
-        host_advance()
-    torch.cuda.synchronize()
-
     # Untimed legs first (the packed decode beside it and the end-to-end run
-    # through host buffers): they also bring the GPU to its working clocks and
-    # state before the K timed steps, which a short timed region would
-    # otherwise partly spend on.
+    # through host buffers); the W warm-up steps then run right before the
+    # timed region (below), so that it starts on a GPU that has not gone idle.
     K = args.steps
     if not args.kernel_only:
         # in-repo packed decode on the workload's shapes (baseline: reads and writes
@@ -1152,16 +1146,22 @@ def run_ours(args):
             host_advance()
 
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # the cursors follow the advance rule, so every timed launch's bytes are
-    # known up front (no host bookkeeping inside the timed region)
-    total_bytes = 0.0
-    for i in range(K):
-        total_bytes += launch_bytes_now()
-        host_advance()
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    # The clock sampler starts before the warm-up: a GPU left idle for a few
+    # hundred milliseconds (as while the sampler starts) pays over 100 us more
+    # on its next launch, which would otherwise land in the timed region.
     with ClockSampler(local) as clocks:
+        for i in range(args.warmup):
+            step(i)
+            host_advance()
+        # the cursors follow the advance rule, so every timed launch's bytes
+        # are known up front (no host bookkeeping inside the timed region)
+        total_bytes = 0.0
+        for i in range(K):
+            total_bytes += launch_bytes_now()
+            host_advance()
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         # one kernel per step and nothing else between launches, so the
         # kernel's average launch duration is the elapsed time over K (events
         # between launches would also cut the overlap of one launch's set-up
