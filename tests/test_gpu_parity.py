@@ -395,6 +395,16 @@ def test_full_size_sampled_long_fp32_ring():
     run_sampled(w, TC, steps=3)
 
 
+def test_full_size_sampled_kda_long_fp32_ring():
+    """The KDA layer (B = 128, HV = HK = 32, K = V = 128) with an fp32 ring at
+    L = 64, the launch `bench.py --workload kda_layer:64:f32` times: up to eight
+    8-entry replay chunks per item on the persistent kernel; sampled rows."""
+    import bench
+    w = bench.pick_workload("kda_layer:64:f32")
+    assert _kernel_for(w, TC) == Bd.KERNEL_PERSISTENT_TC
+    run_sampled(w, TC, steps=3)
+
+
 @pytest.mark.parametrize("B,ring,kernel", [(1, Bd.F16, Bd.KERNEL_SMALL_BATCH), (2, Bd.F32, Bd.KERNEL_SMALL_BATCH),
                                            (8, Bd.F16, Bd.KERNEL_PERSISTENT_TC)],
                          ids=["B1_f16", "B2_f32", "B8_f16"])
