@@ -166,14 +166,16 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
                out_dtype=torch.float32, layers: int = 1, tol: Optional[float] = None,
                check_untouched: bool = True, q_scale: float = 1.0, qk_l2norm: bool = False,
                tweak: Optional[Callable[[int, "I.StepInputs"], None]] = None, overlap: bool = False,
-               outputs: Optional[list] = None, ring_g_offset: int = 0) -> RunReport:
+               outputs: Optional[list] = None, ring_g_offset: int = 0, qkv_offset: int = 0) -> RunReport:
     """Runs `steps` decode steps of `layers` layers sharing one cursor array
     on both sides and asserts parity after every step.  overlap: every layer
     but the first is launched with STEP_OVERLAP_PREVIOUS (the launch before it
     touches neither its cache nor the cursors).  outputs: if given, receives
     each step's outputs (float64, [rows, HV, V]) of every layer.  ring_g_offset:
     the g ring starts that many bytes past a 16-byte boundary (the ABI asks
-    only for float alignment there)."""
+    only for float alignment there).  qkv_offset: mixed_qkv is a view that
+    starts that many elements into a wider buffer (rows neither 16-byte aligned
+    nor a multiple of 16 bytes apart)."""
     steps = w.steps if steps is None else steps
     tol = tolerance(w, recon) if tol is None else tol
     gen = I.generator(w.seed, "cpu")
@@ -203,7 +205,13 @@ def run_parity(w: I.Workload, recon: int, steps: Optional[int] = None,
             step_guards: list = []
             out = guarded(torch.full((rows, w.HV, w.V), float("nan"), dtype=out_dtype), step_guards)
             flags = Bd.STEP_OVERLAP_PREVIOUS if (overlap and li > 0) else 0
-            step = Bd.Step(guarded(si.mixed_qkv, step_guards), guarded(si.g, step_guards),
+            qkv = guarded(si.mixed_qkv, step_guards)
+            if qkv_offset:
+                row = si.mixed_qkv.shape[1]
+                wide = torch.zeros((rows, row + qkv_offset + 6), dtype=si.mixed_qkv.dtype)
+                wide[:, qkv_offset:qkv_offset + row] = si.mixed_qkv
+                qkv = guarded(wide, step_guards)[:, qkv_offset:qkv_offset + row]
+            step = Bd.Step(qkv, guarded(si.g, step_guards),
                            guarded(si.beta, step_guards), idx_dev, out, q_scale=q_scale, qk_l2norm=qk_l2norm,
                            flags=flags)
             decode(desc, layer.dev, wp_dev, ff_dev, step, recon, flushed, status)

@@ -160,6 +160,23 @@ def test_two_layers_second_overlaps_previous(recon):
     assert sum(s.flushes for s in rep.steps) > 0
 
 
+def test_two_layers_kda_second_overlaps_previous():
+    """The same with per-channel gates (KDA), on the persistent kernel."""
+    rep = run_parity(I.with_(KDA_SMALL, steps=18), TCP, layers=2, overlap=True)
+    assert sum(s.flushes for s in rep.steps) > 0
+
+
+@pytest.mark.parametrize("recon", [FF, TC, TCP, OUT], ids=["ffma", "tensor", "tensor_persistent", "output"])
+@pytest.mark.parametrize("l2norm", [False, True], ids=["raw", "l2norm"])
+def test_unaligned_qkv_rows(recon, l2norm):
+    """mixed_qkv one element into a wider buffer: its rows start off any 16-byte
+    boundary and lie an odd number of elements apart, so the persistent kernel
+    loads q, k and v per thread instead of by bulk copy (the ABI asks only for
+    element alignment there)."""
+    rep = run_parity(I.with_(RAGGED, steps=12), recon, qkv_offset=1, qk_l2norm=l2norm, q_scale=0.75)
+    assert sum(s.flushes for s in rep.steps) > 0
+
+
 def test_bf16_output():
     # bf16 rounding of the output alone can be 2^-8 relative: one bf16 ulp on top of the bound
     run_parity(I.with_(RAGGED, steps=10), TC, out_dtype=torch.bfloat16, tol=TOL_TC + 2.0 ** -8)
