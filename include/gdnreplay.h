@@ -164,9 +164,10 @@ typedef struct {
 #define GDN_STEP_OVERLAP_PREVIOUS 1u
 /* GDN_STEP_PERSISTENT_KERNEL: with GDN_RECON_TENSOR, always run the
  *   persistent tensor-core kernel.  By default a batch of at most 64
- *   (row, value head) items runs the small-batch kernel instead (see
- *   gdn_replayssm_decode_kernel); this flag keeps the tensor-core arithmetic at
- *   any batch size.  Ignored by the other recon modes. */
+ *   (row, value head) items runs the small-batch kernel instead, and a layer
+ *   with ring_len 1 the CUDA-core kernel (see gdn_replayssm_decode_kernel);
+ *   this flag keeps the tensor-core kernel at any batch size and ring length.
+ *   Ignored by the other recon modes. */
 #define GDN_STEP_PERSISTENT_KERNEL 2u
 #define GDN_STEP_KNOWN_FLAGS      3u
 
@@ -210,7 +211,11 @@ GDN_API gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gd
  *                             (TENSOR recon the persistent kernel cannot
  *                             take, e.g. a KDA g ring not 16-byte aligned,
  *                             32768 or more value heads, 2^24 or more slots)
- *   GDN_KERNEL_CUDA_CORE      CUDA-core kernel (FFMA or OUTPUT recon)
+ *   GDN_KERNEL_CUDA_CORE      CUDA-core kernel (FFMA or OUTPUT recon; also
+ *                             TENSOR recon at ring_len 1 without
+ *                             GDN_STEP_PERSISTENT_KERNEL: the ring is empty
+ *                             and the decode is the packed decode's
+ *                             read-modify-write, [P1] Design 1)
  *   GDN_KERNEL_SMALL_BATCH    TENSOR recon of a batch with at most 64
  *                             (row, value head) items (unless the step has
  *                             GDN_STEP_PERSISTENT_KERNEL): one block per (row,

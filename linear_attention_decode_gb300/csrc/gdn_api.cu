@@ -137,6 +137,16 @@ gdn_status_t gdn_packed_decode(const gdn_layer_desc_t *desc, float *state, const
   return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_packed_decode launch");
 }
 
+// L = 1: there is no ring, every live row flushes, and the replay contraction
+// is empty, so the decode is the packed decode ([P1] Design 1).  A tensor-core call then
+// runs the CUDA-core replay kernel, which at L = 1 is the packed decode's
+// read-modify-write with the replay's row checks, flush flags and status: the
+// persistent tensor-core kernel would move the same bytes with its per-launch
+// set-up on top.  GDN_STEP_PERSISTENT_KERNEL still forces the persistent kernel.
+static bool tensor_recon_is_empty(const gdn_layer_desc_t *desc, const gdn_step_t *step) {
+  return desc->ring_len == 1 && !(step->flags & GDN_STEP_PERSISTENT_KERNEL);
+}
+
 gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gdn_layer_cache_t *cache,
                                   const int32_t *write_pos, const uint8_t *force_flush,
                                   const gdn_step_t *step, int32_t recon, uint8_t *flushed_out,
@@ -160,7 +170,7 @@ gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gdn_layer_
   P.flushed = flushed_out;
   P.status = dev_status;
   cudaError_t e;
-  if (recon == GDN_RECON_FFMA) {
+  if (recon == GDN_RECON_FFMA || (recon == GDN_RECON_TENSOR && tensor_recon_is_empty(desc, step))) {
     e = gdn::launch_ffma_decode(P, desc->k_dim, desc->gate, true, (cudaStream_t)stream);
   } else if (recon == GDN_RECON_OUTPUT) {
     e = gdn::launch_output_only_decode(P, desc->k_dim, desc->gate, (cudaStream_t)stream);
@@ -182,7 +192,7 @@ gdn_status_t gdn_replayssm_decode_kernel(const gdn_layer_desc_t *desc, const gdn
   if (!kernel) return fail(GDN_ERR_INVALID_ARG, "kernel is NULL");
   if (recon != GDN_RECON_TENSOR && recon != GDN_RECON_FFMA && recon != GDN_RECON_OUTPUT)
     return fail(GDN_ERR_INVALID_ARG, "recon must be GDN_RECON_TENSOR, GDN_RECON_FFMA or GDN_RECON_OUTPUT");
-  if (recon != GDN_RECON_TENSOR) {
+  if (recon != GDN_RECON_TENSOR || tensor_recon_is_empty(desc, step)) {
     *kernel = GDN_KERNEL_CUDA_CORE;
     return GDN_OK;
   }
@@ -225,7 +235,10 @@ gdn_status_t gdn_replayssm_decode_advance(const gdn_layer_desc_t *desc, const gd
   P.status = dev_status;
   cudaError_t e;
   bool fused = false;
-  if (recon == GDN_RECON_FFMA) {
+  if (recon == GDN_RECON_TENSOR && tensor_recon_is_empty(desc, step)) {
+    e = gdn::launch_ffma_decode(P, desc->k_dim, desc->gate, true, (cudaStream_t)stream);
+    fused = true;  // L = 1: a valid cursor is 0 and stays 0 (every live row flushes), so no advance is due
+  } else if (recon == GDN_RECON_FFMA) {
     e = gdn::launch_ffma_decode(P, desc->k_dim, desc->gate, true, (cudaStream_t)stream);
   } else if (recon == GDN_RECON_OUTPUT) {
     e = gdn::launch_output_only_decode(P, desc->k_dim, desc->gate, (cudaStream_t)stream);

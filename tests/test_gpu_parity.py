@@ -266,10 +266,14 @@ def test_l1_replay_is_packed_decode_bitwise():
     assert torch.all(wp == 0)
 
 
-@pytest.mark.parametrize("recon", [TC, TCP], ids=["small_batch", "persistent"])
+@pytest.mark.parametrize("recon", [TC, TCP], ids=["default", "persistent"])
 def test_l1_tensor_path_matches_packed(recon):
+    """L = 1: a tensor-core call runs the CUDA-core replay kernel (the ring is
+    empty, so the decode is the packed decode: identical bits) unless the step
+    asks for the persistent tensor-core kernel (then within 1e-5)."""
     w = I.Workload("L1", N=6, B=4, HV=8, HK=4, K=128, L=1, ring_dtype=Bd.F16, qkv_dtype=Bd.BF16,
                    steps=4, seed=16)
+    assert _kernel_for(w, recon) == (Bd.KERNEL_CUDA_CORE if recon == TC else Bd.KERNEL_PERSISTENT_TC)
     gen = I.generator(w.seed, "cpu")
     S0 = I.state(gen, w.N, w.HV, w.V, w.K, "cpu").cuda()
     idx = I.indices(gen, w.B, w.N, 0, "cpu").cuda()
@@ -282,6 +286,8 @@ def test_l1_tensor_path_matches_packed(recon):
         ob = torch.empty_like(oa)
         decode(d, Bd.Cache(sa), wp, None, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, oa), recon)
         Bd.gdn_packed_decode(d, sb, Bd.Step(si.mixed_qkv, si.g, si.beta, idx, ob))
+        if recon == TC:
+            assert torch.equal(oa, ob) and torch.equal(sa, sb)
         assert rel_err(oa.cpu().numpy(), ob.cpu().numpy()) <= 1e-5
         assert rel_err(sa.cpu().numpy(), sb.cpu().numpy()) <= 1e-5
 
