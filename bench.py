@@ -1150,15 +1150,17 @@ def run_ours(args):
     # hundred milliseconds (as while the sampler starts) pays over 100 us more
     # on its next launch, which would otherwise land in the timed region.
     with ClockSampler(local) as clocks:
-        for i in range(args.warmup):
-            step(i)
-            host_advance()
         # the cursors follow the advance rule, so every timed launch's bytes
-        # are known up front (no host bookkeeping inside the timed region)
+        # are known up front; the host does this bookkeeping before the warm-up
+        # launches, which then run right before the timed region (no idle gap)
+        for i in range(args.warmup):
+            host_advance()
         total_bytes = 0.0
         for i in range(K):
             total_bytes += launch_bytes_now()
             host_advance()
+        for i in range(args.warmup):
+            step(i)
         if ws > 1:
             dist.barrier()
         torch.cuda.synchronize()
