@@ -460,22 +460,32 @@ def measure_replay(w, K, warmup, recon, dev, layers=1, overlap=False, extra_flag
     wp_h = wp.cpu().numpy().copy()
     ob = 2
 
+    # every call checked and packed once (prepared calls), as a serving loop
+    # would: small batches then time the launches, not the Python marshalling
+    calls = []
+    for j in range(len(steps_in)):
+        si = steps_in[j]
+        so = steps_ov[j] if overlap else si
+        row = [Bd.prepare_replayssm_decode(desc, caches[layer], wp, None, si if layer == 0 else so, recon)
+               for layer in range(layers - 1)]
+        row.append(Bd.prepare_replayssm_decode(desc, caches[-1], wp, None, si if layers == 1 else so, recon, adv_ws))
+        calls.append(row)
+    h = stream.cuda_stream
+
     def step(i):
-        si = steps_in[i % len(steps_in)]
-        so = steps_ov[i % len(steps_ov)] if overlap else si
-        for layer in range(layers - 1):
-            Bd.gdn_replayssm_decode(desc, caches[layer], wp, None, si if layer == 0 else so, recon, None, None,
-                                    stream)
-        Bd.gdn_replayssm_decode_advance(desc, caches[-1], wp, None, si if layers == 1 else so, adv_ws, recon,
-                                        None, None, stream)
+        for c in calls[i % len(calls)]:
+            c.run(h)
 
     def host_advance():
         live = idx_h[idx_h >= 0]
         p = wp_h[live]
         wp_h[live] = np.where(p == w.L - 1, 0, p + 1)
 
+    # host bookkeeping (the warm-up steps' cursor moves, then every timed
+    # launch's bytes) before the warm-up launches, which then run right before
+    # the timed region: a GPU left idle even for milliseconds pays extra on its
+    # next launch
     for i in range(warmup):
-        step(i)
         host_advance()
     total = 0.0
     for i in range(K):
@@ -484,6 +494,8 @@ def measure_replay(w, K, warmup, recon, dev, layers=1, overlap=False, extra_flag
         per_layer = launch_bytes(w, p, p == w.L - 1, ob, int((idx_h < 0).sum()), cursors=False)
         total += layers * per_layer + 8 * len(live)
         host_advance()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -534,13 +546,15 @@ def measure_packed(w, K, dev):
     out = torch.empty((rows, w.HV, w.V), dtype=torch.bfloat16, device=dev)
     steps = [Bd.Step(si.mixed_qkv, si.g, si.beta, idx, out) for idx in sets]
     stream = torch.cuda.current_stream()
+    calls = [Bd.prepare_packed_decode(desc, st, stp) for stp in steps]  # as the replay side: prepared calls
+    h = stream.cuda_stream
     for i in range(8):
-        Bd.gdn_packed_decode(desc, st, steps[i % 4], None, stream)
+        calls[i % 4].run(h)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for i in range(K):
-        Bd.gdn_packed_decode(desc, st, steps[i % 4], None, stream)
+        calls[i % 4].run(h)
     b.record(stream)
     torch.cuda.synchronize()
     s = a.elapsed_time(b) / 1e3 / K

@@ -164,7 +164,8 @@ typedef struct {
 #define GDN_STEP_OVERLAP_PREVIOUS 1u
 /* GDN_STEP_PERSISTENT_KERNEL: with GDN_RECON_TENSOR, always run the
  *   persistent tensor-core kernel.  By default a batch of at most 64
- *   (row, value head) items runs the small-batch kernel instead, and a layer
+ *   (row, value head) items (a GDN layer: up to 256 items while items x
+ *   ring_len <= 2048) runs the small-batch kernel instead, and a layer
  *   with ring_len 1 the CUDA-core kernel (see gdn_replayssm_decode_kernel);
  *   this flag keeps the tensor-core kernel at any batch size and ring length.
  *   Ignored by the other recon modes. */
@@ -217,9 +218,11 @@ GDN_API gdn_status_t gdn_replayssm_decode(const gdn_layer_desc_t *desc, const gd
  *                             and the decode is the packed decode's
  *                             read-modify-write, [P1] Design 1)
  *   GDN_KERNEL_SMALL_BATCH    TENSOR recon of a batch with at most 64
- *                             (row, value head) items (unless the step has
+ *                             (row, value head) items, or a GDN layer's batch
+ *                             of at most 256 with items x ring_len <= 2048
+ *                             (unless the step has
  *                             GDN_STEP_PERSISTENT_KERNEL): one block per (row,
- *                             value head, 16 state rows), every block on its
+ *                             value head, slice of 16 to 128 state rows), every block on its
  *                             rows' whole step, replay sum in fp32 on the CUDA
  *                             cores (so within the FFMA bound), so that a
  *                             small batch still spreads over every SM

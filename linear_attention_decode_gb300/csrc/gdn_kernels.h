@@ -29,11 +29,13 @@ cudaError_t launch_tcp_decode(const DecodeParams &P, int D, int gate, const CUte
 // Whether launch_tcp_decode would take this launch (host-side, launches nothing).
 bool tcp_decode_fits(const DecodeParams &P, int D, int gate);
 
-// Small-batch decode (one block per (row, value head, 16 state rows), CUDA
-// cores): taken by the tensor-core recon when the batch has at most
-// kSlabMaxItems (row, value head) items, unless P.persistent_only (measured
-// under CUDA-graph replay, HV = 32: it beats the persistent kernel up to B = 2
-// and loses from B = 8 on, where the CUDA-core replay sum becomes the cost).
+// Small-batch decode (one block per (row, value head, slice of state rows),
+// CUDA cores): taken by the tensor-core recon when the batch has at most
+// kSlabMaxItems (row, value head) items, or, for a GDN layer, at most
+// 4 kSlabMaxItems items with items x L <= 32 kSlabMaxItems, unless
+// P.persistent_only (measured, HV = 32: it beats the persistent kernel up to
+// B = 2 at any ring length and at B = 4 and 8 with short rings; past that its
+// CUDA-core replay sum becomes the cost).
 constexpr int kSlabMaxItems = 64;
 bool slab_decode_takes(const DecodeParams &P, int gate);
 cudaError_t launch_slab_decode(const DecodeParams &P, int D, int gate, cudaStream_t s);

@@ -392,7 +392,15 @@ static int slab_count(const DecodeParams &P, int D) {
 bool slab_decode_takes(const DecodeParams &P, int gate) {
   // the bulk copies of a KDA layer's gates start on 16 bytes
   if (gate == GDN_GATE_PER_K && P.L > 1 && (reinterpret_cast<uintptr_t>(P.ring_g) & 15u) != 0) return false;
-  return !P.persistent_only && (int64_t)P.B * P.HV <= kSlabMaxItems;
+  if (P.persistent_only) return false;
+  const int64_t items = (int64_t)P.B * P.HV;
+  if (items <= kSlabMaxItems) return true;
+  // A GDN layer with a short ring: up to 256 items this kernel's CUDA-core
+  // replay (p ring entries per state element) still costs less than the
+  // persistent kernel's per-launch set-up while items x L stays at or below
+  // 2048 (at 32 value heads: B = 4 up to L = 16, B = 8 up to L = 8; measured
+  // B = 4, L = 4: 6.9 against 10.5 us; B = 8, L = 4: 9.1 against 11.6 us).
+  return gate == GDN_GATE_SCALAR && items <= 4 * kSlabMaxItems && items * P.L <= 32 * kSlabMaxItems;
 }
 
 template <int D, int GATE, int RING_DT>
