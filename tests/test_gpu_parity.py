@@ -440,6 +440,29 @@ def test_full_size_sampled_small_batches(B, ring, kernel):
     run_sampled(w, TC, steps=4)
 
 
+@pytest.mark.parametrize("B,L,ring", [(4, 8, Bd.F16), (8, 4, Bd.F32), (8, 8, Bd.F16)],
+                         ids=["B4_L8_f16", "B8_L4_f32", "B8_L8_f16"])
+def test_full_size_sampled_small_batch_wide_slices(B, L, ring):
+    """GDN batches of 128 and 256 (row, head) items with short rings run the
+    small-batch kernel with slices of 32 and 64 state rows; sampled rows
+    against the oracle over two ring cycles."""
+    w = I.sweep_point(B, L, ring)
+    assert _kernel_for(w, TC) == Bd.KERNEL_SMALL_BATCH
+    run_sampled(w, TC, steps=2 * L)
+
+
+@pytest.mark.parametrize("B,L", [(3, 4), (7, 8)], ids=["128_items_L4", "256_items_L8"])
+def test_small_batch_wide_slices_every_row(B, L):
+    """The same kernel with 32- and 64-row slices (one padding row besides the
+    B live ones: 128 and 256 items) checked on every row, padding rows and
+    flushes included (32 value heads, a small slot pool)."""
+    w = I.Workload(f"wide slices B{B}", N=2 * B + 4, B=B, n_pad=1, HV=32, HK=16, K=128, L=L,
+                   ring_dtype=Bd.F16, qkv_dtype=Bd.BF16, steps=2 * L + 2, staggered=True, seed=18)
+    assert _kernel_for(w, TC) == Bd.KERNEL_SMALL_BATCH
+    rep = run_parity(w, TC)
+    assert sum(s.flushes for s in rep.steps) > 0 and sum(s.appends for s in rep.steps) > 0
+
+
 def test_full_size_sampled_output_only():
     """The output-only readout at the benchmark's layer size, sampled rows."""
     run_sampled(I.HEADLINE, OUT, steps=3)
